@@ -1,0 +1,417 @@
+"""Benchmark of the draft-sampling / verification hot path on GB300.
+
+One step = the whole path over one batch: dspark_q_build (dyadic24 q from
+the draft logits), dspark_draft_sample, and the verification modes of the
+workload (dspark_verify_greedy and/or dspark_verify_ratio).  Default workload:
+C4 -- B = 256 requests, depth 5, V = 129,280, fp32 draft / bf16 target logits,
+Zipf rows with 10 % grammar masks and 1 % tied-remainder rows, dense q,
+greedy and ratio verification (every step of the path but the top-k support,
+which `--workload c3` covers).
+
+Prints ONE JSON line (rank 0):
+  value   verify rows/s (B x 6 rows per step) with inputs resident in HBM,
+          device time from CUDA events on the launching stream;
+  e2e     the same metric through the same C-ABI calls with pinned host
+          buffers: H2D of the step's logits and D2H of its results inside the
+          timed region;
+  roofline  the dominant kernel's algorithmic bytes per launch / its mean
+          CUDA-event duration, against the measured HBM copy bandwidth;
+  cpu_baseline  the CPU oracle timed on a bounded sample of the workload.
+`--impl reference` times the CPU oracle itself as the reference arm.
+Multi-GPU (torchrun): every rank runs its own B requests (request ids offset
+by rank), no collective on the data path; the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+CONFIG_NAMES = {"c1": "configs[0]", "c2": "configs[1]", "c3": "configs[2]", "c4": "configs[3]",
+                "c5": "configs[4]"}
+METRIC = "verify rows/s at V=129280 (B x 6 rows)"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="c4")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+def load_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        return None
+
+
+# --------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.path = os.path.join("/tmp", "dspark_clocks_%d_%d.csv" % (os.getpid(), device_index))
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------ our arm
+def algorithmic_bytes(wl, acc_greedy, acc_ratio):
+    """Bytes each kernel must move per launch (what the method reads/writes)."""
+    R_d = wl.B * wl.depth
+    V = wl.V
+    esz_t = 4 if wl.target_dtype == "f32" else 2
+    if wl.top_k > 0:
+        q_bytes = R_d * V * 4 + R_d * (wl.top_k * 8 + 4)
+        sample_bytes = R_d * (wl.top_k * 8 + 4)
+        q_row = wl.top_k * 8 + 4
+    else:
+        q_bytes = R_d * V * 4 * 2
+        sample_bytes = R_d * V * 4
+        q_row = V * 4
+    out = {"q_build": q_bytes, "draft_sample": sample_bytes}
+    if acc_greedy is not None:
+        out["verify_greedy"] = int(((acc_greedy + 1) * V * esz_t).sum())
+    if acc_ratio is not None:
+        rows = ((acc_ratio + 1) * V * esz_t).sum()
+        resid = (acc_ratio < wl.depth).sum() * q_row
+        out["verify_ratio"] = int(rows + resid)
+    return out
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import draft_sampling_verification_gb300 as ds
+    from draft_sampling_verification_gb300 import build as dsbuild
+    from draft_sampling_verification_gb300 import workloads as W
+
+    dsbuild.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = W.by_name(args.workload)
+    B, depth, V = wl.B, wl.depth, wl.V
+    req_np = (wl.request_ids + np.uint32(rank * B)).astype(np.uint32)
+
+    # inputs resident in HBM
+    xd = torch.from_numpy(wl.draft).to(dev)
+    if wl.target_dtype == "f32":
+        xt = torch.from_numpy(wl.target).to(dev)
+    else:
+        xt = torch.from_numpy(wl.target.view(np.int16)).to(dev).view(torch.bfloat16)
+    temps = torch.from_numpy(wl.temperature).to(dev)
+    req = torch.from_numpy(req_np.view(np.int32)).to(dev)
+    rows_d = B * depth
+    top_k = wl.top_k
+    if top_k > 0:
+        counts = torch.empty((rows_d, top_k), dtype=torch.int32, device=dev)
+        ids = torch.empty((rows_d, top_k), dtype=torch.int32, device=dev)
+        nnz = torch.empty((rows_d,), dtype=torch.int32, device=dev)
+    else:
+        counts = torch.empty((rows_d, V), dtype=torch.int32, device=dev)
+        ids = nnz = None
+    qst = torch.empty((rows_d,), dtype=torch.int32, device=dev)
+    tok = torch.empty((B, depth), dtype=torch.int32, device=dev)
+    sst = torch.empty((B, depth), dtype=torch.int32, device=dev)
+    outs = {m: (torch.empty(B, dtype=torch.int32, device=dev),
+                torch.empty((B, depth + 1), dtype=torch.int32, device=dev),
+                torch.empty(B, dtype=torch.int32, device=dev),
+                torch.empty(B, dtype=torch.int32, device=dev)) for m in wl.modes}
+    stream = torch.cuda.current_stream(dev)
+    kernels = ["q_build", "draft_sample"] + ["verify_" + m for m in wl.modes]
+
+    def step(x_d, x_t, marks=None):
+        if marks:
+            marks[0].record(stream)
+        ds.dspark_q_build(x_d, temps, top_k, counts, ids, nnz, qst, stream)
+        if marks:
+            marks[1].record(stream)
+        ds.dspark_draft_sample(counts, ids, nnz, top_k, B, depth, V, wl.seed, req, tok, sst,
+                               stream)
+        k = 2
+        if marks:
+            marks[k].record(stream)
+        for m in wl.modes:
+            a, c, f, s = outs[m]
+            if m == "greedy":
+                ds.dspark_verify_greedy(x_t, B, depth, tok, a, c, s, stream)
+            else:
+                ds.dspark_verify_ratio(x_t, B, depth, tok, counts, ids, nnz, top_k, wl.seed, req,
+                                       a, c, f, s, stream)
+            k += 1
+            if marks:
+                marks[k].record(stream)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        step(xd, xt)
+    torch.cuda.synchronize()
+    assert int((qst != 0).sum()) == 0 and int((sst != 0).sum()) == 0, "refused rows in bench"
+    for m in wl.modes:
+        assert int((outs[m][3] != 0).sum()) == 0, "refused requests in bench"
+    acc = {m: outs[m][0].cpu().numpy() for m in wl.modes}
+    abytes = algorithmic_bytes(wl, acc.get("greedy"), acc.get("ratio"))
+
+    # ---- device-timed region (inputs resident)
+    clocks = ClockSampler(local_rank)
+    nmarks = len(kernels) + 1
+    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(nmarks)]
+             for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for s in range(args.steps):
+        step(xd, xt, marks[s])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clock_info = clocks.stop()
+    barrier()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    per_kernel = {k: 0.0 for k in kernels}
+    for s in range(args.steps):
+        for i, k in enumerate(kernels):
+            per_kernel[k] += marks[s][i].elapsed_time(marks[s][i + 1])
+    per_kernel = {k: v / args.steps for k, v in per_kernel.items()}
+
+    # ---- end to end: pinned host buffers, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        h_d = torch.from_numpy(wl.draft).pin_memory()
+        h_t = (torch.from_numpy(wl.target) if wl.target_dtype == "f32"
+               else torch.from_numpy(wl.target.view(np.int16))).pin_memory()
+        d_d = torch.empty_like(xd)
+        d_t = torch.empty(xt.shape, dtype=xt.dtype, device=dev)
+        d_t_raw = d_t if wl.target_dtype == "f32" else d_t.view(torch.int16)
+        res_shapes = [(B,), (B, depth + 1), (B,)]
+        h_res = {m: [torch.empty(s, dtype=torch.int32).pin_memory() for s in res_shapes]
+                 for m in wl.modes}
+        h_tok = torch.empty((B, depth), dtype=torch.int32).pin_memory()
+
+        def e2e_step():
+            d_d.copy_(h_d, non_blocking=True)
+            d_t_raw.copy_(h_t, non_blocking=True)
+            step(d_d, d_t)
+            h_tok.copy_(tok, non_blocking=True)
+            for m in wl.modes:
+                a, c, f, s = outs[m]
+                h_res[m][0].copy_(a, non_blocking=True)
+                h_res[m][1].copy_(c, non_blocking=True)
+                h_res[m][2].copy_(s, non_blocking=True)
+
+        for _ in range(max(1, args.warmup // 2)):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / args.steps
+        h2d = h_d.numel() * h_d.element_size() + h_t.numel() * h_t.element_size()
+        d2h = h_tok.numel() * 4 + sum(t.numel() * 4 for m in wl.modes for t in h_res[m])
+        e2e = {"ms_per_step": e2e_ms, "h2d": h2d, "d2h": d2h}
+
+    ms = elapsed_ms / args.steps
+    if world > 1:
+        t = torch.tensor([ms, e2e["ms_per_step"] if e2e else 0.0], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, e2e_max = float(t[0]), float(t[1])
+        if e2e:
+            e2e["ms_per_step"] = e2e_max
+    return wl, ms, per_kernel, abytes, clock_info, e2e
+
+
+# ------------------------------------------------------------ CPU oracle
+def oracle_sample_run(wl, n_req, budget_s):
+    """Runs the oracle over up to n_req requests of the workload within about
+    budget_s seconds; returns (requests done, seconds)."""
+    from oracle import oracle as O
+    O.build()
+    V, depth = wl.V, wl.depth
+    done = 0
+    t0 = time.perf_counter()
+    for b in range(min(n_req, wl.B)):
+        x = wl.draft[b]
+        counts, ids, nnz, st = O.q_build(x, wl.temperature[b * depth:(b + 1) * depth], wl.top_k)
+        tok, sst = O.draft_sample(counts, ids, nnz, wl.top_k, 1, depth, wl.seed,
+                                  wl.request_ids[b:b + 1], V=V)
+        z = wl.target_f32()[b:b + 1]
+        drafts = tok.reshape(1, depth)
+        for m in wl.modes:
+            if m == "greedy":
+                O.verify_greedy(z, drafts)
+            else:
+                O.verify_ratio(z, drafts, counts, ids, nnz, wl.top_k, wl.seed,
+                               wl.request_ids[b:b + 1])
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    return done, time.perf_counter() - t0
+
+
+def cpu_baseline(wl, budget_s):
+    n, secs = oracle_sample_run(wl, wl.B, budget_s)
+    rows = n * (wl.depth + 1)
+    return {"value": rows / secs, "unit": "verify rows/s", "cores": 1, "kind": "oracle",
+            "sample": "%d of %d requests of the same workload (q build, draft sample, %s "
+                      "verification), single thread, %.1f s" % (n, wl.B, "+".join(wl.modes),
+                                                                secs)}
+
+
+def run_reference(args, rank, world):
+    from draft_sampling_verification_gb300 import workloads as W
+    if rank != 0:
+        return
+    wl = W.by_name(args.workload)
+    per_step = max(1, min(wl.B, 2))
+    for _ in range(args.warmup):
+        oracle_sample_run(wl, per_step, 1e9)
+    t0 = time.perf_counter()
+    done = 0
+    for _ in range(args.steps):
+        n, _ = oracle_sample_run(wl, per_step, 1e9)
+        done += n
+    secs = time.perf_counter() - t0
+    value = done * (wl.depth + 1) / secs
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "verify rows/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": secs * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64+u64", "data": "synthetic (seeded generators)",
+        "config": {"workload": "%s (%s)" % (wl.name, CONFIG_NAMES.get(args.workload[:2], "")),
+                   "sample_per_step": "%d of %d requests" % (per_step, wl.B)},
+        "cpu_baseline": {"value": value, "unit": "verify rows/s", "cores": 1, "kind": "oracle",
+                         "sample": "%d requests per step of %s" % (per_step, wl.name)},
+        "e2e": {"value": value, "unit": "verify rows/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    import torch
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    wl, ms, per_kernel, abytes, clocks, e2e = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        peaks = load_peaks()
+        rows = wl.B * (wl.depth + 1) * world
+        value = rows / (ms * 1e-3)
+        dom = max(per_kernel, key=per_kernel.get)
+        achieved = abytes[dom] / (per_kernel[dom] * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"] if peaks else 6800.0
+        step_bytes = sum(abytes.values())
+        line = {
+            "metric": METRIC, "value": value, "unit": "verify rows/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32+u64", "data": "synthetic (seeded generators)",
+            "config": {
+                "workload": "%s (%s)" % (wl.name, CONFIG_NAMES.get(args.workload[:2], "")),
+                "B_per_gpu": wl.B, "depth": wl.depth, "V": wl.V, "q": "top-%d" % wl.top_k
+                if wl.top_k else "dense", "verify": list(wl.modes),
+                "parallelism": "dp%d (independent requests)" % world,
+                "l2": "inputs larger than L2 (%.2f GB per step)" % (
+                    (wl.draft.nbytes + wl.target.nbytes) / 1e9),
+                "draft_positions_per_s": wl.B * wl.depth * world / (ms * 1e-3),
+                "step_algorithmic_bytes": step_bytes,
+                "step_achieved_gbs": step_bytes / (ms * 1e-3) / 1e9,
+                "kernel_ms": {k: round(v, 4) for k, v in per_kernel.items()},
+                "kernel_algorithmic_bytes": abytes,
+            },
+            "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+                         "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                         "peak_source": "measured" if peaks else "fallback"},
+            "clocks": clocks,
+            "gpu_launches": len(per_kernel) * args.steps,
+        }
+        if e2e:
+            line["e2e"] = {"value": rows / (e2e["ms_per_step"] * 1e-3), "unit": "verify rows/s",
+                           "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                           "ms_per_step": e2e["ms_per_step"]}
+        if not args.no_cpu:
+            line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

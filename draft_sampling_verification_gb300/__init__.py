@@ -1,0 +1,190 @@
+"""GB300 draft sampling and verification (dyadic24-standard-v1).
+
+Thin Python binding of the C ABI in ``include/dspark.h``: the functions named
+like the C calls (``dspark_q_build``, ``dspark_draft_sample``,
+``dspark_verify_greedy``, ``dspark_verify_ratio``, ``dspark_target_probs``)
+take torch CUDA tensors, pass their device pointers, sizes and the current
+stream to libdspark.so, and raise on a nonzero return.  Every step of the
+path runs in the library's CUDA kernels; torch only provides device memory
+and streams.  The lower-case helpers (``q_build`` ...) allocate the outputs
+with torch and call the same entry points.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+
+M = 1 << 24
+F32, BF16 = 0, 1
+ST_OK, ST_NONFINITE, ST_ZERO_MASS, ST_ALLOC_INCONSISTENT = 0, 1, 2, 3
+ST_BAD_TEMPERATURE, ST_BAD_Q, ST_BAD_DRAFT, ST_TIMEOUT, ST_INTERNAL = 4, 5, 6, 7, 8
+FLAG_AMBIG_ACCEPT, FLAG_NEAR_BOUNDARY, FLAG_DEGENERATE = 1, 2, 4
+
+__all__ = ["dspark_q_build", "dspark_draft_sample", "dspark_verify_greedy",
+           "dspark_verify_ratio", "dspark_target_probs", "q_build", "draft_sample",
+           "verify_greedy", "verify_ratio", "target_probs", "version"]
+
+
+def version() -> str:
+    return _lib.load().dspark_version().decode()
+
+
+def _call(name, *args):
+    rc = getattr(_lib.load(), name)(*args)
+    if rc != 0:
+        raise RuntimeError("%s failed with code %d" % (name, rc))
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype_code(t):
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError("logits must be float32 or bfloat16, got %s" % t.dtype)
+
+
+def _rows(t):
+    """(rows, V, ld) of a logit tensor whose rows are uniformly strided."""
+    if t.dim() < 2 or t.stride(-1) != 1:
+        raise ValueError("logit rows must be contiguous in their last dimension")
+    V = t.shape[-1]
+    ld = t.stride(-2)
+    rows = 1
+    for i in range(t.dim() - 1):
+        rows *= t.shape[i]
+    # leading dimensions must be a plain multiple of the row stride
+    expect = ld
+    for i in range(t.dim() - 2, -1, -1):
+        if t.shape[i] > 1 and t.stride(i) != expect:
+            raise ValueError("logit rows must be uniformly strided")
+        expect *= t.shape[i]
+    return rows, V, ld
+
+
+def _i32(t):
+    if t is not None and t.dtype not in (torch.int32, torch.uint32):
+        raise TypeError("expected an int32/uint32 tensor")
+    return _ptr(t)
+
+
+# ------------------------------------------------------------ C-named calls
+def dspark_q_build(draft_logits, temperature, top_k, counts, sparse_ids, nnz, row_status,
+                   stream=None):
+    rows, V, ld = _rows(draft_logits)
+    _call("dspark_q_build", _ptr(draft_logits), _dtype_code(draft_logits), ld, rows, V,
+          _ptr(temperature), int(top_k), _i32(counts), _i32(sparse_ids), _i32(nnz),
+          _i32(row_status), _stream(stream))
+
+
+def dspark_draft_sample(counts, sparse_ids, nnz, top_k, B, depth, V, seed, request_ids,
+                        draft_tokens, row_status, stream=None):
+    _call("dspark_draft_sample", _i32(counts), _i32(sparse_ids), _i32(nnz), int(top_k), int(B),
+          int(depth), int(V), int(seed) & (2 ** 64 - 1), _i32(request_ids), _i32(draft_tokens),
+          _i32(row_status), _stream(stream))
+
+
+def dspark_verify_greedy(target_logits, B, depth, draft_tokens, accept_len, committed,
+                         req_status, stream=None):
+    rows, V, ld = _rows(target_logits)
+    if rows != B * (depth + 1):
+        raise ValueError("target_logits must hold B*(depth+1) rows")
+    _call("dspark_verify_greedy", _ptr(target_logits), _dtype_code(target_logits), ld, int(B),
+          int(depth), V, _i32(draft_tokens), _i32(accept_len), _i32(committed),
+          _i32(req_status), _stream(stream))
+
+
+def dspark_verify_ratio(target_logits, B, depth, draft_tokens, counts, sparse_ids, nnz, top_k,
+                        seed, request_ids, accept_len, committed, flags, req_status,
+                        stream=None):
+    rows, V, ld = _rows(target_logits)
+    if rows != B * (depth + 1):
+        raise ValueError("target_logits must hold B*(depth+1) rows")
+    _call("dspark_verify_ratio", _ptr(target_logits), _dtype_code(target_logits), ld, int(B),
+          int(depth), V, _i32(draft_tokens), _i32(counts), _i32(sparse_ids), _i32(nnz),
+          int(top_k), int(seed) & (2 ** 64 - 1), _i32(request_ids), _i32(accept_len),
+          _i32(committed), _i32(flags), _i32(req_status), _stream(stream))
+
+
+def dspark_target_probs(target_logits, p_out, argmax, row_status, stream=None):
+    rows, V, ld = _rows(target_logits)
+    _call("dspark_target_probs", _ptr(target_logits), _dtype_code(target_logits), ld, rows, V,
+          _ptr(p_out), _i32(argmax), _i32(row_status), _stream(stream))
+
+
+# --------------------------------------------------- allocating helpers
+def _empty(shape, dtype, device):
+    return torch.empty(shape, dtype=dtype, device=device)
+
+
+def q_build(draft_logits, temperature=None, top_k=0, stream=None):
+    """draft_logits [..., V]; returns dict(counts, ids, nnz, status) (rows flattened)."""
+    rows, V, _ = _rows(draft_logits)
+    dev = draft_logits.device
+    if top_k > 0:
+        counts = _empty((rows, top_k), torch.int32, dev)
+        ids = _empty((rows, top_k), torch.int32, dev)
+        nnz = _empty((rows,), torch.int32, dev)
+    else:
+        counts = _empty((rows, V), torch.int32, dev)
+        ids = nnz = None
+    status = _empty((rows,), torch.int32, dev)
+    dspark_q_build(draft_logits, temperature, top_k, counts, ids, nnz, status, stream)
+    return {"counts": counts, "ids": ids, "nnz": nnz, "status": status, "top_k": top_k}
+
+
+def draft_sample(q, B, depth, V, seed, request_ids=None, stream=None):
+    dev = q["counts"].device
+    tokens = _empty((B * depth,), torch.int32, dev)
+    status = _empty((B * depth,), torch.int32, dev)
+    dspark_draft_sample(q["counts"], q["ids"], q["nnz"], q["top_k"], B, depth, V, seed,
+                        request_ids, tokens, status, stream)
+    return tokens.view(B, depth), status.view(B, depth)
+
+
+def verify_greedy(target_logits, drafts, stream=None):
+    B, depth = drafts.shape
+    dev = target_logits.device
+    acc = _empty((B,), torch.int32, dev)
+    com = _empty((B, depth + 1), torch.int32, dev)
+    st = _empty((B,), torch.int32, dev)
+    dspark_verify_greedy(target_logits, B, depth, drafts, acc, com, st, stream)
+    return acc, com, st
+
+
+def verify_ratio(target_logits, drafts, q, seed, request_ids=None, stream=None):
+    B, depth = drafts.shape
+    dev = target_logits.device
+    acc = _empty((B,), torch.int32, dev)
+    com = _empty((B, depth + 1), torch.int32, dev)
+    fl = _empty((B,), torch.int32, dev)
+    st = _empty((B,), torch.int32, dev)
+    dspark_verify_ratio(target_logits, B, depth, drafts, q["counts"], q["ids"], q["nnz"],
+                        q["top_k"], seed, request_ids, acc, com, fl, st, stream)
+    return acc, com, fl, st
+
+
+def target_probs(target_logits, want_p=True, stream=None):
+    rows, V, _ = _rows(target_logits)
+    dev = target_logits.device
+    p = _empty((rows, V), torch.float32, dev) if want_p else None
+    am = _empty((rows,), torch.int32, dev)
+    st = _empty((rows,), torch.int32, dev)
+    dspark_target_probs(target_logits, p, am, st, stream)
+    return p, am, st

@@ -1,0 +1,159 @@
+// api.cu -- the extern "C" entry points declared in include/dspark.h.  Host
+// code only: argument checks (nothing is launched on a bad argument), then
+// one kernel launch on the caller's stream.  No allocation, no host sync.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "dspark.h"
+
+namespace dspark {
+cudaError_t launch_q_build(const void* x, int dtype, int64_t ld, int n_rows, int V,
+                           const float* temperature, int top_k, uint32_t* counts, int32_t* ids,
+                           int32_t* nnz, int32_t* status, cudaStream_t stream);
+cudaError_t launch_draft_sample(const uint32_t* counts, const int32_t* ids, const int32_t* nnz,
+                                int top_k, int B, int depth, int V, uint64_t seed,
+                                const uint32_t* request_ids, int32_t* tokens, int32_t* status,
+                                cudaStream_t stream);
+cudaError_t launch_verify(int mode, const void* z, int dtype, int64_t ld, int B, int depth, int V,
+                          const int32_t* drafts, const uint32_t* counts, const int32_t* ids,
+                          const int32_t* nnz, int top_k, uint64_t seed,
+                          const uint32_t* request_ids, int32_t* accept_len, int32_t* committed,
+                          uint32_t* flags, int32_t* status, cudaStream_t stream);
+cudaError_t launch_target_probs(const void* z, int dtype, int64_t ld, int n_rows, int V,
+                                float* p_out, int32_t* argmax, int32_t* status,
+                                cudaStream_t stream);
+}  // namespace dspark
+
+namespace {
+
+constexpr int kMaxGridRows = (1 << 30) / 8;  // rows per launch (8-CTA clusters)
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int esize(int32_t dtype) { return dtype == DSPARK_F32 ? 4 : 2; }
+
+int check_common(int32_t dtype, int32_t V, int64_t ld) {
+  if (dtype != DSPARK_F32 && dtype != DSPARK_BF16) return DSPARK_ERR_DTYPE;
+  if (V < 1 || V > DSPARK_MAX_V) return DSPARK_ERR_SIZE;
+  if (ld < V) return DSPARK_ERR_SIZE;
+  return 0;
+}
+
+int check_topk(int32_t top_k, int32_t V) {
+  if (top_k < 0 || top_k > V || top_k > DSPARK_MAX_TOPK) return DSPARK_ERR_TOPK;
+  return 0;
+}
+
+int launch_result(cudaError_t e) { return e == cudaSuccess ? 0 : (int)e; }
+
+}  // namespace
+
+extern "C" {
+
+const char* dspark_version(void) { return "dspark-gb300 0.1 (" DSPARK_QSEM ", sm_103a)"; }
+
+int dspark_q_build(const void* draft_logits, int32_t dtype, int64_t ld, int32_t n_rows, int32_t V,
+                   const float* temperature, int32_t top_k, uint32_t* counts, int32_t* sparse_ids,
+                   int32_t* nnz, int32_t* row_status, void* stream) {
+  if (int e = check_common(dtype, V, ld)) return e;
+  if (int e = check_topk(top_k, V)) return e;
+  if (n_rows < 0 || n_rows > kMaxGridRows) return DSPARK_ERR_SIZE;
+  if (n_rows == 0) return 0;
+  if (!draft_logits || !counts || !row_status) return DSPARK_ERR_NULL;
+  if (top_k > 0 && (!sparse_ids || !nnz)) return DSPARK_ERR_NULL;
+  if (!aligned(draft_logits, esize(dtype)) || !aligned(counts, 4) || !aligned(row_status, 4) ||
+      (temperature && !aligned(temperature, 4)) || (sparse_ids && !aligned(sparse_ids, 4)) ||
+      (nnz && !aligned(nnz, 4)))
+    return DSPARK_ERR_ALIGN;
+  return launch_result(dspark::launch_q_build(draft_logits, dtype, ld, n_rows, V, temperature,
+                                              top_k, counts, sparse_ids, nnz, row_status,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
+int dspark_draft_sample(const uint32_t* counts, const int32_t* sparse_ids, const int32_t* nnz,
+                        int32_t top_k, int32_t B, int32_t depth, int32_t V, uint64_t seed,
+                        const uint32_t* request_ids, int32_t* draft_tokens, int32_t* row_status,
+                        void* stream) {
+  if (V < 1 || V > DSPARK_MAX_V) return DSPARK_ERR_SIZE;
+  if (depth < 1 || depth > DSPARK_MAX_DEPTH) return DSPARK_ERR_SIZE;
+  if (B < 0 || (int64_t)B * depth > (int64_t)(1 << 30)) return DSPARK_ERR_SIZE;
+  if (int e = check_topk(top_k, V)) return e;
+  if (B == 0) return 0;
+  if (!counts || !draft_tokens || !row_status) return DSPARK_ERR_NULL;
+  if (top_k > 0 && (!sparse_ids || !nnz)) return DSPARK_ERR_NULL;
+  if (!aligned(counts, 4) || !aligned(draft_tokens, 4) || !aligned(row_status, 4) ||
+      (request_ids && !aligned(request_ids, 4)) || (sparse_ids && !aligned(sparse_ids, 4)) ||
+      (nnz && !aligned(nnz, 4)))
+    return DSPARK_ERR_ALIGN;
+  return launch_result(dspark::launch_draft_sample(counts, sparse_ids, nnz, top_k, B, depth, V,
+                                                   seed, request_ids, draft_tokens, row_status,
+                                                   static_cast<cudaStream_t>(stream)));
+}
+
+static int check_verify(const void* target_logits, int32_t dtype, int64_t ld, int32_t B,
+                        int32_t depth, int32_t V, const int32_t* draft_tokens,
+                        const int32_t* accept_len, const int32_t* committed,
+                        const int32_t* req_status) {
+  if (int e = check_common(dtype, V, ld)) return e;
+  if (depth < 1 || depth > DSPARK_MAX_DEPTH) return DSPARK_ERR_SIZE;
+  if (B < 0 || B > kMaxGridRows) return DSPARK_ERR_SIZE;
+  if (B == 0) return 1;  // nothing to do
+  if (!target_logits || !draft_tokens || !accept_len || !committed || !req_status)
+    return DSPARK_ERR_NULL;
+  if (!aligned(target_logits, esize(dtype)) || !aligned(draft_tokens, 4) ||
+      !aligned(accept_len, 4) || !aligned(committed, 4) || !aligned(req_status, 4))
+    return DSPARK_ERR_ALIGN;
+  return 0;
+}
+
+int dspark_verify_greedy(const void* target_logits, int32_t dtype, int64_t ld, int32_t B,
+                         int32_t depth, int32_t V, const int32_t* draft_tokens,
+                         int32_t* accept_len, int32_t* committed, int32_t* req_status,
+                         void* stream) {
+  const int e = check_verify(target_logits, dtype, ld, B, depth, V, draft_tokens, accept_len,
+                             committed, req_status);
+  if (e != 0) return e > 0 ? 0 : e;
+  return launch_result(dspark::launch_verify(0, target_logits, dtype, ld, B, depth, V,
+                                             draft_tokens, nullptr, nullptr, nullptr, 0, 0ull,
+                                             nullptr, accept_len, committed, nullptr, req_status,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+int dspark_verify_ratio(const void* target_logits, int32_t dtype, int64_t ld, int32_t B,
+                        int32_t depth, int32_t V, const int32_t* draft_tokens,
+                        const uint32_t* counts, const int32_t* sparse_ids, const int32_t* nnz,
+                        int32_t top_k, uint64_t seed, const uint32_t* request_ids,
+                        int32_t* accept_len, int32_t* committed, uint32_t* flags,
+                        int32_t* req_status, void* stream) {
+  const int e = check_verify(target_logits, dtype, ld, B, depth, V, draft_tokens, accept_len,
+                             committed, req_status);
+  if (e != 0) return e > 0 ? 0 : e;
+  if (int e2 = check_topk(top_k, V)) return e2;
+  if (!counts) return DSPARK_ERR_NULL;
+  if (top_k > 0 && (!sparse_ids || !nnz)) return DSPARK_ERR_NULL;
+  if (!aligned(counts, 4) || (flags && !aligned(flags, 4)) ||
+      (request_ids && !aligned(request_ids, 4)) || (sparse_ids && !aligned(sparse_ids, 4)) ||
+      (nnz && !aligned(nnz, 4)))
+    return DSPARK_ERR_ALIGN;
+  return launch_result(dspark::launch_verify(1, target_logits, dtype, ld, B, depth, V,
+                                             draft_tokens, counts, sparse_ids, nnz, top_k, seed,
+                                             request_ids, accept_len, committed, flags,
+                                             req_status, static_cast<cudaStream_t>(stream)));
+}
+
+int dspark_target_probs(const void* target_logits, int32_t dtype, int64_t ld, int32_t n_rows,
+                        int32_t V, float* p_out, int32_t* argmax, int32_t* row_status,
+                        void* stream) {
+  if (int e = check_common(dtype, V, ld)) return e;
+  if (n_rows < 0 || n_rows > kMaxGridRows) return DSPARK_ERR_SIZE;
+  if (n_rows == 0) return 0;
+  if (!target_logits || !row_status) return DSPARK_ERR_NULL;
+  if (!aligned(target_logits, esize(dtype)) || !aligned(row_status, 4) ||
+      (p_out && !aligned(p_out, 4)) || (argmax && !aligned(argmax, 4)))
+    return DSPARK_ERR_ALIGN;
+  return launch_result(dspark::launch_target_probs(target_logits, dtype, ld, n_rows, V, p_out,
+                                                   argmax, row_status,
+                                                   static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,293 @@
+// common.cuh -- device helpers shared by the library's kernels: Philox4x32-10,
+// the deterministic fp32 exponential exp_ds, the exact FP64 allocation split,
+// logit loads and block / cluster reductions.
+//
+// Everything on the q path must round exactly as written (IEEE RN, no FTZ,
+// no contraction): those expressions use the explicit __f*_rn intrinsics.
+#pragma once
+
+#include <cooperative_groups.h>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "dspark.h"
+
+namespace cg = cooperative_groups;
+
+namespace dspark {
+
+constexpr uint32_t kM = DSPARK_M;
+
+// ---------------------------------------------------------------- Philox
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as
+// easy as 1, 2, 3", SC'11): ten rounds of two 32x32->64 multiplies of
+// counter words 0 and 2 (multipliers 0xD2511F53, 0xCD9E8D57); the key is
+// advanced by the Weyl increments 0x9E3779B9, 0xBB67AE85 between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int i = 0; i < 10; ++i) {
+    if (i > 0) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    const uint32_t lo0 = 0xD2511F53u * c.x;
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x);
+    const uint32_t lo1 = 0xCD9E8D57u * c.z;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z);
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+  }
+  return c;
+}
+
+// Word 0 of Philox(key = seed, counter = (request, row, purpose, 0)).
+__device__ __forceinline__ uint32_t draw_u32(uint64_t seed, uint32_t request, uint32_t row,
+                                             uint32_t purpose) {
+  return philox4x32_10(make_uint4(request, row, purpose, 0u), (uint32_t)seed,
+                       (uint32_t)(seed >> 32))
+      .x;
+}
+
+// ----------------------------------------------------------------- exp_ds
+// Deterministic fp32 e^d for d <= 0 (0 below -87): Cody-Waite reduction
+// n = rint(d * log2(e)), r = d - n*ln2 with ln2 split into a 16-bit-fraction
+// high part (n*hi exact for |n| <= 127) and the float nearest the rest, then
+// the degree-7 Taylor polynomial of e^r in Horner form (one fma per step) and
+// an exact scaling by 2^n.  Constants: float nearest 1/ln2; ln2 truncated
+// to 16 fraction bits; float nearest (ln2 - that); floats nearest 1/k!.
+constexpr float kL2E = 0x1.715476p+0f;
+constexpr float kLn2Hi = 0x1.62e4p-1f;
+constexpr float kLn2Lo = 0x1.7f7d1cp-20f;
+constexpr float kInvFact2 = 0x1p-1f;
+constexpr float kInvFact3 = 0x1.555556p-3f;
+constexpr float kInvFact4 = 0x1.555556p-5f;
+constexpr float kInvFact5 = 0x1.111112p-7f;
+constexpr float kInvFact6 = 0x1.6c16c2p-10f;
+constexpr float kInvFact7 = 0x1.a01a02p-13f;
+
+__device__ __forceinline__ float exp_ds_poly(float d, int* n_out) {
+  const float t = __fmul_rn(d, kL2E);
+  const float n = rintf(t);
+  float r = __fmaf_rn(-n, kLn2Hi, d);
+  r = __fmaf_rn(-n, kLn2Lo, r);
+  float p = kInvFact7;
+  p = __fmaf_rn(p, r, kInvFact6);
+  p = __fmaf_rn(p, r, kInvFact5);
+  p = __fmaf_rn(p, r, kInvFact4);
+  p = __fmaf_rn(p, r, kInvFact3);
+  p = __fmaf_rn(p, r, kInvFact2);
+  p = __fmaf_rn(p, r, 1.0f);
+  p = __fmaf_rn(p, r, 1.0f);
+  *n_out = (int)n;
+  return p;
+}
+
+__device__ __forceinline__ float exp_ds(float d) {
+  if (!(d >= -87.0f)) return 0.0f;
+  int n;
+  const float p = exp_ds_poly(d, &n);
+  return __fmul_rn(p, __int_as_float((127 + n) << 23));
+}
+
+// Integer weight E = floor(exp_ds(d) * 2^40) of a token at distance d <= 0
+// from the row maximum.  Below d = -28 the weight is 0 for every float d
+// (exp_ds(d) < 2^-40 there), so the polynomial is skipped.
+__device__ __forceinline__ float weight_float(float d) {
+  return (d >= -28.0f) ? exp_ds(d) : 0.0f;
+}
+
+// E = floor(e * 2^40) for e in {0} U [2^-126, 1], returned as (Ei, se) with
+// E = Ei << se and Ei < 2^24.
+__device__ __forceinline__ void weight_split(float e, uint32_t* Ei, int* se) {
+  const uint32_t b = __float_as_uint(e);
+  const int ef = (int)(b >> 23);  // e >= 0
+  const uint32_t p24 = (b & 0x7FFFFFu) | 0x800000u;
+  const int sh = ef - 110;  // e = p24 * 2^(ef-150); E = p24 * 2^(ef-110) floored
+  if (e == 0.0f || sh <= -24) {
+    *Ei = 0u;
+    *se = 0;
+  } else if (sh >= 0) {
+    *Ei = p24;
+    *se = sh;
+  } else {
+    *Ei = p24 >> (-sh);
+    *se = 0;
+  }
+}
+
+__device__ __forceinline__ uint64_t weight_u64(float e) {
+  uint32_t Ei;
+  int se;
+  weight_split(e, &Ei, &se);
+  return (uint64_t)Ei << se;
+}
+
+// ------------------------------------------------- FP64 allocation split
+// k = RN64(2^24 / RN64(S)) is passed as mk * 2^ek (mk in [2^52, 2^53)).
+// a = RN64(E * k) is computed exactly with integer arithmetic (the product
+// of a <= 24-bit E and the 53-bit mk rounded to 53 bits, ties to even),
+// which is bit-identical to the FP64 multiply.  a = A * 2^-t with t >= 28;
+// floor(a) = A >> t; the fraction is r = (A mod 2^t) * 2^-t.
+struct AllocSplit {
+  uint32_t f;      // floor(a)  (<= 2^24)
+  uint64_t rnum;   // A mod 2^t
+  int t;           // fraction bits
+};
+
+__device__ __forceinline__ AllocSplit alloc_split(uint32_t Ei, int se, uint64_t mk, int ek) {
+  AllocSplit out;
+  if (Ei == 0u) {
+    out.f = 0u;
+    out.rnum = 0ull;
+    out.t = 64;
+    return out;
+  }
+  const unsigned __int128 P = (unsigned __int128)Ei * (unsigned __int128)mk;  // < 2^77
+  const uint64_t Phi = (uint64_t)(P >> 64);
+  const int nb = Phi ? (128 - __clzll((long long)Phi)) : (64 - __clzll((long long)(uint64_t)P));
+  int s = nb - 53;  // >= 0 since P >= 2^52
+  uint64_t A;
+  if (s == 0) {
+    A = (uint64_t)P;
+  } else {
+    A = (uint64_t)(P >> s);
+    const uint64_t rem = (uint64_t)P & ((1ull << s) - 1ull);  // s <= 24
+    const uint64_t half = 1ull << (s - 1);
+    if (rem > half || (rem == half && (A & 1ull))) ++A;
+    if (A == (1ull << 53)) {
+      A >>= 1;
+      ++s;
+    }
+  }
+  const int t = -(s + se + ek);
+  out.t = t;
+  if (t >= 64) {
+    out.f = 0u;
+    out.rnum = A;
+  } else {
+    out.f = (uint32_t)(A >> t);
+    out.rnum = A & ((1ull << t) - 1ull);
+  }
+  return out;
+}
+
+// Bucket of the fraction: floor(r * 4096).
+__device__ __forceinline__ uint32_t frac_bucket(const AllocSplit& a) {
+  const int sh = a.t - 12;
+  return (sh >= 64) ? 0u : (uint32_t)(a.rnum >> sh);
+}
+
+// Exact fraction as an FP64 bit pattern (monotone for r >= 0).
+__device__ __forceinline__ uint64_t frac_key(const AllocSplit& a) {
+  // 2^-t built from its bits (t <= 90 here, so the power is a normal double)
+  const double scale = __longlong_as_double((long long)(1023 - a.t) << 52);
+  const double r = __dmul_rn(__ull2double_rn(a.rnum), scale);
+  return (uint64_t)__double_as_longlong(r);
+}
+
+// ------------------------------------------------------------ logit loads
+__device__ __forceinline__ float bf16_to_f32(uint16_t h) {
+  return __uint_as_float(((uint32_t)h) << 16);
+}
+
+__device__ __forceinline__ float load_logit(const void* row, int dtype, int64_t v) {
+  if (dtype == DSPARK_F32) return __ldg(reinterpret_cast<const float*>(row) + v);
+  return bf16_to_f32(__ldg(reinterpret_cast<const unsigned short*>(row) + v));
+}
+
+// Monotone unsigned key of a float (larger float -> larger key).
+__device__ __forceinline__ uint32_t float_key(float y) {
+  const uint32_t u = __float_as_uint(y);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// ------------------------------------------------------ block reductions
+template <typename T, typename Op>
+__device__ __forceinline__ T warp_reduce(T v, Op op) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = op(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Reduces over the block; every thread gets the result.  `scratch` holds at
+// least 32 elements; the call contains two __syncthreads().
+template <typename T, typename Op>
+__device__ __forceinline__ T block_reduce(T v, Op op, T* scratch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = (blockDim.x + 31) >> 5;
+  v = warp_reduce(v, op);
+  __syncthreads();
+  if (lane == 0) scratch[warp] = v;
+  __syncthreads();
+  T r = scratch[0];
+  for (int i = 1; i < nw; ++i) r = op(r, scratch[i]);
+  return r;
+}
+
+struct OpAddU64 {
+  __device__ uint64_t operator()(uint64_t a, uint64_t b) const { return a + b; }
+};
+struct OpAddU32 {
+  __device__ uint32_t operator()(uint32_t a, uint32_t b) const { return a + b; }
+};
+struct OpOrU32 {
+  __device__ uint32_t operator()(uint32_t a, uint32_t b) const { return a | b; }
+};
+struct OpMaxF {
+  __device__ float operator()(float a, float b) const { return fmaxf(a, b); }
+};
+struct OpMinU64 {
+  __device__ uint64_t operator()(uint64_t a, uint64_t b) const { return a < b ? a : b; }
+};
+struct OpMaxU64 {
+  __device__ uint64_t operator()(uint64_t a, uint64_t b) const { return a > b ? a : b; }
+};
+
+// Inclusive scan over the block for one uint32 per thread; returns the
+// inclusive prefix, *total gets the block total.  scratch >= 32 words.
+__device__ __forceinline__ uint32_t block_inclusive_scan(uint32_t v, uint32_t* scratch,
+                                                         uint32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = (blockDim.x + 31) >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  __syncthreads();
+  if (lane == 31) scratch[warp] = v;
+  __syncthreads();
+  uint32_t before = 0, all = 0;
+  for (int i = 0; i < nw; ++i) {
+    const uint32_t s = scratch[i];
+    if (i < warp) before += s;
+    all += s;
+  }
+  *total = all;
+  return v + before;
+}
+
+// Inclusive scan over the block for one uint64 per thread; *total gets the
+// block total.  scratch >= 32 elements.
+__device__ __forceinline__ uint64_t block_inclusive_scan_u64(uint64_t v, uint64_t* scratch,
+                                                             uint64_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = (blockDim.x + 31) >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint64_t n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  __syncthreads();
+  if (lane == 31) scratch[warp] = v;
+  __syncthreads();
+  uint64_t before = 0, all = 0;
+  for (int i = 0; i < nw; ++i) {
+    const uint64_t s = scratch[i];
+    if (i < warp) before += s;
+    all += s;
+  }
+  *total = all;
+  return v + before;
+}
+
+}  // namespace dspark

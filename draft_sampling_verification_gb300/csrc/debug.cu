@@ -1,0 +1,59 @@
+// debug.cu -- element-wise access to exp_ds / the integer weights and to
+// Philox4x32-10 (include/dspark_debug.h).
+#include "common.cuh"
+#include "dspark_debug.h"
+
+namespace {
+
+__global__ void exp_weights_kernel(const float* d, int64_t n, float* e_out, uint64_t* E_out) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const float e = dspark::exp_ds(d[i]);
+    if (e_out) e_out[i] = e;
+    if (E_out) E_out[i] = dspark::weight_u64(dspark::weight_float(d[i]));
+  }
+}
+
+__global__ void philox_kernel(const uint4* ctr, uint64_t seed, int64_t n, uint4* out) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x)
+    out[i] = dspark::philox4x32_10(ctr[i], (uint32_t)seed, (uint32_t)(seed >> 32));
+}
+
+int grid_for(int64_t n) {
+  const int64_t g = (n + 255) / 256;
+  return (int)(g < 152 * 16 ? (g < 1 ? 1 : g) : 152 * 16);
+}
+
+}  // namespace
+
+extern "C" {
+
+int dspark_debug_exp_weights(const float* d, int64_t n, float* e_out, uint64_t* E_out,
+                             void* stream) {
+  if (n < 0) return DSPARK_ERR_SIZE;
+  if (n == 0) return 0;
+  if (!d) return DSPARK_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(d) & 3) || (reinterpret_cast<uintptr_t>(e_out) & 3) ||
+      (reinterpret_cast<uintptr_t>(E_out) & 7))
+    return DSPARK_ERR_ALIGN;
+  exp_weights_kernel<<<grid_for(n), 256, 0, static_cast<cudaStream_t>(stream)>>>(d, n, e_out,
+                                                                                   E_out);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? 0 : (int)e;
+}
+
+int dspark_debug_philox(const uint32_t* ctr, uint64_t seed, int64_t n, uint32_t* out,
+                        void* stream) {
+  if (n < 0) return DSPARK_ERR_SIZE;
+  if (n == 0) return 0;
+  if (!ctr || !out) return DSPARK_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(ctr) & 15) || (reinterpret_cast<uintptr_t>(out) & 15))
+    return DSPARK_ERR_ALIGN;
+  philox_kernel<<<grid_for(n), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<const uint4*>(ctr), seed, n, reinterpret_cast<uint4*>(out));
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? 0 : (int)e;
+}
+
+}  // extern "C"

@@ -22,8 +22,9 @@ Recipes (sizes at full scale):
   seeded affine permutation of the ids (rank = (a v + b) mod V + 1, a coprime
   with V); target = draft + N(0, 0.7^2) fp32; sparse top-256 q; ratio; seed 2.
 * C4  B=256: Zipf draft fp32, target = bf16(draft + N(0, 0.7^2)); per
-  (request, position) 10 % of ids masked to -inf in both the draft row and
-  its target row (target row 5 has its own mask); 1 % of draft rows carry a
+  (request, position) exactly 10 % of ids (a seeded affine selection) masked
+  to -inf in both the draft row and its target row (target row 5 has its own
+  mask); 1 % of draft rows carry a
   top logit shared by g in {3, 5, 7} ids spread over the vocabulary and the
   whole row snapped to a 1/4 grid, so many tokens (the argmax group among
   them) share identical remainders and the lowest-id rule decides the grant;
@@ -73,21 +74,31 @@ class Workload:
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round fp32 to bf16 (nearest, ties to even); returns uint16 bit patterns."""
-    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    lsb = (u >> 16) & 1
-    r = ((u + 0x7FFF + lsb) >> 16).astype(np.uint16)
-    nan = np.isnan(x)
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    u = x.reshape(-1).view(np.uint32)
+    out = np.empty(u.size, np.uint16)
+    step = 1 << 24
+    for s in range(0, u.size, step):
+        c = u[s:s + step]
+        r = (c >> 16) & 1
+        r += c
+        r += 0x7FFF  # no wrap for any non-NaN pattern (at most 0xFF807FFF)
+        r >>= 16
+        out[s:s + step] = r
+    nan = np.isnan(x.reshape(-1))
     if nan.any():
-        r[nan] = 0x7FC0
-    return r
+        out[nan] = 0x7FC0
+    return out.reshape(x.shape)
 
 
 def _normal(rng, shape, sigma):
-    return (rng.standard_normal(shape, dtype=np.float32) * np.float32(sigma)).astype(np.float32)
+    out = rng.standard_normal(shape, dtype=np.float32)
+    out *= np.float32(sigma)
+    return out
 
 
-def _affine_ranks(rng, n_rows, V):
-    """Per row a seeded permutation of 0..V-1: rank(v) = (a v + b) mod V."""
+def _affine_params(rng, n_rows, V):
+    """Per row (a, b) of a seeded affine permutation v -> (a v + b) mod V."""
     a = np.empty(n_rows, np.int64)
     for i in range(n_rows):
         while True:
@@ -96,18 +107,33 @@ def _affine_ranks(rng, n_rows, V):
                 a[i] = cand
                 break
     b = rng.integers(0, max(V, 1), size=n_rows, dtype=np.int64)
+    return a, b
+
+
+def _affine_ranks(a, b, V):
     v = np.arange(V, dtype=np.int64)
     return (a[:, None] * v[None, :] + b[:, None]) % V
 
 
-def zipf_rows(rng, n_rows, V, slope=1.1, noise=0.3, chunk=256):
+def zipf_rows(rng, n_rows, V, slope=1.1, noise=0.3, chunk=64):
     """logit(v) = -slope * ln(rank(v) + 1) + N(0, noise^2), seeded permutation."""
+    table = (-slope * np.log1p(np.arange(V, dtype=np.float64))).astype(np.float32)
+    a, b = _affine_params(rng, n_rows, V)
     out = np.empty((n_rows, V), np.float32)
     for s in range(0, n_rows, chunk):
         e = min(n_rows, s + chunk)
-        ranks = _affine_ranks(rng, e - s, V)
-        out[s:e] = (-slope * np.log1p(ranks.astype(np.float64))).astype(np.float32)
+        np.take(table, _affine_ranks(a[s:e], b[s:e], V), out=out[s:e])
         out[s:e] += _normal(rng, (e - s, V), noise)
+    return out
+
+
+def affine_masks(rng, n_rows, V, n_mask, chunk=64):
+    """Per row exactly n_mask masked ids: those whose affine rank is < n_mask."""
+    a, b = _affine_params(rng, n_rows, V)
+    out = np.empty((n_rows, V), bool)
+    for s in range(0, n_rows, chunk):
+        e = min(n_rows, s + chunk)
+        np.less(_affine_ranks(a[s:e], b[s:e], V), n_mask, out=out[s:e])
     return out
 
 
@@ -178,11 +204,7 @@ def config4(B=256, V=V_FULL, depth=DEPTH, rng=None, tie_fraction=0.01, mask_frac
     rng = rng or np.random.default_rng(1004)
     xd = zipf_rows(rng, B * depth, V).reshape(B, depth, V)
     n_mask = int(round(mask_fraction * V))
-    masks = np.zeros((B, depth + 1, V), bool)
-    for b in range(B):
-        for j in range(depth + 1):
-            if n_mask > 0:
-                masks[b, j, rng.choice(V, size=n_mask, replace=False)] = True
+    masks = affine_masks(rng, B * (depth + 1), V, n_mask).reshape(B, depth + 1, V)
     tie_rows = []
     n_tie = max(1, int(round(tie_fraction * B * depth))) if V >= 8 else 0
     for r in rng.choice(B * depth, size=min(n_tie, B * depth), replace=False):
@@ -197,8 +219,9 @@ def config4(B=256, V=V_FULL, depth=DEPTH, rng=None, tie_fraction=0.01, mask_frac
     xt = np.empty((B, depth + 1, V), np.float32)
     xt[:, :depth] = xd + _normal(rng, (B, depth, V), 0.7)
     xt[:, depth] = zipf_rows(rng, B, V) + _normal(rng, (B, V), 0.7)
-    xd[masks[:, :depth]] = -np.inf
-    xt[masks] = -np.inf
+    for b in range(B):
+        xd[b][masks[b, :depth]] = -np.inf
+        xt[b][masks[b]] = -np.inf
     return Workload("C4 B=%d zipf fp32 draft / bf16 target dense, 10%% mask, 1%% ties" % B, B,
                     depth, V, xd, f32_to_bf16_bits(xt), "bf16", _temps(B, depth, 1.0), 0, 3,
                     ("greedy", "ratio"), _req(B), {"tie_rows": tie_rows})

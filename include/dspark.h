@@ -1,0 +1,228 @@
+/*
+ * dspark.h -- C ABI of the GB300 draft-sampling and verification library
+ * (libdspark.so, CUDA kernels for sm_103a).
+ *
+ * What it computes, and where the method is defined:
+ *   "PP1 q transport and scheduling design", section "Distribution contract
+ *   and precision": the dyadic categorical q (integer counts c_v >= 0 summing
+ *   exactly to M = 2^24, q(v) = c_v / M), built from temperature-scaled draft
+ *   weights by FP64 floor plus largest remainders with ties to the lowest
+ *   token id, optionally on a global top-k support; one token drawn per
+ *   position from a uniform 24-bit integer as the first cumulative count
+ *   strictly greater than the draw; ratio tests against the target p and a
+ *   full-vocabulary residual.  Same page, "Versioned v2 message design": the
+ *   validation list, separate RNG domains for proposal, acceptance and
+ *   correction/bonus draws, and the commit (accepted count plus the
+ *   correction or bonus id).  "DeepSeek-V4.1 DSpark", "State and sampling
+ *   contracts": greedy verification accepts while the target argmax equals
+ *   the proposal.  "Remote DSpark drafter -- wire and state contract",
+ *   section 2: the anchor-as-first block (target row j scores the token
+ *   drafted at position j; row `depth` gives the bonus) and lowest-index ties
+ *   of the argmax.
+ *
+ * Conventions for every call:
+ *   - Pointers are DEVICE pointers unless stated otherwise.  The caller owns
+ *     every buffer; the library allocates nothing, keeps no state between
+ *     calls and never synchronises the host.  `stream` is a cudaStream_t
+ *     (NULL = the legacy default stream).  All work is enqueued on `stream`.
+ *   - Return value (decided on the host before anything is launched):
+ *       0  enqueued;
+ *      <0  argument error (one of DSPARK_ERR_*), nothing launched;
+ *      >0  the cudaError_t of a failed launch.
+ *   - Per-row / per-request device statuses (DSPARK_ST_*) are valid once the
+ *     stream has reached the call.  A refused draft row gets all-zero counts
+ *     and token -1; a refused request gets accept_len 0 and committed all -1
+ *     (the whole unverified proposal is discarded, as the PP1 page asks).
+ *   - Logit rows may have any stride `ld` >= V (in elements) and any 4-byte
+ *     (fp32) or 2-byte (bf16) alignment; only the V elements of each row are
+ *     read.  bf16 logits are widened to fp32 exactly.
+ *   - Every integer output is a pure function of the inputs, the seed, the
+ *     request id and the row: it does not depend on the batch size, on the
+ *     other rows or on the launch shape.
+ *   - Random draws: Philox4x32-10 (Salmon et al., SC'11) with key =
+ *     (seed low 32 bits, seed high 32 bits) and counter = (request id, row,
+ *     purpose, 0); a draw is word 0 of the output.  24-bit draws are word 0
+ *     shifted right by 8.  Request ids are request_ids[b] or, if that pointer
+ *     is NULL, b.  Callers fold generation and round into seed or request id.
+ */
+#ifndef DSPARK_H
+#define DSPARK_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DSPARK_QSEM "dyadic24-standard-v1"
+#define DSPARK_M 16777216u           /* total mass of every q row, 2^24      */
+#define DSPARK_MAX_V 131072          /* largest vocabulary (row length)      */
+#define DSPARK_MAX_DEPTH 8           /* draft positions per request          */
+#define DSPARK_MAX_TOPK 1024         /* largest sparse support               */
+
+/* logit element types */
+#define DSPARK_F32 0
+#define DSPARK_BF16 1
+
+/* Philox purposes (word 2 of the counter), fixed in the ABI */
+#define DSPARK_PURPOSE_PROPOSAL 0u
+#define DSPARK_PURPOSE_ACCEPT 1u
+#define DSPARK_PURPOSE_RESIDUAL 2u
+#define DSPARK_PURPOSE_BONUS 3u
+
+/* host-side argument errors */
+#define DSPARK_ERR_NULL (-1)         /* a required pointer is NULL           */
+#define DSPARK_ERR_SIZE (-2)         /* V, rows, B, depth, ld out of range   */
+#define DSPARK_ERR_DTYPE (-3)        /* unknown dtype                        */
+#define DSPARK_ERR_TOPK (-4)         /* top_k < 0, > V or > DSPARK_MAX_TOPK  */
+#define DSPARK_ERR_ALIGN (-5)        /* pointer not aligned to its element   */
+#define DSPARK_ERR_DEVICE (-6)       /* no usable sm_103 device current      */
+
+/* device statuses (per draft row, or per request) */
+#define DSPARK_ST_OK 0
+#define DSPARK_ST_NONFINITE 1        /* NaN or +inf logit (or y overflowed)  */
+#define DSPARK_ST_ZERO_MASS 2        /* no finite logit                      */
+#define DSPARK_ST_ALLOC_INCONSISTENT 3 /* remaining tickets out of range     */
+#define DSPARK_ST_BAD_TEMPERATURE 4  /* T not finite, <= 0, 1/T not normal   */
+#define DSPARK_ST_BAD_Q 5            /* q row mass != M or not canonical     */
+#define DSPARK_ST_BAD_DRAFT 6        /* draft id out of range or q(x) == 0   */
+#define DSPARK_ST_TIMEOUT 7          /* a bounded wait inside a kernel expired */
+#define DSPARK_ST_INTERNAL 8         /* an internal capacity was exceeded    */
+
+/* verification flags (per request, ratio verification) */
+#define DSPARK_FLAG_AMBIG_ACCEPT 1u  /* |u*q - p| <= 1e-6 * q at a tested row */
+#define DSPARK_FLAG_NEAR_BOUNDARY 2u /* final draw within 1e-6 (probability
+                                        units) of a cumulative boundary     */
+#define DSPARK_FLAG_DEGENERATE 4u    /* residual mass was zero: drew from p  */
+
+/*
+ * dspark_q_build -- dyadic24-standard-v1 q for n_rows draft rows
+ * ("PP1 q transport and scheduling design", Distribution contract and
+ * precision: proposal construction and sparse top-k).
+ *
+ * Per row r (logits at draft_logits + r*ld, V elements, dtype `dtype`):
+ *   T = temperature[r] (1.0 if temperature == NULL, a device pointer);
+ *   refuse (BAD_TEMPERATURE) unless T is finite and > 0 and RN32(1/T) is a
+ *   finite normal float; refuse (NONFINITE) on NaN or +inf logits or a finite
+ *   logit whose scaled value overflows; -inf logits are masked.
+ *   y_v = RN32(x_v * RN32(1/T)); support = all finite y (top_k == 0) or the
+ *   top_k largest y with ties to the lowest id (all finite ones if fewer);
+ *   empty support -> ZERO_MASS.  m = max y; E_v = floor(exp_ds(RN32(y_v - m))
+ *   * 2^40) with exp_ds the library's deterministic fp32 exponential
+ *   (Cody-Waite reduction, degree-7 Taylor polynomial in fma Horner form);
+ *   S = sum E_v in uint64; k = RN64(2^24 / RN64(S)); a_v = RN64(E_v * k);
+ *   counts = floor(a_v) plus one for the M - sum floor(a_v) support tokens
+ *   with the largest a_v - floor(a_v), ties to the lowest id.  Rows where the
+ *   remaining tickets fall outside [0, #positive remainders] or the final sum
+ *   is not M are refused (ALLOC_INCONSISTENT).
+ *
+ * Outputs:
+ *   top_k == 0: counts[n_rows][V] (row stride V); sparse_ids and nnz unused
+ *     (may be NULL).
+ *   top_k  > 0: sparse_ids[n_rows][top_k] ascending token ids of the nonzero
+ *     counts, counts[n_rows][top_k] the matching counts, nnz[n_rows] their
+ *     number; unused slots hold id -1 and count 0.
+ *   row_status[n_rows]: DSPARK_ST_*.
+ * Limits: 1 <= V <= DSPARK_MAX_V, 1 <= n_rows, ld >= V, 0 <= top_k <=
+ * min(V, DSPARK_MAX_TOPK).  Pointers: draft_logits aligned to its element,
+ * counts / sparse_ids / nnz / row_status / temperature 4-byte aligned.
+ */
+int dspark_q_build(const void* draft_logits, int32_t dtype, int64_t ld, int32_t n_rows,
+                   int32_t V, const float* temperature, int32_t top_k, uint32_t* counts,
+                   int32_t* sparse_ids, int32_t* nnz, int32_t* row_status, void* stream);
+
+/*
+ * dspark_draft_sample -- one token per draft row from its q
+ * ("PP1 q transport and scheduling design", Distribution contract and
+ * precision: "a uniform 24-bit integer and exact integer cumulative counts
+ * (first cumulative count strictly greater than the draw)").
+ *
+ * Row r = b*depth + j (request b, position j): D = Philox(seed; request id,
+ * j, PROPOSAL) word 0 >> 8; token = the first id, in ascending order, whose
+ * inclusive cumulative count exceeds D.  Counts as written by
+ * dspark_q_build (dense [B*depth][V] when top_k == 0, sparse
+ * [B*depth][top_k] with sparse_ids and nnz otherwise).  A row whose counts do
+ * not sum to M, or whose sparse ids are not strictly ascending in [0, V), is
+ * refused (BAD_Q, token -1).
+ * Outputs: draft_tokens[B*depth], row_status[B*depth].
+ */
+int dspark_draft_sample(const uint32_t* counts, const int32_t* sparse_ids, const int32_t* nnz,
+                        int32_t top_k, int32_t B, int32_t depth, int32_t V, uint64_t seed,
+                        const uint32_t* request_ids, int32_t* draft_tokens, int32_t* row_status,
+                        void* stream);
+
+/*
+ * dspark_verify_greedy -- greedy verification ("DeepSeek-V4.1 DSpark",
+ * State and sampling contracts: greedy verification matches the target
+ * argmax; the argmax takes the lowest id among equal maxima).
+ *
+ * target_logits: B*(depth+1) rows, row b*(depth+1)+j at target_logits +
+ * (b*(depth+1)+j)*ld.  draft_tokens[B][depth].  For each request the rows
+ * are read in order, stopping at the first row whose argmax differs from the
+ * draft: L = first such j (else depth); committed[b][0..L-1] = drafts,
+ * committed[b][L] = argmax of row L (the correction, or the bonus when
+ * L == depth), committed[b][L+1..depth] = -1; accept_len[b] = L.
+ * Rows after the deciding row are not read and not validated.
+ * Refusals: a draft id outside [0, V) (BAD_DRAFT); a NaN/+inf in a read row
+ * (NONFINITE); a read row with no finite logit (ZERO_MASS).
+ * Outputs: accept_len[B], committed[B][depth+1], req_status[B].
+ */
+int dspark_verify_greedy(const void* target_logits, int32_t dtype, int64_t ld, int32_t B,
+                         int32_t depth, int32_t V, const int32_t* draft_tokens,
+                         int32_t* accept_len, int32_t* committed, int32_t* req_status,
+                         void* stream);
+
+/*
+ * dspark_verify_ratio -- standard ratio verification with the dyadic q
+ * ("PP1 q transport and scheduling design": ratio tests and full-vocabulary
+ * residual sampling with the target p and the defined q; separate
+ * acceptance and correction/bonus RNG domains).
+ *
+ * p_j = softmax of target row j at T = 1 (-inf -> 0).  For j = 0, 1, ...:
+ *   c = q_j(x_j) (dense row or sparse lookup); c == 0 -> BAD_DRAFT;
+ *   U = Philox(seed; request id, j, ACCEPT) word 0 >> 8;
+ *   accept  <=>  U * c < p_j(x_j) * 2^48   (i.e. u < p/q with u = U / 2^24).
+ * At the first rejection L < depth the correction is drawn from
+ * max(p_L - q_L, 0) over all V tokens with w = Philox(seed; request id, L,
+ * RESIDUAL) word 0: t = w/2^32 * Z (Z the residual mass) and the token is the
+ * first id whose cumulative residual exceeds t.  If every draft is accepted
+ * the bonus is drawn the same way from p_depth with purpose BONUS at row
+ * depth.  committed as in dspark_verify_greedy.  Rows after the deciding
+ * row are not read.
+ * Refusals: draft id outside [0, V) or c == 0 at a tested row (BAD_DRAFT);
+ * NONFINITE / ZERO_MASS for a read target row; a sparse q row of a tested
+ * position that is not canonical (ids strictly ascending in [0, V), counts
+ * > 0, sum M) or a dense residual row whose counts do not sum to M (BAD_Q).
+ * p is computed in fp32 on the GPU: a decision with |u*q - p| <= 1e-6*q and a
+ * final draw within 1e-6 of a cumulative boundary may differ from exact
+ * arithmetic; such requests carry DSPARK_FLAG_* in flags[b] (flags may be
+ * NULL).
+ * Outputs: accept_len[B], committed[B][depth+1], flags[B], req_status[B].
+ */
+int dspark_verify_ratio(const void* target_logits, int32_t dtype, int64_t ld, int32_t B,
+                        int32_t depth, int32_t V, const int32_t* draft_tokens,
+                        const uint32_t* counts, const int32_t* sparse_ids, const int32_t* nnz,
+                        int32_t top_k, uint64_t seed, const uint32_t* request_ids,
+                        int32_t* accept_len, int32_t* committed, uint32_t* flags,
+                        int32_t* req_status, void* stream);
+
+/*
+ * dspark_target_probs -- the target distribution p of n_rows logit rows at
+ * T = 1 ("PP1 q transport and scheduling design": the full target p after
+ * the unchanged target processors, T = 1, top_p = 1), with the argmax
+ * (lowest id among maxima).  p_out[n_rows][V] fp32 (may be NULL),
+ * argmax[n_rows] (may be NULL), row_status[n_rows] (NONFINITE / ZERO_MASS
+ * as above; a refused row gets p = 0 and argmax -1).
+ */
+int dspark_target_probs(const void* target_logits, int32_t dtype, int64_t ld, int32_t n_rows,
+                        int32_t V, float* p_out, int32_t* argmax, int32_t* row_status,
+                        void* stream);
+
+/* Library build identifier (static string, host). */
+const char* dspark_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSPARK_H */

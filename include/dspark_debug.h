@@ -1,0 +1,40 @@
+/*
+ * dspark_debug.h -- element-wise entry points of libdspark.so that expose two
+ * building blocks of the q path for exhaustive checks against a reference:
+ * the deterministic exponential behind the draft weights and the Philox
+ * generator behind every draw.  Same conventions as dspark.h (device
+ * pointers, caller-owned buffers, asynchronous on `stream`, 0 / <0 / >0
+ * return codes).
+ */
+#ifndef DSPARK_DEBUG_H
+#define DSPARK_DEBUG_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * For each d[i] (fp32, d <= 0 is the meaningful range): e_out[i] =
+ * exp_ds(d[i]) and E_out[i] = floor(exp_ds(d[i]) * 2^40), the integer weight
+ * a draft token at distance d from the row maximum receives
+ * ("PP1 q transport and scheduling design", Distribution contract and
+ * precision: normalised draft weights; exp_ds is the library's fixed fp32
+ * exponential, see dspark_q_build).  Either output may be NULL.
+ */
+int dspark_debug_exp_weights(const float* d, int64_t n, float* e_out, uint64_t* E_out,
+                             void* stream);
+
+/*
+ * Philox4x32-10 (Salmon et al., SC'11) of n counters: out[i][0..3] =
+ * Philox(key = (seed low, seed high), counter = ctr[i][0..3]).
+ */
+int dspark_debug_philox(const uint32_t* ctr, uint64_t seed, int64_t n, uint32_t* out,
+                        void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSPARK_DEBUG_H */

@@ -384,13 +384,25 @@ void oracle_categorical_pick_many(const uint32_t* counts, const int32_t* ids,
 }
 
 /* Draft sample: D = (philox(seed; request, row, PROPOSAL) word 0) >> 8, the
- * top 24 bits of the 32-bit draw (reading Q7).  Returns the token or -1 if
- * the row's counts do not sum to M (BAD_Q). */
+ * top 24 bits of the 32-bit draw (reading Q7).  A row whose counts do not
+ * sum to M, or a sparse row (ids != NULL) that is not canonical -- at least
+ * one entry, ids strictly ascending in [0, V), every count > 0 -- is refused
+ * (BAD_Q, token -1), following the validation list of [TR-v2]. */
 int32_t oracle_draft_sample_row(const uint32_t* counts, const int32_t* ids,
-                                int32_t n, uint64_t seed, uint32_t request,
-                                uint32_t row, int32_t* status)
+                                int32_t n, int32_t V, uint64_t seed,
+                                uint32_t request, uint32_t row, int32_t* status)
 {
     uint64_t total = 0;
+    if (ids) {
+        if (n < 1) { *status = OR_BAD_Q; return -1; }
+        for (int32_t i = 0; i < n; ++i) {
+            if (ids[i] < 0 || ids[i] >= V || counts[i] == 0 ||
+                (i > 0 && ids[i] <= ids[i - 1])) {
+                *status = OR_BAD_Q;
+                return -1;
+            }
+        }
+    }
     for (int32_t i = 0; i < n; ++i) total += counts[i];
     if (total != (uint64_t)OR_M) { *status = OR_BAD_Q; return -1; }
     uint32_t D = oracle_draw_u32(seed, request, row, OR_PURPOSE_PROPOSAL) >> 8;

@@ -62,7 +62,7 @@ def lib():
                 "oracle_q_build": (None, [_P, _I64, _I32, _I32, _P, _I32, _P, _P, _P, _P]),
                 "oracle_categorical_pick": (_I32, [_P, _P, _I32, _U32]),
                 "oracle_categorical_pick_many": (None, [_P, _P, _I32, _P, _I64, _P]),
-                "oracle_draft_sample_row": (_I32, [_P, _P, _I32, _U64, _U32, _U32, _P]),
+                "oracle_draft_sample_row": (_I32, [_P, _P, _I32, _I32, _U64, _U32, _U32, _P]),
                 "oracle_target_row": (ctypes.c_int, [_P, _I32, _P, _P]),
                 "oracle_target_probs": (None, [_P, _I64, _I32, _I32, _P, _P, _P]),
                 "oracle_ratio_accept": (ctypes.c_int, [_U32, _U32, _F64]),
@@ -161,9 +161,11 @@ def categorical_pick_many(counts, D, ids=None):
     return out
 
 
-def draft_sample(counts, ids, nnz, top_k, B, depth, seed, request_ids=None):
-    """counts: dense [B*depth, V] or sparse [B*depth, top_k]."""
+def draft_sample(counts, ids, nnz, top_k, B, depth, seed, request_ids=None, V=None):
+    """counts: dense [B*depth, V] or sparse [B*depth, top_k] (then V is needed)."""
     counts = _c(counts, np.uint32)
+    if top_k == 0:
+        V = counts.shape[1]
     n_rows = B * depth
     req = np.arange(B, dtype=np.uint32) if request_ids is None else _c(request_ids, np.uint32)
     tokens = np.full(n_rows, -1, np.int32)
@@ -174,13 +176,16 @@ def draft_sample(counts, ids, nnz, top_k, B, depth, seed, request_ids=None):
         b, j = divmod(r, depth)
         if top_k > 0:
             n = int(nnz[r])
+            if n < 1 or n > top_k:
+                tokens[r], status[r] = -1, BAD_Q
+                continue
             c = _c(counts[r, :n], np.uint32)
             i = _c(ids[r, :n], np.int32)
-            tok = L.oracle_draft_sample_row(_ptr(c), _ptr(i), n, seed, int(req[b]), j,
+            tok = L.oracle_draft_sample_row(_ptr(c), _ptr(i), n, V, seed, int(req[b]), j,
                                             ctypes.byref(st))
         else:
             c = _c(counts[r], np.uint32)
-            tok = L.oracle_draft_sample_row(_ptr(c), None, c.size, seed, int(req[b]), j,
+            tok = L.oracle_draft_sample_row(_ptr(c), None, c.size, V, seed, int(req[b]), j,
                                             ctypes.byref(st))
         tokens[r] = tok
         status[r] = st.value

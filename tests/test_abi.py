@@ -1,0 +1,64 @@
+"""The C-ABI library builds for sm_103a, loads, exports every symbol the
+public headers declare, and refuses bad arguments on the host (negative
+return codes, nothing launched) -- no GPU needed."""
+import ctypes
+
+import pytest
+
+from draft_sampling_verification_gb300 import _lib, build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _lib.header_symbols()
+    assert set(names) >= {"dspark_q_build", "dspark_draft_sample", "dspark_verify_greedy",
+                          "dspark_verify_ratio", "dspark_target_probs", "dspark_version"}
+    for n in names:
+        assert hasattr(lib, n), n
+    assert b"dyadic24-standard-v1" in lib.dspark_version()
+
+
+def test_no_oracle_symbols_in_library(lib):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True,
+                         text=True).stdout
+    assert "oracle_" not in out
+
+
+P = ctypes.c_void_p(16)  # a non-null, aligned placeholder; never dereferenced
+
+
+def test_q_build_argument_errors(lib):
+    f = lib.dspark_q_build
+    assert f(P, 0, 8, 1, 0, None, 0, P, None, None, P, None) == -2      # V = 0
+    assert f(P, 0, 8, 1, 131073, None, 0, P, None, None, P, None) == -2  # V too large
+    assert f(P, 0, 4, 1, 8, None, 0, P, None, None, P, None) == -2      # ld < V
+    assert f(P, 7, 8, 1, 8, None, 0, P, None, None, P, None) == -3      # dtype
+    assert f(P, 0, 8, 1, 8, None, 9, P, None, None, P, None) == -4      # top_k > V
+    assert f(P, 0, 8, 1, 8, None, -1, P, None, None, P, None) == -4
+    assert f(None, 0, 8, 1, 8, None, 0, P, None, None, P, None) == -1   # null logits
+    assert f(P, 0, 8, 1, 8, None, 4, P, None, None, P, None) == -1      # sparse w/o ids
+    assert f(ctypes.c_void_p(18), 0, 8, 1, 8, None, 0, P, None, None, P, None) == -5
+    assert f(P, 0, 8, 0, 8, None, 0, None, None, None, None, None) == 0  # empty batch
+
+
+def test_sample_and_verify_argument_errors(lib):
+    assert lib.dspark_draft_sample(P, None, None, 0, 1, 0, 8, 0, None, P, P, None) == -2
+    assert lib.dspark_draft_sample(P, None, None, 0, 1, 9, 8, 0, None, P, P, None) == -2
+    assert lib.dspark_draft_sample(None, None, None, 0, 1, 5, 8, 0, None, P, P, None) == -1
+    assert lib.dspark_draft_sample(P, None, None, 0, 0, 5, 8, 0, None, P, P, None) == 0
+    assert lib.dspark_verify_greedy(P, 0, 8, 1, 0, 8, P, P, P, P, None) == -2
+    assert lib.dspark_verify_greedy(P, 1, 8, 1, 5, 8, None, P, P, P, None) == -1
+    assert lib.dspark_verify_greedy(P, 1, 8, 0, 5, 8, P, P, P, P, None) == 0
+    assert lib.dspark_verify_ratio(P, 0, 8, 1, 5, 8, P, None, None, None, 0, 0, None, P, P,
+                                   None, P, None) == -1
+    assert lib.dspark_verify_ratio(P, 0, 8, 1, 5, 8, P, P, None, None, 4, 0, None, P, P,
+                                   None, P, None) == -1
+    assert lib.dspark_target_probs(P, 0, 8, 1, 0, None, None, P, None) == -2
+    assert lib.dspark_debug_philox(P, 0, -1, P, None) == -2
+    assert lib.dspark_debug_exp_weights(None, 4, None, None, None) == -1

@@ -1,0 +1,172 @@
+"""GPU parity of q construction and the draft draw against the oracle:
+bit-exact counts, sparse ids, nnz, statuses and tokens, on random rows of
+many lengths (ragged slices, a single element, full vocabulary), strided and
+unaligned rows, bf16 logits, the degenerate and refused rows, and the draft
+rows of every workload."""
+import numpy as np
+import pytest
+import torch
+
+import draft_sampling_verification_gb300 as ds
+from draft_sampling_verification_gb300 import workloads as W
+from parity import compare_q, np_
+
+pytestmark = pytest.mark.gpu
+
+M = 1 << 24
+
+
+def rows_for(V, rng, n_each=2):
+    out = []
+    for _ in range(n_each):
+        out.append(rng.normal(0, 2, V))
+        out.append(rng.normal(0, 9, V))
+        z = -1.1 * np.log1p(rng.permutation(V)) + rng.normal(0, 0.3, V)
+        out.append(z)
+        zm = z.copy()
+        zm[rng.random(V) < 0.3] = -np.inf
+        if np.isfinite(zm).sum() == 0:
+            zm[0] = 0.0
+        out.append(zm)
+        out.append(np.round(rng.normal(0, 2, V) * 4) / 4)   # heavy exact ties
+    out.append(np.zeros(V))                                   # uniform row
+    one = np.full(V, -np.inf)
+    one[rng.integers(V)] = 3.0
+    out.append(one)                                           # one finite logit
+    return np.array(out, np.float32)
+
+
+def run_q(x, temps, top_k, ld_pad=0, dtype=torch.float32, offset=0):
+    n, V = x.shape
+    buf = torch.zeros(n * (V + ld_pad) + offset + 8, dtype=torch.float32, device="cuda")
+    view = buf[offset:offset + n * (V + ld_pad)].view(n, V + ld_pad)[:, :V]
+    view.copy_(torch.from_numpy(x))
+    if dtype == torch.bfloat16:
+        bb = torch.zeros(n * (V + ld_pad) + offset + 8, dtype=torch.bfloat16, device="cuda")
+        view = bb[offset:offset + n * (V + ld_pad)].view(n, V + ld_pad)[:, :V]
+        view.copy_(torch.from_numpy(x).to(torch.bfloat16))
+    t = None if temps is None else torch.from_numpy(np.asarray(temps, np.float32)).cuda()
+    q = ds.q_build(view, t, top_k)
+    torch.cuda.synchronize()
+    return q, view
+
+
+@pytest.mark.parametrize("V", [1, 2, 3, 8, 13, 257, 4099, 65537, 129280])
+@pytest.mark.parametrize("top_k", [0, 1, 16, 256])
+def test_q_build_random_rows(oracle, V, top_k):
+    if top_k > V:
+        pytest.skip("top_k > V")
+    rng = np.random.default_rng(V * 7 + top_k)
+    x = rows_for(V, rng, n_each=1 if V > 10000 else 2)
+    temps = rng.choice([1.0, 0.7, 1.3, 0.25], size=x.shape[0]).astype(np.float32)
+    q, _ = run_q(x, temps, top_k)
+    compare_q(q, oracle.q_build(x, temps, top_k))
+
+
+@pytest.mark.parametrize("ld_pad,offset", [(3, 1), (1, 2), (5, 3)])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_q_build_strided_unaligned(oracle, ld_pad, offset, dtype):
+    rng = np.random.default_rng(ld_pad + 10 * offset)
+    V = 4099
+    x = rows_for(V, rng, n_each=1)
+    q, view = run_q(x, None, 0, ld_pad=ld_pad, dtype=dtype, offset=offset)
+    xr = view.float().cpu().numpy()  # bf16 widened exactly
+    compare_q(q, oracle.q_build(xr, None, 0))
+    qs, _ = run_q(x, None, 64, ld_pad=ld_pad, dtype=dtype, offset=offset)
+    compare_q(qs, oracle.q_build(xr, None, 64))
+
+
+def test_q_build_uniform_full_vocab_closed_form():
+    V = 129280
+    q, _ = run_q(np.zeros((3, V), np.float32), [1.0, 0.5, 2.0], 0)
+    c = np_(q["counts"])
+    expect = np.full(V, 129, np.int64)
+    expect[:100096] += 1
+    for r in range(3):
+        assert np.array_equal(c[r], expect)
+    assert np.all(np_(q["status"]) == 0)
+
+
+def test_q_build_refusals(oracle):
+    V = 5000
+    rng = np.random.default_rng(3)
+    x = rng.normal(0, 2, (6, V)).astype(np.float32)
+    x[0, 17] = np.nan
+    x[1, 4999] = np.inf
+    x[2, :] = -np.inf
+    x[3, 5] = 3e38
+    temps = np.array([1.0, 1.0, 1.0, 0.5, 0.0, np.inf], np.float32)
+    for top_k in (0, 32):
+        q, _ = run_q(x, temps, top_k)
+        ref = oracle.q_build(x, temps, top_k)
+        compare_q(q, ref)
+        assert np_(q["status"]).tolist() == [1, 1, 2, 1, 4, 4]
+        assert np_(q["counts"]).sum() == 0
+
+
+def test_q_build_batch_invariance():
+    rng = np.random.default_rng(9)
+    V = 129280
+    x = rows_for(V, rng, n_each=1)
+    full, _ = run_q(x, None, 0)
+    for r in (0, 3, x.shape[0] - 1):
+        alone, _ = run_q(x[r:r + 1], None, 0)
+        assert torch.equal(alone["counts"][0], full["counts"][r])
+
+
+WORKLOADS = [
+    ("c1", {}), ("c2", {}), ("c3", {"B": 8}), ("c4", {"B": 24}),
+    ("c5", {"B": 4, "variant": "accept"}), ("c5", {"B": 4, "variant": "reject"}),
+    ("c5", {"B": 4, "variant": "mixed", "top_k": 0}),
+]
+
+
+def _wl(name, kw):
+    if name == "c5":
+        return W.config5(**kw)
+    return {"c1": W.config1, "c2": W.config2, "c3": W.config3, "c4": W.config4}[name](**kw)
+
+
+@pytest.mark.parametrize("name,kw", WORKLOADS)
+def test_workload_q_and_draft_sample(oracle, name, kw):
+    wl = _wl(name, kw)
+    x = wl.draft.reshape(wl.B * wl.depth, wl.V)
+    q, _ = run_q(x, wl.temperature, wl.top_k)
+    ref = oracle.q_build(x, wl.temperature, wl.top_k)
+    compare_q(q, ref)
+    req = torch.from_numpy(wl.request_ids.view(np.int32)).cuda()
+    tok, st = ds.draft_sample(q, wl.B, wl.depth, wl.V, wl.seed, req)
+    rtok, rst = oracle.draft_sample(ref[0], ref[1], ref[2], wl.top_k, wl.B, wl.depth, wl.seed,
+                                    wl.request_ids, V=wl.V)
+    assert np.array_equal(np_(st).ravel(), rst)
+    assert np.array_equal(np_(tok).ravel(), rtok)
+
+
+def test_draft_sample_refuses_bad_rows(oracle):
+    V, depth = 300, 2
+    counts = np.zeros((4, V), np.uint32)
+    counts[:, 7] = M
+    counts[1, 7] -= 1                      # wrong mass
+    counts[2, 7] = M // 2
+    counts[2, 299] = M // 2
+    counts[3, :] = M // V
+    counts[3, :M - (M // V) * V] += 1
+    ct = torch.from_numpy(counts.view(np.int32)).cuda()
+    q = {"counts": ct, "ids": None, "nnz": None, "top_k": 0}
+    tok, st = ds.draft_sample(q, 2, depth, V, 123)
+    rtok, rst = oracle.draft_sample(counts, None, None, 0, 2, depth, 123)
+    assert np.array_equal(np_(st).ravel(), rst) and rst.tolist()[:2] == [0, 5]
+    assert np.array_equal(np_(tok).ravel(), rtok)
+    # sparse: unsorted ids, zero count, nnz out of range, out-of-range id
+    ids = np.array([[3, 9, -1, -1], [9, 3, -1, -1], [3, 9, -1, -1], [3, 9, 12, -1],
+                    [3, 400, -1, -1], [5, -1, -1, -1]], np.int32)
+    sc = np.array([[M - 5, 5, 0, 0], [M - 5, 5, 0, 0], [M, 0, 0, 0], [1, 2, M - 3, 0],
+                   [M - 1, 1, 0, 0], [M, 0, 0, 0]], np.uint32)
+    nnz = np.array([2, 2, 2, 3, 2, 0], np.int32)
+    q = {"counts": torch.from_numpy(sc.view(np.int32)).cuda(),
+         "ids": torch.from_numpy(ids).cuda(), "nnz": torch.from_numpy(nnz).cuda(), "top_k": 4}
+    tok, st = ds.draft_sample(q, 3, 2, V, 77)
+    rtok, rst = oracle.draft_sample(sc, ids, nnz, 4, 3, 2, 77, V=V)
+    assert rst.tolist() == [0, 5, 5, 0, 5, 5]
+    assert np.array_equal(np_(st).ravel(), rst)
+    assert np.array_equal(np_(tok).ravel(), rtok)
