@@ -48,6 +48,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="c4")
+    ap.add_argument("--batch", type=int, default=0, help="override B (requests per GPU)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -77,7 +78,7 @@ class ClockSampler:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
                 stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -149,7 +150,7 @@ def run_ours(args, rank, world, local_rank):
     dsbuild.build()
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    wl = W.by_name(args.workload)
+    wl = W.by_name(args.workload, **({"B": args.batch} if args.batch else {}))
     B, depth, V = wl.B, wl.depth, wl.V
     req_np = (wl.request_ids + np.uint32(rank * B)).astype(np.uint32)
 

@@ -417,7 +417,7 @@ __global__ void __cluster_dims__(kQCluster, 1, 1) __launch_bounds__(kQThreads, 2
         if (acc != kk) bad_gather = 1;
       }
       __syncthreads();
-      const int nsup = (int)min(base_of[kQCluster], (uint32_t)DSPARK_MAX_TOPK);
+      const int nsup = bad_gather ? 0 : (int)base_of[kQCluster];
       if (!bad_gather) {
         for (int r = 0; r < kQCluster; ++r) {
           const Sup* rs = cluster.map_shared_rank(&sh.sup[0], r);

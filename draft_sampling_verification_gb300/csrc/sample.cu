@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(kSThreads) draft_sample_kernel(SParams p) {
         if ((uint64_t)D < base + tile) {
           const bool hit = (base + incl > (uint64_t)D) && (base + incl - c <= (uint64_t)D);
           const unsigned m = __ballot_sync(0xffffffffu, hit && c > 0u);
-          if (lane == 0) result = v0 + __ffs(m) - 1;
+          if (lane == 0 && m) result = v0 + __ffs(m) - 1;
           break;
         }
         base += tile;
@@ -113,7 +113,7 @@ __global__ void __launch_bounds__(kSThreads) draft_sample_kernel(SParams p) {
           if ((uint64_t)D < base + tile) {
             const bool hit = (base + incl > (uint64_t)D) && (base + incl - c <= (uint64_t)D);
             const unsigned m = __ballot_sync(0xffffffffu, hit && c > 0u);
-            if (lane == 0) result = ids[i0 + __ffs(m) - 1];
+            if (lane == 0 && m) result = ids[i0 + __ffs(m) - 1];
             break;
           }
           base += tile;

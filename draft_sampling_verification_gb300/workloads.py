@@ -234,11 +234,12 @@ def config5(B, variant="mixed", top_k=TOP_K, V=V_FULL, depth=DEPTH, rng=None):
 
 
 def by_name(name: str, **kw) -> Workload:
-    """'c1'..'c4', or 'c5:<B>:<variant>:<sparse|dense>'."""
+    """'c1'..'c4', or 'c5:<B>:<variant>:<sparse|dense>'; keyword B overrides the batch."""
     name = name.lower()
     if name.startswith("c5"):
         parts = name.split(":")
         B = int(parts[1]) if len(parts) > 1 else 1024
+        B = kw.pop("B", B)
         variant = parts[2] if len(parts) > 2 else "mixed"
         q = parts[3] if len(parts) > 3 else "sparse"
         return config5(B, variant=variant, top_k=TOP_K if q == "sparse" else 0, **kw)

@@ -71,17 +71,19 @@ def oracle_verify(wl, mode, drafts, qref):
 
 
 def compare_verify(gpu, ref, mode):
-    """Returns (n_mismatch_unflagged, n_flagged, n_rows).  Integer outputs must
-    match bit for bit, except ratio requests carrying an ambiguity flag on
-    either side (a decision or draw inside the stated 1e-6 band)."""
+    """Returns (unflagged mismatches, flagged mismatches, flagged requests,
+    requests).  Integer outputs must match bit for bit, except on ratio
+    requests that either side flags (a decision with |u*q - p| <= 1e-6*q, or
+    a final draw within 1e-6 of a cumulative boundary)."""
     ga, gc, gf, gs = [np_(x) for x in gpu]
     ra, rc, rf, rs = ref
     if mode == "greedy":
         assert np.array_equal(gs, rs)
         assert np.array_equal(ga, ra)
         assert np.array_equal(gc, rc)
-        return 0, 0, ga.size
+        return 0, 0, 0, ga.size
     gf = gf.view(np.uint32)
     flagged = ((gf & 3) != 0) | ((rf & 3) != 0)
     same = (ga == ra) & (gc == rc).all(axis=1) & (gs == rs)
-    return int((~same & ~flagged).sum()), int(flagged.sum()), ga.size
+    return (int((~same & ~flagged).sum()), int((~same & flagged).sum()), int(flagged.sum()),
+            ga.size)
