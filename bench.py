@@ -1,8 +1,9 @@
 """Benchmark of the draft-sampling / verification hot path on GB300.
 
-One step = the whole path over one batch: dspark_q_build (dyadic24 q from
-the draft logits), dspark_draft_sample, and the verification modes of the
-workload (dspark_verify_greedy and/or dspark_verify_ratio).  Default workload:
+One step = the whole path over one batch: dspark_q_build_sample (the dyadic24
+q from the draft logits and the draft draw from it, one launch), then the
+verification modes of the workload (dspark_verify_greedy and/or
+dspark_verify_ratio).  Default workload:
 C4 -- B = 256 requests, depth 5, V = 129,280, fp32 draft / bf16 target logits,
 Zipf rows with 10 % grammar masks and 1 % tied-remainder rows, dense q,
 greedy and ratio verification (every step of the path but the top-k support,
@@ -122,15 +123,14 @@ def algorithmic_bytes(wl, acc_greedy, acc_ratio):
     R_d = wl.B * wl.depth
     V = wl.V
     esz_t = 4 if wl.target_dtype == "f32" else 2
+    # q build + draw: draft logits read, q written, tokens written
     if wl.top_k > 0:
-        q_bytes = R_d * V * 4 + R_d * (wl.top_k * 8 + 4)
-        sample_bytes = R_d * (wl.top_k * 8 + 4)
+        q_bytes = R_d * V * 4 + R_d * (wl.top_k * 8 + 4) + R_d * 4
         q_row = wl.top_k * 8 + 4
     else:
-        q_bytes = R_d * V * 4 * 2
-        sample_bytes = R_d * V * 4
+        q_bytes = R_d * V * 4 * 2 + R_d * 4
         q_row = V * 4
-    out = {"q_build": q_bytes, "draft_sample": sample_bytes}
+    out = {"q_build_sample": q_bytes}
     if acc_greedy is not None:
         out["verify_greedy"] = int(((acc_greedy + 1) * V * esz_t).sum())
     if acc_ratio is not None:
@@ -179,17 +179,15 @@ def run_ours(args, rank, world, local_rank):
                 torch.empty(B, dtype=torch.int32, device=dev),
                 torch.empty(B, dtype=torch.int32, device=dev)) for m in wl.modes}
     stream = torch.cuda.current_stream(dev)
-    kernels = ["q_build", "draft_sample"] + ["verify_" + m for m in wl.modes]
+    kernels = ["q_build_sample"] + ["verify_" + m for m in wl.modes]
+    sst.zero_()
 
     def step(x_d, x_t, marks=None):
         if marks:
             marks[0].record(stream)
-        ds.dspark_q_build(x_d, temps, top_k, counts, ids, nnz, qst, stream)
-        if marks:
-            marks[1].record(stream)
-        ds.dspark_draft_sample(counts, ids, nnz, top_k, B, depth, V, wl.seed, req, tok, sst,
-                               stream)
-        k = 2
+        ds.dspark_q_build_sample(x_d, B, depth, temps, top_k, wl.seed, req, counts, ids, nnz,
+                                 tok, qst, stream)
+        k = 1
         if marks:
             marks[k].record(stream)
         for m in wl.modes:

@@ -23,9 +23,9 @@ ST_OK, ST_NONFINITE, ST_ZERO_MASS, ST_ALLOC_INCONSISTENT = 0, 1, 2, 3
 ST_BAD_TEMPERATURE, ST_BAD_Q, ST_BAD_DRAFT, ST_TIMEOUT, ST_INTERNAL = 4, 5, 6, 7, 8
 FLAG_AMBIG_ACCEPT, FLAG_NEAR_BOUNDARY, FLAG_DEGENERATE = 1, 2, 4
 
-__all__ = ["dspark_q_build", "dspark_draft_sample", "dspark_verify_greedy",
+__all__ = ["dspark_q_build", "dspark_q_build_sample", "dspark_draft_sample", "dspark_verify_greedy",
            "dspark_verify_ratio", "dspark_target_probs", "q_build", "draft_sample",
-           "verify_greedy", "verify_ratio", "target_probs", "version"]
+           "verify_greedy", "verify_ratio", "target_probs", "q_build_sample", "version"]
 
 
 def version() -> str:
@@ -93,6 +93,17 @@ def dspark_q_build(draft_logits, temperature, top_k, counts, sparse_ids, nnz, ro
           _i32(row_status), _stream(stream))
 
 
+def dspark_q_build_sample(draft_logits, B, depth, temperature, top_k, seed, request_ids, counts,
+                          sparse_ids, nnz, draft_tokens, row_status, stream=None):
+    rows, V, ld = _rows(draft_logits)
+    if rows != B * depth:
+        raise ValueError("draft_logits must hold B*depth rows")
+    _call("dspark_q_build_sample", _ptr(draft_logits), _dtype_code(draft_logits), ld, int(B),
+          int(depth), V, _ptr(temperature), int(top_k), int(seed) & (2 ** 64 - 1),
+          _i32(request_ids), _i32(counts), _i32(sparse_ids), _i32(nnz), _i32(draft_tokens),
+          _i32(row_status), _stream(stream))
+
+
 def dspark_draft_sample(counts, sparse_ids, nnz, top_k, B, depth, V, seed, request_ids,
                         draft_tokens, row_status, stream=None):
     _call("dspark_draft_sample", _i32(counts), _i32(sparse_ids), _i32(nnz), int(top_k), int(B),
@@ -147,6 +158,25 @@ def q_build(draft_logits, temperature=None, top_k=0, stream=None):
     status = _empty((rows,), torch.int32, dev)
     dspark_q_build(draft_logits, temperature, top_k, counts, ids, nnz, status, stream)
     return {"counts": counts, "ids": ids, "nnz": nnz, "status": status, "top_k": top_k}
+
+
+def q_build_sample(draft_logits, B, depth, seed, temperature=None, top_k=0, request_ids=None,
+                   stream=None):
+    """Fused q build + draft draw; returns (q dict, tokens [B, depth])."""
+    rows, V, _ = _rows(draft_logits)
+    dev = draft_logits.device
+    if top_k > 0:
+        counts = _empty((rows, top_k), torch.int32, dev)
+        ids = _empty((rows, top_k), torch.int32, dev)
+        nnz = _empty((rows,), torch.int32, dev)
+    else:
+        counts = _empty((rows, V), torch.int32, dev)
+        ids = nnz = None
+    status = _empty((rows,), torch.int32, dev)
+    tokens = _empty((B, depth), torch.int32, dev)
+    dspark_q_build_sample(draft_logits, B, depth, temperature, top_k, seed, request_ids, counts,
+                          ids, nnz, tokens, status, stream)
+    return {"counts": counts, "ids": ids, "nnz": nnz, "status": status, "top_k": top_k}, tokens
 
 
 def draft_sample(q, B, depth, V, seed, request_ids=None, stream=None):

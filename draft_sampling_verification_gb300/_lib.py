@@ -21,6 +21,8 @@ _I32, _I64, _U64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64
 SIGNATURES = {
     "dspark_q_build": [_P, _I32, _I64, _I32, _I32, _P, _I32, _P, _P, _P, _P, _P],
     "dspark_draft_sample": [_P, _P, _P, _I32, _I32, _I32, _I32, _U64, _P, _P, _P, _P],
+    "dspark_q_build_sample": [_P, _I32, _I64, _I32, _I32, _I32, _P, _I32, _U64, _P, _P, _P, _P,
+                              _P, _P, _P],
     "dspark_verify_greedy": [_P, _I32, _I64, _I32, _I32, _I32, _P, _P, _P, _P, _P],
     "dspark_verify_ratio": [_P, _I32, _I64, _I32, _I32, _I32, _P, _P, _P, _P, _I32, _U64, _P,
                             _P, _P, _P, _P, _P],

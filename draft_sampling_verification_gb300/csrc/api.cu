@@ -9,7 +9,8 @@
 namespace dspark {
 cudaError_t launch_q_build(const void* x, int dtype, int64_t ld, int n_rows, int V,
                            const float* temperature, int top_k, uint32_t* counts, int32_t* ids,
-                           int32_t* nnz, int32_t* status, cudaStream_t stream);
+                           int32_t* nnz, int32_t* status, int32_t* tokens, uint64_t seed,
+                           const uint32_t* request_ids, int depth, cudaStream_t stream);
 cudaError_t launch_draft_sample(const uint32_t* counts, const int32_t* ids, const int32_t* nnz,
                                 int top_k, int B, int depth, int V, uint64_t seed,
                                 const uint32_t* request_ids, int32_t* tokens, int32_t* status,
@@ -66,7 +67,30 @@ int dspark_q_build(const void* draft_logits, int32_t dtype, int64_t ld, int32_t 
       (nnz && !aligned(nnz, 4)))
     return DSPARK_ERR_ALIGN;
   return launch_result(dspark::launch_q_build(draft_logits, dtype, ld, n_rows, V, temperature,
+                                              top_k, counts, sparse_ids, nnz, row_status, nullptr,
+                                              0ull, nullptr, 1, static_cast<cudaStream_t>(stream)));
+}
+
+int dspark_q_build_sample(const void* draft_logits, int32_t dtype, int64_t ld, int32_t B,
+                          int32_t depth, int32_t V, const float* temperature, int32_t top_k,
+                          uint64_t seed, const uint32_t* request_ids, uint32_t* counts,
+                          int32_t* sparse_ids, int32_t* nnz, int32_t* draft_tokens,
+                          int32_t* row_status, void* stream) {
+  if (int e = check_common(dtype, V, ld)) return e;
+  if (int e = check_topk(top_k, V)) return e;
+  if (depth < 1 || depth > DSPARK_MAX_DEPTH) return DSPARK_ERR_SIZE;
+  if (B < 0 || (int64_t)B * depth > kMaxGridRows) return DSPARK_ERR_SIZE;
+  if (B == 0) return 0;
+  if (!draft_logits || !counts || !row_status || !draft_tokens) return DSPARK_ERR_NULL;
+  if (top_k > 0 && (!sparse_ids || !nnz)) return DSPARK_ERR_NULL;
+  if (!aligned(draft_logits, esize(dtype)) || !aligned(counts, 4) || !aligned(row_status, 4) ||
+      !aligned(draft_tokens, 4) || (temperature && !aligned(temperature, 4)) ||
+      (sparse_ids && !aligned(sparse_ids, 4)) || (nnz && !aligned(nnz, 4)) ||
+      (request_ids && !aligned(request_ids, 4)))
+    return DSPARK_ERR_ALIGN;
+  return launch_result(dspark::launch_q_build(draft_logits, dtype, ld, B * depth, V, temperature,
                                               top_k, counts, sparse_ids, nnz, row_status,
+                                              draft_tokens, seed, request_ids, depth,
                                               static_cast<cudaStream_t>(stream)));
 }
 

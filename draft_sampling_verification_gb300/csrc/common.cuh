@@ -64,9 +64,18 @@ constexpr float kInvFact5 = 0x1.111112p-7f;
 constexpr float kInvFact6 = 0x1.6c16c2p-10f;
 constexpr float kInvFact7 = 0x1.a01a02p-13f;
 
-__device__ __forceinline__ float exp_ds_poly(float d, int* n_out) {
-  const float t = __fmul_rn(d, kL2E);
-  const float n = rintf(t);
+// rint(t) for |t| < 2^22 by adding and removing 1.5 * 2^23 (each addition
+// rounds to nearest, ties to even, exactly once); *ni gets rint(t) as int.
+__device__ __forceinline__ float rint_magic(float t, int* ni) {
+  const float tm = __fadd_rn(t, 12582912.0f);
+  *ni = __float_as_int(tm) - 0x4B400000;
+  return __fsub_rn(tm, 12582912.0f);
+}
+
+__device__ __forceinline__ float exp_ds(float d) {
+  if (!(d >= -87.0f)) return 0.0f;
+  int ni;
+  const float n = rint_magic(__fmul_rn(d, kL2E), &ni);
   float r = __fmaf_rn(-n, kLn2Hi, d);
   r = __fmaf_rn(-n, kLn2Lo, r);
   float p = kInvFact7;
@@ -77,15 +86,9 @@ __device__ __forceinline__ float exp_ds_poly(float d, int* n_out) {
   p = __fmaf_rn(p, r, kInvFact2);
   p = __fmaf_rn(p, r, 1.0f);
   p = __fmaf_rn(p, r, 1.0f);
-  *n_out = (int)n;
-  return p;
-}
-
-__device__ __forceinline__ float exp_ds(float d) {
-  if (!(d >= -87.0f)) return 0.0f;
-  int n;
-  const float p = exp_ds_poly(d, &n);
-  return __fmul_rn(p, __int_as_float((127 + n) << 23));
+  // p * 2^n: p is in [0.7, 1.42) and the result stays normal for d >= -87,
+  // so the scaling is an exact add to the exponent field
+  return __int_as_float(__float_as_int(p) + (ni << 23));
 }
 
 // Integer weight E = floor(exp_ds(d) * 2^40) of a token at distance d <= 0
@@ -110,6 +113,24 @@ __device__ __forceinline__ void weight_split(float e, uint32_t* Ei, int* se) {
     *se = sh;
   } else {
     *Ei = p24 >> (-sh);
+    *se = 0;
+  }
+}
+
+// E as (Ei, se) from its exact float value Ef (an integer < 2^41 with at most
+// 24 significant bits): E = Ei << se.
+__device__ __forceinline__ void weight_split_ef(float Ef, uint32_t* Ei, int* se) {
+  const uint32_t b = __float_as_uint(Ef);
+  const int ex = (int)(b >> 23);
+  const uint32_t m24 = (b & 0x7FFFFFu) | 0x800000u;
+  if (Ef == 0.0f) {
+    *Ei = 0u;
+    *se = 0;
+  } else if (ex >= 150) {
+    *Ei = m24;
+    *se = ex - 150;
+  } else {
+    *Ei = m24 >> (150 - ex);  // exact: Ef is an integer
     *se = 0;
   }
 }
@@ -288,6 +309,76 @@ __device__ __forceinline__ uint64_t block_inclusive_scan_u64(uint64_t v, uint64_
   }
   *total = all;
   return v + before;
+}
+
+// -------------------------------------------------- TMA bulk copy, mbarrier
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
+// global memory into this CTA's shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_bulk(void* dst, const void* src, uint32_t bytes,
+                                              uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// One try_wait with a suspend-time hint: the thread may sleep in hardware
+// (up to the hint) until the phase completes instead of spinning.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t phase) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(phase), "r"(1000000u)
+      : "memory");
+  return ok != 0u;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Waits for phase `phase` of `bar` for at most kWaitLimitNs; false on timeout.
+// Between polls the thread sleeps with an exponential backoff (64 ns .. 1 us),
+// so a waiting warp takes almost no issue slots from the rest of the SM.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t phase) {
+  if (mbar_try_wait(bar, phase)) return true;
+  const uint64_t t0 = global_ns();
+  uint32_t nap = 64;
+  while (global_ns() - t0 < kWaitLimitNs) {
+    __nanosleep(nap);
+    if (mbar_try_wait(bar, phase)) return true;
+    nap = nap < 1024u ? 2u * nap : 1024u;
+  }
+  return false;
+}
+
+// Float holding an integer in [0, 2^23) to int, by the 2^23 offset trick.
+__device__ __forceinline__ int small_float_to_int(float v) {
+  return __float_as_int(__fadd_rn(v, 8388608.0f)) - 0x4B000000;
 }
 
 }  // namespace dspark

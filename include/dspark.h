@@ -132,6 +132,21 @@ int dspark_q_build(const void* draft_logits, int32_t dtype, int64_t ld, int32_t 
                    int32_t* sparse_ids, int32_t* nnz, int32_t* row_status, void* stream);
 
 /*
+ * dspark_q_build_sample -- dspark_q_build of the B*depth draft rows followed
+ * by the draft draw of dspark_draft_sample, in one launch: the draw runs on
+ * the counts while they are still on chip, so the counts are not read back.
+ * Outputs (counts, sparse_ids, nnz, draft_tokens[B*depth], row_status) are
+ * exactly those of the two calls in sequence with the same arguments; a
+ * refused row gets token -1.  Same limits as the two calls (1 <= depth <=
+ * DSPARK_MAX_DEPTH).
+ */
+int dspark_q_build_sample(const void* draft_logits, int32_t dtype, int64_t ld, int32_t B,
+                          int32_t depth, int32_t V, const float* temperature, int32_t top_k,
+                          uint64_t seed, const uint32_t* request_ids, uint32_t* counts,
+                          int32_t* sparse_ids, int32_t* nnz, int32_t* draft_tokens,
+                          int32_t* row_status, void* stream);
+
+/*
  * dspark_draft_sample -- one token per draft row from its q
  * ("PP1 q transport and scheduling design", Distribution contract and
  * precision: "a uniform 24-bit integer and exact integer cumulative counts

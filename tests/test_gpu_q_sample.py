@@ -140,6 +140,38 @@ def test_workload_q_and_draft_sample(oracle, name, kw):
                                     wl.request_ids, V=wl.V)
     assert np.array_equal(np_(st).ravel(), rst)
     assert np.array_equal(np_(tok).ravel(), rtok)
+    # the fused entry: same counts and the same draws in one launch
+    d = torch.from_numpy(np.ascontiguousarray(wl.draft)).cuda()
+    temps = torch.from_numpy(wl.temperature).cuda()
+    qf, ftok = ds.q_build_sample(d, wl.B, wl.depth, wl.seed, temps, wl.top_k, req)
+    torch.cuda.synchronize()
+    compare_q(qf, ref)
+    assert np.array_equal(np_(ftok).ravel(), rtok)
+
+
+@pytest.mark.parametrize("V", [1, 3, 257, 4099])
+@pytest.mark.parametrize("top_k", [0, 2, 64])
+def test_fused_sample_small_and_refused(oracle, V, top_k):
+    if top_k > V:
+        pytest.skip("top_k > V")
+    rng = np.random.default_rng(V + top_k)
+    B, depth = 3, 4
+    x = rows_for(V, rng, n_each=1)[: B * depth]
+    while x.shape[0] < B * depth:
+        x = np.concatenate([x, rng.normal(0, 1, (1, V)).astype(np.float32)])
+    x[5, 0] = np.nan          # a refused row inside the batch
+    temps = np.ones(B * depth, np.float32)
+    temps[7] = 0.0            # another one
+    req = np.array([5, 0, 77], np.uint32)
+    xt = torch.from_numpy(x).cuda()
+    qf, ftok = ds.q_build_sample(xt, B, depth, 1234, torch.from_numpy(temps).cuda(), top_k,
+                                 torch.from_numpy(req.view(np.int32)).cuda())
+    torch.cuda.synchronize()
+    ref = oracle.q_build(x, temps, top_k)
+    compare_q(qf, ref)
+    rtok, rst = oracle.draft_sample(ref[0], ref[1], ref[2], top_k, B, depth, 1234, req, V=V)
+    rtok = np.where(ref[3] == 0, rtok, -1)
+    assert np.array_equal(np_(ftok).ravel(), rtok)
 
 
 def test_draft_sample_refuses_bad_rows(oracle):
