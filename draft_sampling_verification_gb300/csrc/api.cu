@@ -11,6 +11,10 @@ cudaError_t launch_q_build(const void* x, int dtype, int64_t ld, int n_rows, int
                            const float* temperature, int top_k, uint32_t* counts, int32_t* ids,
                            int32_t* nnz, int32_t* status, int32_t* tokens, uint64_t seed,
                            const uint32_t* request_ids, int depth, cudaStream_t stream);
+cudaError_t launch_q_dense(const void* x, int dtype, int64_t ld, int n_rows, int V,
+                           const float* temperature, uint32_t* counts, int32_t* status,
+                           int32_t* tokens, uint64_t seed, const uint32_t* request_ids, int depth,
+                           cudaStream_t stream);
 cudaError_t launch_draft_sample(const uint32_t* counts, const int32_t* ids, const int32_t* nnz,
                                 int top_k, int B, int depth, int V, uint64_t seed,
                                 const uint32_t* request_ids, int32_t* tokens, int32_t* status,
@@ -66,6 +70,10 @@ int dspark_q_build(const void* draft_logits, int32_t dtype, int64_t ld, int32_t 
       (temperature && !aligned(temperature, 4)) || (sparse_ids && !aligned(sparse_ids, 4)) ||
       (nnz && !aligned(nnz, 4)))
     return DSPARK_ERR_ALIGN;
+  if (top_k == 0)
+    return launch_result(dspark::launch_q_dense(draft_logits, dtype, ld, n_rows, V, temperature,
+                                                counts, row_status, nullptr, 0ull, nullptr, 1,
+                                                static_cast<cudaStream_t>(stream)));
   return launch_result(dspark::launch_q_build(draft_logits, dtype, ld, n_rows, V, temperature,
                                               top_k, counts, sparse_ids, nnz, row_status, nullptr,
                                               0ull, nullptr, 1, static_cast<cudaStream_t>(stream)));
@@ -88,6 +96,11 @@ int dspark_q_build_sample(const void* draft_logits, int32_t dtype, int64_t ld, i
       (sparse_ids && !aligned(sparse_ids, 4)) || (nnz && !aligned(nnz, 4)) ||
       (request_ids && !aligned(request_ids, 4)))
     return DSPARK_ERR_ALIGN;
+  if (top_k == 0)
+    return launch_result(dspark::launch_q_dense(draft_logits, dtype, ld, B * depth, V, temperature,
+                                                counts, row_status, draft_tokens, seed,
+                                                request_ids, depth,
+                                                static_cast<cudaStream_t>(stream)));
   return launch_result(dspark::launch_q_build(draft_logits, dtype, ld, B * depth, V, temperature,
                                               top_k, counts, sparse_ids, nnz, row_status,
                                               draft_tokens, seed, request_ids, depth,

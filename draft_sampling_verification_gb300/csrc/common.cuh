@@ -72,8 +72,10 @@ __device__ __forceinline__ float rint_magic(float t, int* ni) {
   return __fsub_rn(tm, 12582912.0f);
 }
 
-__device__ __forceinline__ float exp_ds(float d) {
-  if (!(d >= -87.0f)) return 0.0f;
+// exp_ds(d) * 2^k for d in [-87, 0]: the scaling by 2^(n + k) is an exact
+// add to the exponent field of p (p is in [0.7, 1.42)), valid while the
+// result stays a normal float, i.e. n + k >= -126.
+__device__ __forceinline__ float exp_ds_pow2(float d, int k) {
   int ni;
   const float n = rint_magic(__fmul_rn(d, kL2E), &ni);
   float r = __fmaf_rn(-n, kLn2Hi, d);
@@ -86,9 +88,18 @@ __device__ __forceinline__ float exp_ds(float d) {
   p = __fmaf_rn(p, r, kInvFact2);
   p = __fmaf_rn(p, r, 1.0f);
   p = __fmaf_rn(p, r, 1.0f);
-  // p * 2^n: p is in [0.7, 1.42) and the result stays normal for d >= -87,
-  // so the scaling is an exact add to the exponent field
-  return __int_as_float(__float_as_int(p) + (ni << 23));
+  return __int_as_float(__float_as_int(p) + ((ni + k) << 23));
+}
+
+__device__ __forceinline__ float exp_ds(float d) {
+  if (!(d >= -87.0f)) return 0.0f;
+  return exp_ds_pow2(d, 0);
+}
+
+// floor(exp_ds(d) * 2^40) as an exact float for any d <= 0 (or -inf): the
+// distance is clamped at -30, where, as everywhere below -28, the weight is 0.
+__device__ __forceinline__ float weight40(float d) {
+  return floorf(exp_ds_pow2(fmaxf(d, -30.0f), 40));
 }
 
 // Integer weight E = floor(exp_ds(d) * 2^40) of a token at distance d <= 0

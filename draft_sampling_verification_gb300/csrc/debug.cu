@@ -10,7 +10,8 @@ __global__ void exp_weights_kernel(const float* d, int64_t n, float* e_out, uint
        i += (int64_t)gridDim.x * blockDim.x) {
     const float e = dspark::exp_ds(d[i]);
     if (e_out) e_out[i] = e;
-    if (E_out) E_out[i] = dspark::weight_u64(dspark::weight_float(d[i]));
+    // the weight as the q kernels compute it: floor(exp_ds(d) * 2^40), exact
+    if (E_out) E_out[i] = __float2ull_rz(dspark::weight40(d[i]));
   }
 }
 

@@ -119,8 +119,8 @@ def _float_range(lo, hi, step):
 @pytest.mark.parametrize("lo,hi,step", [(-0.0, -1.0, 31), (-1.0, -28.0, 29), (-28.0, -87.5, 7)])
 def test_library_exp_weights_bit_exact(oracle, lo, hi, step):
     d = _float_range(lo, hi, step)
-    d = np.concatenate([d, np.array([0.0, -0.0, -np.inf, -87.0, -28.0, -27.999998],
-                                    np.float32)])
+    d = np.concatenate([d, np.array([0.0, -0.0, -np.inf, -87.0, -28.0, -27.999998, -30.0,
+                                     -29.999998, -100.0, -1e30, -3.4e38], np.float32)])
     e, E = lib_weights(d)
     ref = oracle.exp_ds(d)
     assert np.array_equal(e.view(np.uint32), ref.view(np.uint32))
