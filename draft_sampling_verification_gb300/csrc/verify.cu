@@ -200,54 +200,98 @@ __device__ RowStat slice_stat(const void* row, int dtype, int lo, int n, VShared
   return block_stat(st, sh);
 }
 
-__device__ __forceinline__ const void* row_ptr(const VParams& p, int64_t r) {
-  return reinterpret_cast<const char*>(p.z) + r * p.ld * (p.dtype == DSPARK_F32 ? 4 : 2);
-}
+// ------------------------------------------------------- verification
+// One 8-CTA cluster per request.  Each target row's slice arrives in shared
+// memory by bulk copies (interior 16-byte groups) and plain loads (the two
+// partial edge groups); the statistics are two cheap passes over it (max and
+// first argmax; sum of exp relative to the thread's own max), merged per
+// block and then across the cluster in rank order.  The exchange slots are
+// double-buffered, so each exchange costs one cluster barrier.  The final
+// draw computes exact 46-bit fixed-point weights of row L once, keeps the
+// mass of every block of 32 groups, and the CTA holding the draw finds its
+// block from those sums and its token with one warp.
+constexpr int kVTma = 4;
+constexpr int kVMaxBlocks = 160;  // blocks of 32 groups per slice (fp32: <= 129)
 
-// Fixed-point weight of token v for the final draw: residual max(p - q, 0)
-// (qrow != NULL: dense counts; qsm: sparse lookup) or p itself.
-struct DrawWeights {
-  float m, s;
-  const uint32_t* qrow;      // dense counts row or NULL
-  const int32_t* sids;       // sparse ids row or NULL
-  const uint32_t* scnt;      // sparse counts row
-  int snnz;
-  bool use_q;
+struct __align__(16) VX {
+  float m;        // max of the slice (NaN-propagating)
+  float s;        // sum of exp(z - m) over the slice (ratio mode)
+  float amv;      // argmax value (greedy mode)
+  int ami;        // argmax id, lowest among the maxima
+  uint64_t z;     // fixed-point draw mass of the slice
+  uint64_t cs;    // q mass of the slice (dense residual rows)
+  uint32_t fl;    // bit0: a bulk copy timed out
+  uint32_t pad[3];
 };
 
-__device__ __forceinline__ uint32_t q_count(const DrawWeights& w, int v) {
-  if (w.qrow) return __ldg(w.qrow + v);
-  if (w.sids) {
-    int a = 0, b = w.snnz - 1;
-    while (a <= b) {
-      const int mid = (a + b) >> 1;
-      const int id = __ldg(w.sids + mid);
-      if (id == v) return __ldg(w.scnt + mid);
-      if (id < v) a = mid + 1;
-      else b = mid - 1;
-    }
+struct VSh2 {
+  VX x[2];
+  uint64_t mbar[kVTma];
+  uint64_t bsum[kVMaxBlocks];
+  float wm[8], ws[8], wam[8];
+  int wai[8];
+  uint64_t wz[8], wc[8];
+  float M, S, AMV;
+  int AMI;
+  uint32_t FL;
+  uint64_t Z, before, CS;
+  int q_ok;
+  uint32_t q_c;
+  int timeout;
+  int found;
+  uint32_t near;
+};
+
+struct OpMaxNaNv {
+  __device__ float operator()(float a, float b) const {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
   }
-  return 0u;
+};
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-__device__ __forceinline__ uint64_t draw_weight(const DrawWeights& w, int v, float zv) {
-  const float pv = (zv == -INFINITY) ? 0.0f : __fdiv_rn(expf(zv - w.m), w.s);
-  float r = pv;
-  if (w.use_q) {
-    const float qv = (float)q_count(w, v) * 0x1p-24f;
-    r = fmaxf(pv - qv, 0.0f);
-  }
-  return (uint64_t)__float2ull_rz(__fmul_rn(r, kTwo46f));
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
-template <int kMode>
-__global__ void __cluster_dims__(kVCluster, 1, 1) __launch_bounds__(kVThreads, 2)
+// (m, s) pairs: s is a sum of exp(z - m); merged to the larger m.
+__device__ __forceinline__ void ms_merge(float& m, float& s, float m2, float s2) {
+  const float M = fmaxf(m, m2);
+  if (M == -INFINITY) {
+    m = M;
+    s = 0.0f;
+    return;
+  }
+  const float a = (m == -INFINITY) ? 0.0f : s * expf(m - M);
+  const float c = (m2 == -INFINITY) ? 0.0f : s2 * expf(m2 - M);
+  m = M;
+  s = a + c;
+}
+
+__device__ __forceinline__ void am_merge(float& v, int& i, float v2, int i2) {
+  if (v2 > v || (v2 == v && i2 < i)) {
+    v = v2;
+    i = i2;
+  }
+}
+
+template <int kMode, int kDt>
+__global__ void __cluster_dims__(kVCluster, 1, 1) __launch_bounds__(kVThreads, 3)
     verify_kernel(VParams p) {
+  constexpr int EPG = (kDt == DSPARK_F32) ? 4 : 8;  // elements per 16-byte group
+  constexpr int ESZ = (kDt == DSPARK_F32) ? 4 : 2;
   cg::cluster_group cluster = cg::this_cluster();
-  __shared__ VShared sh;
+  __shared__ VSh2 sh;
+  extern __shared__ __align__(128) unsigned char vbuf[];
+  const float* vf = reinterpret_cast<const float*>(vbuf);
+  const uint16_t* vh = reinterpret_cast<const uint16_t*>(vbuf);
   const int rank = (int)cluster.block_rank();
   const int b = blockIdx.x / kVCluster;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int depth = p.depth, V = p.V;
   const int lo = rank * p.chunk;
   const int n = max(0, min(V, lo + p.chunk) - lo);
@@ -259,52 +303,209 @@ __global__ void __cluster_dims__(kVCluster, 1, 1) __launch_bounds__(kVThreads, 2
     const int x = drafts[j];
     if (x < 0 || x >= V) status = DSPARK_ST_BAD_DRAFT;
   }
+  if (tid == 0) {
+    for (int c = 0; c < kVTma; ++c) mbar_init(&sh.mbar[c], 1);
+    mbar_init_fence();
+    sh.timeout = 0;
+  }
+  __syncthreads();
+  uint32_t phase = 0;
+  int xi = 0;
   int L = depth, pick = -1;
   uint32_t flags = 0;
-  int writer = -1;     // rank of the CTA that found the drawn token
-  bool drawn = false;  // the request reached its final draw (same in every CTA)
+  int writer = -1;
+  bool drawn = false;
+
+  auto val = [&](int s) -> float {
+    if (kDt == DSPARK_F32) return vf[s];
+    return __uint_as_float(((uint32_t)vh[s]) << 16);
+  };
+  // the EPG values of group g
+  auto group = [&](int g, float* z) {
+    if (kDt == DSPARK_F32) {
+      const float4 q = reinterpret_cast<const float4*>(vbuf)[g];
+      z[0] = q.x;
+      z[1] = q.y;
+      z[2] = q.z;
+      z[3] = q.w;
+    } else {
+      const uint4 q = reinterpret_cast<const uint4*>(vbuf)[g];
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        z[2 * i] = __uint_as_float(w[i] << 16);
+        z[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      }
+    }
+  };
 
   for (int j = 0; j <= depth && status == DSPARK_ST_OK; ++j) {
-    const void* row = row_ptr(p, (int64_t)b * (depth + 1) + j);
-    const RowStat mine = slice_stat(row, p.dtype, lo, n, sh);
-    if (tid == 0) sh.pub.st = mine;
+    const char* zrow = reinterpret_cast<const char*>(p.z) +
+                       ((int64_t)b * (depth + 1) + j) * p.ld * ESZ;
+    const int off = (int)((reinterpret_cast<uintptr_t>(zrow + (int64_t)lo * ESZ) / ESZ) % EPG);
+    const int ng = (off + n + EPG - 1) / EPG;
+    const int g_first = (off == 0) ? 0 : 1;
+    const int g_last = (off + n) / EPG - 1;
+    const int n_int = max(0, g_last - g_first + 1);
+    const char* gbase = zrow + (int64_t)(lo - off) * ESZ;  // 16-byte aligned
+    __syncthreads();  // every read of the previous row's slice is done
+    if (tid == 0 && n_int > 0) {
+      fence_proxy_async_smem();
+      for (int c = 0; c < kVTma; ++c) {
+        const int g0 = g_first + (n_int * c) / kVTma, g1 = g_first + (n_int * (c + 1)) / kVTma;
+        const uint32_t bytes = (uint32_t)(g1 - g0) * 16u;
+        mbar_arrive_expect_tx(&sh.mbar[c], bytes);
+        if (bytes) tma_load_bulk(vbuf + 16 * g0, gbase + 16 * g0, bytes, &sh.mbar[c]);
+      }
+    }
+    if (tid < 2 * EPG) {
+      const int g = (tid < EPG) ? 0 : ng - 1;
+      if (g >= 0 && !(n_int > 0 && g >= g_first && g <= g_last)) {
+        const int s = g * EPG + (tid % EPG);
+        const bool in = (s >= off && s < off + n);
+        if (kDt == DSPARK_F32)
+          reinterpret_cast<float*>(vbuf)[s] =
+              in ? __ldg(reinterpret_cast<const float*>(gbase) + s) : -INFINITY;
+        else
+          reinterpret_cast<uint16_t*>(vbuf)[s] =
+              in ? __ldg(reinterpret_cast<const unsigned short*>(gbase) + s) : (uint16_t)0xFF80u;
+      }
+    }
+    if (n_int > 0) {
+      if (tid == 0)
+        for (int c = 0; c < kVTma; ++c)
+          if (!mbar_wait_bounded(&sh.mbar[c], phase)) sh.timeout = 1;
+      phase ^= 1u;
+    }
+    __syncthreads();
+
+    // ---- row statistics of this slice
+    float mx = -INFINITY, sm = 0.0f, amv = -INFINITY;
+    int ami = 0x7FFFFFFF;
+    for (int g = tid; g < ng; g += kVThreads) {
+      float z[EPG];
+      group(g, z);
+#pragma unroll
+      for (int i = 0; i < EPG; ++i) {
+        mx = OpMaxNaNv()(mx, z[i]);
+        if (kMode == kGreedy && z[i] > amv) {
+          amv = z[i];
+          ami = lo - off + g * EPG + i;
+        }
+      }
+    }
+    if (kMode == kRatio && mx > -INFINITY && mx < INFINITY) {
+      for (int g = tid; g < ng; g += kVThreads) {
+        float z[EPG];
+        group(g, z);
+#pragma unroll
+        for (int i = 0; i < EPG; ++i) sm += (z[i] == -INFINITY) ? 0.0f : expf(z[i] - mx);
+      }
+    }
+    // block merge
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, mx, o);
+      if (kMode == kRatio) {
+        const float s2 = __shfl_xor_sync(0xffffffffu, sm, o);
+        if (mx == mx && m2 == m2 && mx < INFINITY && m2 < INFINITY) ms_merge(mx, sm, m2, s2);
+        else mx = OpMaxNaNv()(mx, m2);
+      } else {
+        mx = OpMaxNaNv()(mx, m2);
+        const float a2 = __shfl_xor_sync(0xffffffffu, amv, o);
+        const int i2 = __shfl_xor_sync(0xffffffffu, ami, o);
+        am_merge(amv, ami, a2, i2);
+      }
+    }
+    if (lane == 0) {
+      sh.wm[warp] = mx;
+      sh.ws[warp] = sm;
+      sh.wam[warp] = amv;
+      sh.wai[warp] = ami;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      float m = sh.wm[0], s = sh.ws[0], av = sh.wam[0];
+      int ai = sh.wai[0];
+      for (int w = 1; w < kVThreads / 32; ++w) {
+        if (kMode == kRatio) {
+          const float m2 = sh.wm[w], s2 = sh.ws[w];
+          if (m == m && m2 == m2 && m < INFINITY && m2 < INFINITY) ms_merge(m, s, m2, s2);
+          else m = OpMaxNaNv()(m, m2);
+        } else {
+          m = OpMaxNaNv()(m, sh.wm[w]);
+          am_merge(av, ai, sh.wam[w], sh.wai[w]);
+        }
+      }
+      VX& e = sh.x[xi];
+      e.m = m;
+      e.s = s;
+      e.amv = av;
+      e.ami = ai;
+      e.fl = sh.timeout ? 1u : 0u;
+    }
     cluster.sync();
-    RowStat st = cluster.map_shared_rank(&sh.pub, 0)->st;
-    for (int r = 1; r < kVCluster; ++r) st = stat_merge(st, cluster.map_shared_rank(&sh.pub, r)->st);
-    cluster.sync();  // pubs free again
-    if (st.bad) {
+    if (tid == 0) {
+      // peers' partials in rank order (identical in every CTA)
+      float m = -INFINITY, s = 0.0f, av = -INFINITY;
+      int ai = 0x7FFFFFFF;
+      uint32_t fl = 0;
+      bool bad = false;
+      for (int r = 0; r < kVCluster; ++r) {
+        const VX* e = cluster.map_shared_rank(&sh.x[xi], r);
+        const float m2 = e->m;
+        fl |= e->fl;
+        if (!(m2 < INFINITY)) bad = true;  // NaN or +inf in that slice
+        if (kMode == kRatio) ms_merge(m, s, bad ? -INFINITY : m2, bad ? 0.0f : e->s);
+        else {
+          m = fmaxf(m, m2);
+          am_merge(av, ai, e->amv, e->ami);
+        }
+      }
+      sh.M = bad ? NAN : m;
+      sh.S = s;
+      sh.AMV = av;
+      sh.AMI = ai;
+      sh.FL = fl;
+    }
+    xi ^= 1;
+    __syncthreads();
+    const float M = sh.M, S = sh.S;
+    if (sh.FL & 1u) {
+      status = DSPARK_ST_TIMEOUT;
+      break;
+    }
+    if (!(M < INFINITY)) {
       status = DSPARK_ST_NONFINITE;
       break;
     }
-    if (st.m == -INFINITY) {
+    if (M == -INFINITY) {
       status = DSPARK_ST_ZERO_MASS;
       break;
     }
     if (kMode == kGreedy) {
-      if (j == depth || st.ami != drafts[j]) {
+      if (j == depth || sh.AMI != drafts[j]) {
         L = j;
-        pick = st.ami;
+        pick = sh.AMI;
         break;
       }
       continue;
     }
-    // ---- ratio verification
-    DrawWeights w;
-    w.m = st.m;
-    w.s = st.s;
-    w.qrow = nullptr;
-    w.sids = nullptr;
-    w.scnt = nullptr;
-    w.snnz = 0;
-    w.use_q = false;
+
+    // ---- ratio test of draft j
+    bool use_q = false;
     uint32_t purpose = DSPARK_PURPOSE_BONUS;
+    const uint32_t* qrow = nullptr;  // dense counts row j
+    const int32_t* sids = nullptr;   // sparse row j
+    const uint32_t* scnt = nullptr;
+    int snnz = 0;
     if (j < depth) {
       const int x = drafts[j];
       const int64_t qr = (int64_t)b * depth + j;
       uint32_t c;
       if (p.top_k == 0) {
-        w.qrow = p.counts + qr * V;
-        c = __ldg(w.qrow + x);
+        qrow = p.counts + qr * V;
+        c = __ldg(qrow + x);
       } else {
         // canonical sparse row: 1 <= nnz <= top_k, ids strictly ascending in
         // [0, V), counts > 0, total M
@@ -316,36 +517,36 @@ __global__ void __cluster_dims__(kVCluster, 1, 1) __launch_bounds__(kVThreads, 2
           sh.q_c = 0u;
         }
         __syncthreads();
+        uint64_t tot = 0;
         if (nz < 1 || nz > p.top_k) {
           if (tid == 0) sh.q_ok = 0;
         } else {
-          uint64_t tot = 0;
-          for (int i = tid; i < nz; i += blockDim.x) {
+          for (int i = tid; i < nz; i += kVThreads) {
             const int id = ids[i];
             const uint32_t cc = cn[i];
             if (id < 0 || id >= V || cc == 0u || (i > 0 && ids[i - 1] >= id)) sh.q_ok = 0;
             if (id == x) sh.q_c = cc;
             tot += cc;
           }
-          tot = block_reduce(tot, OpAddU64(), sh.red64);
-          if (tid == 0 && tot != (uint64_t)kM) sh.q_ok = 0;
         }
+        tot = block_reduce(tot, OpAddU64(), sh.wz);
+        if (tid == 0 && nz >= 1 && nz <= p.top_k && tot != (uint64_t)kM) sh.q_ok = 0;
         __syncthreads();
         if (!sh.q_ok) {
           status = DSPARK_ST_BAD_Q;
           break;
         }
         c = sh.q_c;
-        w.sids = ids;
-        w.scnt = cn;
-        w.snnz = nz;
+        sids = ids;
+        scnt = cn;
+        snnz = nz;
       }
       if (c == 0u) {
         status = DSPARK_ST_BAD_DRAFT;
         break;
       }
-      const float zx = load_logit(row, p.dtype, x);
-      const float px = (zx == -INFINITY) ? 0.0f : __fdiv_rn(expf(zx - st.m), st.s);
+      const float zx = load_logit(zrow, kDt, x);
+      const float px = (zx == -INFINITY) ? 0.0f : __fdiv_rn(expf(zx - M), S);
       const uint32_t U = draw_u32(p.seed, req, (uint32_t)j, DSPARK_PURPOSE_ACCEPT) >> 8;
       const double uc = (double)((uint64_t)U * (uint64_t)c);
       const double p48 = (double)px * 281474976710656.0;
@@ -353,100 +554,212 @@ __global__ void __cluster_dims__(kVCluster, 1, 1) __launch_bounds__(kVThreads, 2
         flags |= DSPARK_FLAG_AMBIG_ACCEPT;
       if (uc < p48) continue;  // accepted
       L = j;
-      w.use_q = true;
+      use_q = true;
       purpose = DSPARK_PURPOSE_RESIDUAL;
-      if (p.top_k == 0) {
-        // the dense residual row must carry mass M
-        uint64_t cs = 0;
-        for (int v = lo + tid; v < lo + n; v += blockDim.x) cs += __ldg(w.qrow + v);
-        cs = block_reduce(cs, OpAddU64(), sh.red64);
-        if (tid == 0) sh.pub.csum = cs;
-        cluster.sync();
-        uint64_t all = 0;
-        for (int r = 0; r < kVCluster; ++r) all += cluster.map_shared_rank(&sh.pub, r)->csum;
-        cluster.sync();
-        if (all != (uint64_t)kM) {
-          status = DSPARK_ST_BAD_Q;
-          break;
-        }
+      if (qrow && tid == 0) {
+        // the counts of this slice are read next: start them towards L2
+        const uintptr_t a0 = (reinterpret_cast<uintptr_t>(qrow + lo) + 15) & ~(uintptr_t)15;
+        const uintptr_t a1 = reinterpret_cast<uintptr_t>(qrow + lo + n) & ~(uintptr_t)15;
+        if (a1 > a0) prefetch_l2(reinterpret_cast<const void*>(a0), (uint32_t)(a1 - a0));
       }
     } else {
       L = depth;
     }
-    // ---- final draw over row j: residual (ratio rejection) or p (bonus)
+
+    // ---- final draw over row j: residual max(p - q, 0) or p itself
     const uint32_t wdraw = draw_u32(p.seed, req, (uint32_t)j, purpose);
+    const float invS = __frcp_rn(S);
+    auto pv = [&](float z) -> float {
+      return (z == -INFINITY) ? 0.0f : __fmul_rn(expf(z - M), invS);
+    };
+    auto wfix = [&](float r) -> uint64_t { return __float2ull_rz(__fmul_rn(r, kTwo46f)); };
+    // q of the sparse row at id v (binary search; -1 ids never match)
+    auto sparse_q = [&](int v) -> uint32_t {
+      int a = 0, e = snnz - 1;
+      while (a <= e) {
+        const int mid = (a + e) >> 1;
+        const int id = __ldg(sids + mid);
+        if (id == v) return __ldg(scnt + mid);
+        if (id < v) a = mid + 1;
+        else e = mid - 1;
+      }
+      return 0u;
+    };
+    const int nblk = (ng + 31) / 32;
     for (int attempt = 0; attempt < 2; ++attempt) {
-      uint64_t zs = 0;
-      row_foreach(row, p.dtype, lo, n, [&](int v, float zv) { zs += draw_weight(w, v, zv); });
-      zs = block_reduce(zs, OpAddU64(), sh.red64);
-      if (tid == 0) sh.pub.z = zs;
-      cluster.sync();
-      uint64_t before = 0, Z = 0;
-      for (int r = 0; r < kVCluster; ++r) {
-        const uint64_t zr = cluster.map_shared_rank(&sh.pub, r)->z;
-        if (r < rank) before += zr;
-        Z += zr;
+      const bool dense_q = use_q && qrow != nullptr;
+      const bool sparse_qm = use_q && sids != nullptr;
+      uint64_t zs = 0, cs = 0;
+      for (int gb = 0; gb < ng; gb += kVThreads) {
+        const int g = gb + tid;
+        uint64_t gsum = 0;
+        if (g < ng) {
+          float z[EPG];
+          group(g, z);
+#pragma unroll
+          for (int i = 0; i < EPG; ++i) {
+            const int s = g * EPG + i;
+            const bool in = (s >= off && s < off + n);
+            float r = pv(z[i]);
+            if (dense_q && in) {
+              const uint32_t q = __ldg(qrow + (lo - off + s));
+              cs += q;
+              r = fmaxf(__fsub_rn(r, (float)q * 0x1p-24f), 0.0f);
+            }
+            gsum += wfix(r);
+          }
+        }
+        // one block = the 32 groups of one warp in one iteration
+        const uint64_t bs = warp_reduce(gsum, OpAddU64());
+        if (lane == 0 && gb / 32 + warp < nblk) sh.bsum[gb / 32 + warp] = bs;
+        zs += gsum;
+      }
+      __syncthreads();
+      if (sparse_qm) {
+        // support ids in this slice: their weight is max(p - q, 0), not p
+        for (int i = tid; i < snnz; i += kVThreads) {
+          const int v = __ldg(sids + i);
+          if (v < lo || v >= lo + n) continue;
+          const int s = v - lo + off;
+          const float pr = pv(val(s));
+          const float r = fmaxf(__fsub_rn(pr, (float)__ldg(scnt + i) * 0x1p-24f), 0.0f);
+          const uint64_t d = wfix(pr) - wfix(r);
+          atomicAdd(reinterpret_cast<unsigned long long*>(&sh.bsum[(s / EPG) / 32]),
+                    (unsigned long long)(0ull - d));
+          zs -= d;
+        }
+      }
+      zs = warp_reduce(zs, OpAddU64());
+      cs = warp_reduce(cs, OpAddU64());
+      if (lane == 0) {
+        sh.wz[warp] = zs;
+        sh.wc[warp] = cs;
+      }
+      __syncthreads();
+      if (tid == 0) {
+        uint64_t a = 0, c2 = 0;
+        for (int w = 0; w < kVThreads / 32; ++w) {
+          a += sh.wz[w];
+          c2 += sh.wc[w];
+        }
+        sh.x[xi].z = a;
+        sh.x[xi].cs = c2;
       }
       cluster.sync();
-      if (Z == 0ull && w.use_q) {  // no residual mass: draw from p instead
+      if (tid == 0) {
+        uint64_t before = 0, Z = 0, CS = 0;
+        for (int r = 0; r < kVCluster; ++r) {
+          const VX* e = cluster.map_shared_rank(&sh.x[xi], r);
+          const uint64_t zr = e->z;
+          if (r < rank) before += zr;
+          Z += zr;
+          CS += e->cs;
+        }
+        sh.Z = Z;
+        sh.before = before;
+        sh.CS = CS;
+      }
+      xi ^= 1;
+      __syncthreads();
+      const uint64_t Z = sh.Z, before = sh.before;
+      const uint64_t mine = sh.x[xi ^ 1].z;
+      if (dense_q && sh.CS != (uint64_t)kM) {
+        status = DSPARK_ST_BAD_Q;
+        break;
+      }
+      if (Z == 0ull && use_q) {  // no residual mass: draw from p instead
         flags |= DSPARK_FLAG_DEGENERATE;
-        w.use_q = false;
+        use_q = false;
         continue;
       }
       const uint64_t T = __umul64hi((uint64_t)wdraw << 32, Z);  // floor(w * Z / 2^32) < Z
-      // exactly one CTA's slice holds T; it walks its slice in id order and
-      // writes the request's outputs
       drawn = true;
       writer = -1;
-      const bool mine_has = (T >= before) && (T < before + zs);
-      if (mine_has) {
-        // ordered scan over groups of this slice
-        __shared__ int found;
-        __shared__ uint32_t found_near;
-        if (tid == 0) {
-          found = -1;
-          found_near = 0u;
+      if (T >= before && T - before < mine) {
+        // the block holding T, then the token inside it (warp 0)
+        if (warp == 0) {
+          const uint64_t t = T - before;
+          uint64_t base = 0;
+          int blk = -1;
+          for (int k0 = 0; k0 < nblk && blk < 0; k0 += 32) {
+            const int k = k0 + lane;
+            const uint64_t v = (k < nblk) ? sh.bsum[k] : 0ull;
+            uint64_t incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const uint64_t u = __shfl_up_sync(0xffffffffu, incl, o);
+              if (lane >= o) incl += u;
+            }
+            const bool hit = (k < nblk) && v > 0ull && t - base < incl && t - base >= incl - v;
+            const unsigned msk = __ballot_sync(0xffffffffu, hit);
+            if (msk) {
+              const int l = __ffs(msk) - 1;
+              blk = k0 + l;
+              base += __shfl_sync(0xffffffffu, incl - v, l);
+            } else {
+              base += __shfl_sync(0xffffffffu, incl, 31);
+            }
+          }
+          int found = -1;
+          uint32_t near = 0u;
+          if (blk >= 0) {
+            const int g = blk * 32 + lane;
+            uint64_t wv[EPG];
+            uint64_t gsum = 0;
+            if (g < ng) {
+              float z[EPG];
+              group(g, z);
+#pragma unroll
+              for (int i = 0; i < EPG; ++i) {
+                const int s = g * EPG + i;
+                const bool in = (s >= off && s < off + n);
+                float r = pv(z[i]);
+                if (use_q && in) {
+                  const uint32_t q = qrow ? __ldg(qrow + (lo - off + s)) : sparse_q(lo - off + s);
+                  r = fmaxf(__fsub_rn(r, (float)q * 0x1p-24f), 0.0f);
+                }
+                wv[i] = wfix(r);
+                gsum += wv[i];
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < EPG; ++i) wv[i] = 0ull;
+            }
+            uint64_t incl = gsum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const uint64_t u = __shfl_up_sync(0xffffffffu, incl, o);
+              if (lane >= o) incl += u;
+            }
+            const uint64_t tb = t - base;  // position inside the block
+            const bool hit = gsum > 0ull && tb < incl && tb >= incl - gsum;
+            const unsigned msk = __ballot_sync(0xffffffffu, hit);
+            if (msk && lane == __ffs(msk) - 1) {
+              uint64_t cum = incl - gsum;
+              for (int i = 0; i < EPG; ++i) {
+                const uint64_t prev = cum;
+                cum += wv[i];
+                if (tb < cum) {
+                  found = lo - off + g * EPG + i;
+                  near = (tb - prev <= kNearTol || cum - tb <= kNearTol) ? 1u : 0u;
+                  break;
+                }
+              }
+              sh.found = found;
+              sh.near = near;
+            }
+            if (!msk && lane == 0) {
+              sh.found = -1;
+              sh.near = 0u;
+            }
+          } else if (lane == 0) {
+            sh.found = -1;
+            sh.near = 0u;
+          }
         }
         __syncthreads();
-        const int gsz = (p.dtype == DSPARK_F32) ? 4 : 8;
-        const int offs = (p.dtype == DSPARK_F32)
-                             ? (int)((reinterpret_cast<uintptr_t>(reinterpret_cast<const float*>(row) + lo) >> 2) & 3)
-                             : (int)((reinterpret_cast<uintptr_t>(reinterpret_cast<const unsigned short*>(row) + lo) >> 1) & 7);
-        const int ng = (offs + n + gsz - 1) / gsz;
-        uint64_t base = before;
-        for (int t0 = 0; t0 < ng; t0 += blockDim.x) {
-          const int g = t0 + tid;
-          uint64_t wv[8];
-          uint64_t mysum = 0;
-          for (int i = 0; i < gsz; ++i) {
-            const int s = g * gsz + i;
-            wv[i] = 0;
-            if (g < ng && s >= offs && s < offs + n) {
-              const int v = lo - offs + s;
-              wv[i] = draw_weight(w, v, load_logit(row, p.dtype, v));
-            }
-            mysum += wv[i];
-          }
-          uint64_t tot;
-          const uint64_t incl = block_inclusive_scan_u64(mysum, sh.red64, &tot);
-          uint64_t cum = base + incl - mysum;
-          if (T >= cum && T < cum + mysum) {
-            for (int i = 0; i < gsz; ++i) {
-              const uint64_t prev = cum;
-              cum += wv[i];
-              if (T < cum) {
-                found = lo - offs + g * gsz + i;
-                found_near = (T - prev <= kNearTol || cum - T <= kNearTol) ? 1u : 0u;
-                break;
-              }
-            }
-          }
-          base += tot;
-          __syncthreads();
-          if (found >= 0) break;
-        }
-        pick = found;
-        if (found_near) flags |= DSPARK_FLAG_NEAR_BOUNDARY;
+        pick = sh.found;
+        if (sh.near) flags |= DSPARK_FLAG_NEAR_BOUNDARY;
         if (pick < 0) status = DSPARK_ST_INTERNAL;
         writer = rank;
       }
@@ -473,7 +786,7 @@ __global__ void __cluster_dims__(kVCluster, 1, 1) __launch_bounds__(kVThreads, 2
     }
     p.status[b] = status;
   }
-  cluster.sync();
+  cluster.sync();  // no CTA leaves while a peer may still read its shared memory
 }
 
 // ------------------------------------------------------------ target p
@@ -552,11 +865,23 @@ cudaError_t launch_verify(int mode, const void* z, int dtype, int64_t ld, int B,
   p.flags = flags;
   p.status = status;
   p.chunk = verify_chunk(V);
+  // the slice buffer: chunk elements plus one 16-byte group of slack
+  const int esz = (dtype == DSPARK_F32) ? 4 : 2;
+  const int smem = p.chunk * esz + 32;
+  auto go = [&](auto kern) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    kern<<<B * kVCluster, kVThreads, smem, stream>>>(p);
+    return cudaGetLastError();
+  };
   if (mode == kGreedy)
-    verify_kernel<kGreedy><<<B * kVCluster, kVThreads, 0, stream>>>(p);
-  else
-    verify_kernel<kRatio><<<B * kVCluster, kVThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+    return dtype == DSPARK_F32 ? go(verify_kernel<kGreedy, DSPARK_F32>)
+                               : go(verify_kernel<kGreedy, DSPARK_BF16>);
+  return dtype == DSPARK_F32 ? go(verify_kernel<kRatio, DSPARK_F32>)
+                             : go(verify_kernel<kRatio, DSPARK_BF16>);
 }
 
 cudaError_t launch_target_probs(const void* z, int dtype, int64_t ld, int n_rows, int V,
