@@ -274,6 +274,14 @@ struct OpMaxU64 {
   __device__ uint64_t operator()(uint64_t a, uint64_t b) const { return a > b ? a : b; }
 };
 
+// 32-bit sums and ors over a full warp by the hardware warp reduction
+__device__ __forceinline__ uint32_t warp_reduce(uint32_t v, OpAddU32) {
+  return __reduce_add_sync(0xffffffffu, v);
+}
+__device__ __forceinline__ uint32_t warp_reduce(uint32_t v, OpOrU32) {
+  return __reduce_or_sync(0xffffffffu, v);
+}
+
 // Inclusive scan over the block for one uint32 per thread; returns the
 // inclusive prefix, *total gets the block total.  scratch >= 32 words.
 __device__ __forceinline__ uint32_t block_inclusive_scan(uint32_t v, uint32_t* scratch,

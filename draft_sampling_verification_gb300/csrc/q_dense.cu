@@ -47,7 +47,9 @@ constexpr int kWarps = kThr / 32;
 constexpr int kBins = 2048;              // fraction buckets, floor(2048 r)
 constexpr int kFine = kBins / 64;        // fine bins per coarse bin
 constexpr int kCandCap = 64;             // threshold-bin members listed per CTA
-constexpr int kUncCap = 128;             // elements left to the exact split per CTA
+constexpr int kBlkCap = 130;             // count sums of 32-group blocks (<= 129 per slice)
+constexpr int kWin = 3072;               // slice positions compacted per window (many members)
+constexpr int kTab = 64;                 // distinct member fractions kept per CTA
 constexpr int kEscCap = 40;              // floors >= kFMax, at most 32 per row
 constexpr int kTma = 4;                  // bulk copies (and mbarriers) per slice
 constexpr uint32_t kFMax = (1u << 19) - 1u;
@@ -56,6 +58,8 @@ constexpr uint32_t kPos = 1u << 11;      // r > 0
 constexpr uint32_t kGrant = 1u << 12;    // member granted its ticket
 constexpr uint32_t kLowMask = 0x1FFFu;   // grant | pos | bucket
 constexpr uint32_t kNoThr = 0x1FFFu;     // threshold when no ticket is granted
+// certification half-width: 2048 fr must lie within this of a half-integer
+constexpr float kHalfMargin = 0.5f - 0x1p-12f - 0x1p-15f;
 
 struct __align__(16) Cand {
   uint64_t key;  // exact fraction (FP64 bit pattern)
@@ -83,17 +87,33 @@ struct __align__(16) Pub {
   uint32_t n_grant; // granted members (many-member path)
   uint32_t flags2;  // after pass B: bit0 a finite logit overflowed to -inf
   uint32_t flags3;  // after pass C: bit1 internal (escape list full)
-  uint32_t pad;
+  uint32_t flags4;  // many-member path: bit0 a table of fractions overflowed
   uint32_t coarse[64];
+};
+
+// Many-member path: member positions compacted per window, then the table of
+// distinct exact fractions (read by peers), then every peer's table merged.
+struct ManyShared {
+  union {
+    uint16_t list[kWin];
+    struct {
+      uint64_t key[kCl * kTab];
+      uint32_t cnt[kCl * kTab];
+    } merged;
+  };
+  uint64_t tkey[kTab];
+  uint32_t tcnt[kTab];
+  uint8_t state[kTab];  // 0 below the threshold fraction, 1 above, 2 at it
 };
 
 struct DShared {
   union {
-    uint32_t hist[kBins];
+    uint32_t hist[kBins + 16];  // + dummy bins taking the elements that do not count
     Cand all[kBins * 4 / (int)sizeof(Cand)];  // every member of the row (512)
+    ManyShared many;
   };
   Cand cand[kCandCap];
-  int32_t unc[kUncCap];
+  uint32_t bsum[kBlkCap];  // count sum of each block of 32 groups
   Esc esc[kEscCap];
   Pub pub;
   uint64_t mbar[kTma];
@@ -112,8 +132,11 @@ struct DShared {
   float khi, klo;
   float m, invT;
   int bad_T, timeout, status;
-  uint32_t n_cand, n_unc, n_esc;
+  uint32_t n_cand, n_esc;
   uint32_t R, Rin, thr, total, fits;
+  uint64_t thrk;
+  uint32_t need, fovf;
+  uint32_t wcnt[kWarps];
   int sel_bin;
   uint32_t sel_above, sel_count, scan_base;
 };
@@ -155,7 +178,7 @@ __device__ __forceinline__ T warp0_combine(const T* part, T ident, Op op) {
 
 // Exact split of a = RN64(E * k) for one element: word (or escape entry),
 // floor, histogram.  Used for the elements the float test leaves open.
-__device__ __forceinline__ uint32_t exact_word(float Ef, uint64_t mk, int ek, DShared& sh, int s,
+__device__ __noinline__ uint32_t exact_word(float Ef, uint64_t mk, int ek, DShared& sh, int s,
                                                uint32_t* F, uint32_t* internal) {
   uint32_t Ei;
   int se;
@@ -177,6 +200,32 @@ __device__ __forceinline__ uint32_t exact_word(float Ef, uint64_t mk, int ek, DS
     *internal = 1u;
   }
   return kEsc;
+}
+
+// The float split of one weight (see the file comment): the word, its floor,
+// its bucket, and whether the float result is certified.
+struct FloatSplit {
+  uint32_t word, f, b;
+  bool cert, zero;
+};
+__device__ __forceinline__ FloatSplit float_split(float Ef, float khi, float klo) {
+  FloatSplit o;
+  const float p1 = __fmul_rn(Ef, khi);
+  const float e1 = __fmaf_rn(Ef, khi, -p1);
+  const float p2 = __fmul_rn(Ef, klo);
+  const float f0 = floorf(p1);
+  const float fr = __fadd_rn(__fsub_rn(p1, f0), __fadd_rn(e1, p2));
+  const float fb = __fmul_rn(fr, 2048.0f);
+  const float G = floorf(fb);
+  o.cert = fabsf(__fsub_rn(__fsub_rn(fb, G), 0.5f)) < kHalfMargin && f0 < (float)(kFMax - 2u);
+  // f0 and G as integers (|G| < 2^13 here): f = f0 + floor(G / 2048)
+  const int f0i = __float_as_int(__fadd_rn(f0, 12582912.0f)) - 0x4B400000;
+  const int Gi = __float_as_int(__fadd_rn(G, 12582912.0f)) - 0x4B400000;
+  o.f = (uint32_t)(f0i + (Gi >> 11));
+  o.b = (uint32_t)Gi & (kBins - 1u);
+  o.zero = (Ef == 0.0f);
+  o.word = o.zero ? 0u : ((o.f << 13) | kPos | o.b);
+  return o;
 }
 
 __device__ __forceinline__ int esc_find(const DShared& sh, int s) {
@@ -338,7 +387,6 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThr, 3)
     sh.invT = iT;
     sh.bad_T = (!(isfinite(T) && T > 0.0f) || !(isfinite(iT) && iT >= 0x1p-126f)) ? 1 : 0;
     sh.n_cand = 0;
-    sh.n_unc = 0;
     sh.n_esc = 0;
     sh.timeout = 0;
     if (use_tma_dtype && n_int > 0) {
@@ -475,7 +523,7 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThr, 3)
       reinterpret_cast<float4*>(sl)[g] = make_float4(e0, e1, e2, e3);
     }
   }
-  for (int i = tid; i < kBins; i += kThr) sh.hist[i] = 0u;
+  for (int i = tid; i < kBins + 16; i += kThr) sh.hist[i] = 0u;
   S = warp_reduce(S, OpAddU64());
   ovf = warp_reduce(ovf, OpOrU32());
   if (lane == 0) {
@@ -529,62 +577,38 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThr, 3)
 
   // ---- pass C: words and fraction histogram
   uint32_t F = 0, internal = 0;
-  // the trip count is the same for every thread (warp votes inside)
-  for (int gb = 0; gb < ngroups; gb += kThr) {
-    const int g = gb + tid;
-    const bool valid = g < ngroups;
-    const float4 e4 = valid ? reinterpret_cast<const float4*>(sl)[g] : make_float4(0.f, 0.f, 0.f, 0.f);
-    const float ee[4] = {e4.x, e4.y, e4.z, e4.w};
-    uint32_t w[4];
-    bool open[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float Ef = ee[i];
-      const float p1 = __fmul_rn(Ef, khi);
-      const float e1 = __fmaf_rn(Ef, khi, -p1);
-      const float p2 = __fmul_rn(Ef, klo);
-      const float f0 = floorf(p1);
-      const float fr = __fadd_rn(__fsub_rn(p1, f0), __fadd_rn(e1, p2));
-      const float fb = __fmul_rn(fr, 2048.0f);
-      const float G = floorf(fb);
-      const float h = __fmaf_rn(p1, -0x1p-34f, 0.5f - 0x1p-12f);
-      const bool cert = fabsf(__fsub_rn(__fsub_rn(fb, G), 0.5f)) < h &&
-                        f0 < (float)(kFMax - 2u);
-      // f0 and G as integers (both below 2^22 in magnitude here)
-      const int f0i = __float_as_int(__fadd_rn(f0, 12582912.0f)) - 0x4B400000;
-      const int Gi = __float_as_int(__fadd_rn(G, 12582912.0f)) - 0x4B400000;
-      const uint32_t f = (uint32_t)(f0i + (Gi >> 11));
-      const uint32_t b = (uint32_t)Gi & (kBins - 1u);
-      const bool zero = (Ef == 0.0f);
-      open[i] = !(cert || zero);
-      w[i] = zero ? 0u : ((f << 13) | kPos | b);
-      if (cert && !zero) {
-        F += f;
-        atomicAdd(&sh.hist[b], 1u);
-      }
-    }
-    const bool any_open = open[0] || open[1] || open[2] || open[3];
-    if (__any_sync(0xffffffffu, any_open)) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if (open[i]) {
-          const uint32_t j = atomicAdd(&sh.n_unc, 1u);
-          if (j < (uint32_t)kUncCap) {
-            sh.unc[j] = 4 * g + i;
-            w[i] = __float_as_uint(ee[i]);  // E kept for the exact split
-          } else {
-            w[i] = exact_word(ee[i], mk, ek, sh, 4 * g + i, &F, &internal);
-          }
-        }
-    }
-    if (valid) reinterpret_cast<uint4*>(slu)[g] = make_uint4(w[0], w[1], w[2], w[3]);
-  }
-  __syncthreads();
+  uint32_t gmask = 0;  // bit it: group tid + 256 it holds an element the float split left open
   {
-    const uint32_t nu = min(sh.n_unc, (uint32_t)kUncCap);
-    for (uint32_t j = tid; j < nu; j += kThr) {
-      const int s = sh.unc[j];
-      slu[s] = exact_word(__uint_as_float(slu[s]), mk, ek, sh, s, &F, &internal);
+    int it = 0;
+    for (int g = tid; g < ngroups; g += kThr, ++it) {
+      const float4 e4 = reinterpret_cast<const float4*>(sl)[g];
+      const float ee[4] = {e4.x, e4.y, e4.z, e4.w};
+      uint32_t w[4];
+      bool any_open = false;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const FloatSplit fs = float_split(ee[i], khi, klo);
+        const bool counted = fs.cert && !fs.zero;
+        any_open = any_open || !(fs.cert || fs.zero);
+        w[i] = fs.word;
+        // branch-free: the elements that do not count go to a dummy bin
+        F += counted ? fs.f : 0u;
+        atomicAdd(&sh.hist[counted ? fs.b : kBins + (tid & 15)], 1u);
+      }
+      gmask |= any_open ? (1u << it) : 0u;
+      reinterpret_cast<uint4*>(slu)[g] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+  // the open elements (about 1 in 2000): E again from the logit, the exact split
+  for (uint32_t m2 = gmask; m2 != 0u; m2 &= m2 - 1u) {
+    const int g = tid + kThr * (__ffs(m2) - 1);
+    for (int i = 0; i < 4; ++i) {
+      const int s = 4 * g + i;
+      if (s < off || s >= off + n) continue;
+      const float x = load_logit(xrow, p.dtype, (int64_t)(lo - off + s));
+      const float Ef = weight40(__fsub_rn(scale ? __fmul_rn(x, invT) : x, m));
+      const FloatSplit fs = float_split(Ef, khi, klo);
+      if (!(fs.cert || fs.zero)) slu[s] = exact_word(Ef, mk, ek, sh, s, &F, &internal);
     }
   }
   F = warp_reduce(F, OpAddU32());
@@ -669,62 +693,99 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThr, 3)
   int status = sh.status;
   const uint32_t R = sh.R, Rin = sh.Rin, thr = sh.thr;
 
-  // ---- pass E: counts = f + [bin above the threshold bin]; members listed
-  uint32_t csum = 0;
-  const int offc = (int)((reinterpret_cast<uintptr_t>(crow + lo) / 4) & 3);
+  // ---- pass E: counts = f + [bin above the threshold bin], 128-bit stores;
+  // groups holding a member of the threshold bin are flagged and listed after
+  // the loop; escapes are corrected from their list
+  const uint32_t carry_k = kLowMask - thr;
+  const uint32_t esc_c = (kEsc + carry_k) >> 13;  // what the loop writes for an escape
   if (status == DSPARK_ST_OK) {
-    // the trip count is the same for every thread (warp votes inside)
-    for (int gb = 0; gb < ngroups; gb += kThr) {
+    const bool vec = ((reinterpret_cast<uintptr_t>(crow + lo) / 4) & 3) == (uintptr_t)off;
+    uint32_t* cbase = crow + lo - off;  // slice position s is cbase[s]
+    uint32_t mmask = 0;                 // bit it: group tid + 256 it holds a member
+    int it = 0;
+    // the trip count is the same for every thread (one warp reduction per step)
+    for (int gb = 0; gb < ngroups; gb += kThr, ++it) {
       const int g = gb + tid;
       const bool valid = g < ngroups;
       const uint4 w4 = valid ? reinterpret_cast<const uint4*>(slu)[g] : make_uint4(0u, 0u, 0u, 0u);
-      const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
-      uint32_t c[4];
-      bool odd = false;
-#pragma unroll
+      // f + [low > thr]: low + (kLowMask - thr) carries into bit 13 exactly
+      // when low > thr
+      const uint32_t c0 = (w4.x + carry_k) >> 13, c1 = (w4.y + carry_k) >> 13;
+      const uint32_t c2 = (w4.z + carry_k) >> 13, c3 = (w4.w + carry_k) >> 13;
+      const uint32_t xm = min(min((w4.x ^ thr) & kLowMask, (w4.y ^ thr) & kLowMask),
+                              min((w4.z ^ thr) & kLowMask, (w4.w ^ thr) & kLowMask));
+      mmask |= (valid && xm == 0u) ? (1u << it) : 0u;
+      const bool full = valid && g >= g_first && g <= g_last;  // all four inside the slice
+      uint32_t gsum = 0;
+      if (full) {
+        gsum = c0 + c1 + c2 + c3;
+        if (vec) {
+          reinterpret_cast<uint4*>(cbase)[g] = make_uint4(c0, c1, c2, c3);
+        } else {
+          cbase[4 * g] = c0;
+          cbase[4 * g + 1] = c1;
+          cbase[4 * g + 2] = c2;
+          cbase[4 * g + 3] = c3;
+        }
+      }
+      // one block = the 32 groups of one warp in one step
+      const uint32_t bs = __reduce_add_sync(0xffffffffu, gsum);
+      if (lane == 0 && gb / 32 + warp < kBlkCap) sh.bsum[gb / 32 + warp] = bs;
+    }
+    __syncthreads();
+    // partial edge groups (first and last): element by element
+    if (tid < 8) {
+      const int g = (tid < 4) ? 0 : ngroups - 1;
+      const bool dup = (tid >= 4 && g == 0);
+      const bool edge = g >= 0 && !(g >= g_first && g <= g_last);
+      const int s = 4 * g + (tid & 3);
+      if (!dup && edge && s >= off && s < off + n) {
+        // an escape is stored by the correction below, which expects esc_c here
+        const uint32_t w = slu[s];
+        const uint32_t c = (w + carry_k) >> 13;
+        if (w != kEsc) cbase[s] = c;
+        atomicAdd(&sh.bsum[g / 32], c);
+      }
+    }
+    // escapes: the right count, and the block sum corrected
+    for (uint32_t j = tid; j < min(sh.n_esc, (uint32_t)kEscCap); j += kThr) {
+      const int s = sh.esc[j].s;
+      if (s < off || s >= off + n) continue;
+      const uint32_t low = sh.esc[j].low;
+      const uint32_t c = sh.esc[j].f + ((low > thr) ? 1u : 0u);
+      cbase[s] = c;
+      atomicAdd(&sh.bsum[(s >> 2) >> 5], c - esc_c);
+      if (low == thr) {
+        const uint32_t q = atomicAdd(&sh.n_cand, 1u);
+        if (q < (uint32_t)kCandCap) {
+          sh.cand[q].v = lo - off + s;
+          sh.cand[q].s = s;
+        }
+      }
+    }
+    // members of the threshold bin, from the flagged groups
+    for (uint32_t m2 = mmask; m2 != 0u; m2 &= m2 - 1u) {
+      const int g = tid + kThr * (__ffs(m2) - 1);
       for (int i = 0; i < 4; ++i) {
-        const uint32_t low = ww[i] & kLowMask;
-        c[i] = (ww[i] >> 13) + ((low > thr) ? 1u : 0u);
-        odd = odd || low == thr || ww[i] == kEsc;
-      }
-      if (__any_sync(0xffffffffu, odd)) {
-        if (odd)
-          for (int i = 0; i < 4; ++i) {
-            const int s = 4 * g + i;
-            uint32_t low = ww[i] & kLowMask;
-            if (ww[i] == kEsc) {
-              const int j = esc_find(sh, s);
-              low = j < 0 ? 0u : sh.esc[j].low;
-              c[i] = j < 0 ? 0u : sh.esc[j].f + ((low > thr) ? 1u : 0u);
-            }
-            if (low == thr && s >= off && s < off + n) {
-              const uint32_t q = atomicAdd(&sh.n_cand, 1u);
-              if (q < (uint32_t)kCandCap) {
-                sh.cand[q].v = lo - off + s;
-                sh.cand[q].s = s;
-              }
-            }
-          }
-      }
-      const int s0 = 4 * g;
-      if (!valid) continue;
-      if (s0 >= off && s0 + 3 < off + n) {
-        csum += c[0] + c[1] + c[2] + c[3];
-        if (offc == off)
-          *reinterpret_cast<uint4*>(crow + lo - off + s0) = make_uint4(c[0], c[1], c[2], c[3]);
-        else
-          for (int i = 0; i < 4; ++i) crow[lo - off + s0 + i] = c[i];
-      } else {
-        for (int i = 0; i < 4; ++i) {
-          const int s = s0 + i;
-          if (s < off || s >= off + n) continue;
-          csum += c[i];
-          crow[lo - off + s] = c[i];
+        const int s = 4 * g + i;
+        if (s < off || s >= off + n || (slu[s] & kLowMask) != thr || slu[s] == kEsc) continue;
+        const uint32_t q = atomicAdd(&sh.n_cand, 1u);
+        if (q < (uint32_t)kCandCap) {
+          sh.cand[q].v = lo - off + s;
+          sh.cand[q].s = s;
         }
       }
     }
   }
   __syncthreads();
+  // the CTA's count sum (before member grants), from the block sums
+  if (warp == 0 && status == DSPARK_ST_OK) {
+    const int nblk = (ngroups + 31) / 32;
+    uint32_t t = 0;
+    for (int k = lane; k < nblk; k += 32) t += sh.bsum[k];
+    t = __reduce_add_sync(0xffffffffu, t);
+    if (lane == 0) sh.wred32[0] = t;
+  }
   // exact fractions of the listed members
   auto exact_key = [&](int s) -> uint64_t {
     const float x = load_logit(xrow, p.dtype, (int64_t)(lo - off + s));
@@ -737,15 +798,10 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThr, 3)
   const uint32_t my_cand = sh.n_cand;
   for (uint32_t j = tid; j < min(my_cand, (uint32_t)kCandCap); j += kThr)
     sh.cand[j].key = exact_key(sh.cand[j].s);
-  csum = warp_reduce(csum, OpAddU32());
-  if (lane == 0) sh.wred32[warp] = csum;
   __syncthreads();
-  if (warp == 0) {
-    const uint32_t c2 = warp0_combine(sh.wred32, 0u, OpAddU32());
-    if (lane == 0) {
-      sh.pub.csum = c2;
-      sh.pub.ncand = my_cand;
-    }
+  if (tid == 0) {
+    sh.pub.csum = (status == DSPARK_ST_OK) ? sh.wred32[0] : 0u;
+    sh.pub.ncand = my_cand;
   }
   cluster.sync();  // S4
   if (warp == 0) {
@@ -784,6 +840,7 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThr, 3)
       f = w >> 13;
     }
     crow[lo - off + s] = f + 1u;
+    atomicAdd(&sh.bsum[(s >> 2) >> 5], 1u);
   };
 
   if (R > 0 && fits && Rin > 0) {
@@ -831,91 +888,250 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThr, 3)
     }
     __syncthreads();
   } else if (R > 0 && !fits && Rin > 0) {
-    // many members: the exact fraction threshold by 8-bit radix levels over
-    // the keys (unless they all hold one fraction), then the remaining tickets
-    // go to the lowest ids holding the threshold fraction
-    auto is_member = [&](int s) -> bool {
-      if (s < off || s >= off + n) return false;
+    // many members (exact ties): every member's exact fraction is computed
+    // once, on compacted windows so that whole warps work, and counted in a
+    // small table of distinct fractions per CTA; the row's tables give the
+    // threshold fraction, and the remaining tickets go to the lowest ids
+    // holding it.  More distinct fractions than a table holds: 8-bit radix
+    // levels over the exact fractions.
+    ManyShared& ms = sh.many;
+    constexpr uint32_t kMark = kGrant;  // marked member: grant bit set, pos bit clear
+    auto low_of = [&](int s) -> uint32_t {
       const uint32_t w = slu[s];
-      if (w != kEsc) return (w & kLowMask) == thr;
+      if (w != kEsc) return w & kLowMask;
       const int j = esc_find(sh, s);
-      return j >= 0 && sh.esc[j].low == thr;
+      return j < 0 ? 0u : sh.esc[j].low;
     };
-    uint64_t kmin = ~0ull, kmax = 0ull;
-    for (int g = tid; g < ngroups; g += kThr)
-      for (int i = 0; i < 4; ++i)
-        if (is_member(4 * g + i)) {
-          const uint64_t key = exact_key(4 * g + i);
-          kmin = min(kmin, key);
-          kmax = max(kmax, key);
-        }
-    kmin = block_reduce(kmin, OpMinU64(), sh.wred64);
-    kmax = block_reduce(kmax, OpMaxU64(), sh.wred64);
-    if (tid == 0) {
-      sh.pub.kmin = kmin;
-      sh.pub.kmax = kmax;
-    }
-    cluster.sync();
-    if (tid == 0) {
-      uint64_t a = ~0ull, b = 0ull;
-      for (int r = 0; r < kCl; ++r) {
-        a = min(a, *cluster.map_shared_rank(&sh.pub.kmin, r));
-        b = max(b, *cluster.map_shared_rank(&sh.pub.kmax, r));
+    auto set_low = [&](int s, uint32_t low) {
+      const uint32_t w = slu[s];
+      if (w != kEsc) {
+        slu[s] = (w & ~kLowMask) | low;
+        return;
       }
+      const int j = esc_find(sh, s);
+      if (j >= 0) sh.esc[j].low = low;
+    };
+    auto is_member = [&](int s) -> bool { return s >= off && s < off + n && low_of(s) == thr; };
+    auto cls_state = [&](uint32_t low) -> int {  // -1: not a marked member
+      return ((low & (kMark | kPos)) == kMark) ? (int)ms.state[low & (kTab - 1)] : -1;
+    };
+    const int npos = 4 * ngroups;
+    if (tid < kTab) {
+      ms.tkey[tid] = ~0ull;
+      ms.tcnt[tid] = 0u;
+    }
+    uint32_t tovf = 0;
+    uint64_t kmn = ~0ull, kmx = 0ull;
+    for (int wb = 0; wb < npos; wb += kWin) {
+      constexpr int kPer = kWin / kThr;  // positions per thread in a window
+      const int p0 = wb + tid * kPer;
+      uint32_t bits = 0, cnt = 0;
+      for (int i = 0; i < kPer; ++i)
+        if (p0 + i < npos && is_member(p0 + i)) {
+          bits |= 1u << i;
+          ++cnt;
+        }
+      uint32_t tot;
+      const uint32_t incl = block_inclusive_scan(cnt, sh.wred32, &tot);
+      uint32_t o = incl - cnt;
+      for (int i = 0; i < kPer; ++i)
+        if ((bits >> i) & 1u) ms.list[o++] = (uint16_t)(p0 + i);
+      __syncthreads();
+      for (uint32_t j0 = 0; j0 < tot; j0 += kThr) {
+        const uint32_t j = j0 + tid;
+        const bool valid = j < tot;
+        const int sp = valid ? (int)ms.list[j] : 0;
+        const uint64_t key = valid ? exact_key(sp) : ~0ull;
+        if (valid) {
+          kmn = min(kmn, key);
+          kmx = max(kmx, key);
+        }
+        const unsigned grp = __match_any_sync(0xffffffffu, key);
+        const int leader = __ffs(grp) - 1;
+        uint32_t cls = kTab;
+        if (valid && lane == leader) {
+          int h = (int)((key ^ (key >> 23) ^ (key >> 41)) & (uint64_t)(kTab - 1));
+          for (int t = 0; t < kTab; ++t) {
+            const unsigned long long old = atomicCAS(
+                reinterpret_cast<unsigned long long*>(&ms.tkey[h]), ~0ull, (unsigned long long)key);
+            if (old == ~0ull || old == key) {
+              atomicAdd(&ms.tcnt[h], (uint32_t)__popc(grp));
+              cls = (uint32_t)h;
+              break;
+            }
+            h = (h + 1) & (kTab - 1);
+          }
+        }
+        cls = __shfl_sync(0xffffffffu, cls, leader);
+        if (valid) {
+          if (cls < (uint32_t)kTab) set_low(sp, kMark | cls);
+          else tovf = 1u;
+        }
+      }
+      __syncthreads();
+    }
+    tovf = block_reduce(tovf, OpOrU32(), sh.wred32);
+    kmn = block_reduce(kmn, OpMinU64(), sh.wred64);
+    kmx = block_reduce(kmx, OpMaxU64(), sh.wred64);
+    if (tid == 0) {
+      sh.pub.flags4 = tovf;
+      sh.pub.kmin = kmn;
+      sh.pub.kmax = kmx;
+    }
+    cluster.sync();  // tables published
+    if (tid == 0) {
+      uint32_t fo = 0;
+      uint64_t a = ~0ull, bb = 0ull;
+      for (int r = 0; r < kCl; ++r) {
+        fo |= *cluster.map_shared_rank(&sh.pub.flags4, r);
+        a = min(a, *cluster.map_shared_rank(&sh.pub.kmin, r));
+        bb = max(bb, *cluster.map_shared_rank(&sh.pub.kmax, r));
+      }
+      sh.fovf = fo;
       sh.gmin = a;
-      sh.gmax = b;
+      sh.gmax = bb;
     }
     __syncthreads();
-    const uint64_t gmin = sh.gmin, gmax = sh.gmax;
-    const bool one_key = (gmin == gmax);
-    uint64_t thrk = gmin, prefix = 0ull;
-    uint32_t need = Rin;
-    if (!one_key) {
-      for (int lvl = 0; lvl < 8; ++lvl) {
-        const int sft = 56 - 8 * lvl;
-        cluster.sync();  // peers are done reading this CTA's histogram
-        for (int i = tid; i < 256; i += kThr) sh.hist[i] = 0u;
-        __syncthreads();
+    uint32_t mine = 0;
+    if (sh.fovf == 0u) {
+      // every table of the row, merged here
+      if (tid == 0) {
+        sh.thrk = 0ull;
+        sh.need = 0u;
+      }
+      for (int t = tid; t < kCl * kTab; t += kThr) {
+        const int r = t / kTab, slot = t % kTab;
+        ms.merged.key[t] = *cluster.map_shared_rank(&ms.tkey[slot], r);
+        ms.merged.cnt[t] = *cluster.map_shared_rank(&ms.tcnt[slot], r);
+      }
+      __syncthreads();
+      // the threshold fraction holds the Rin-th ticket: above < Rin <= above + at
+      for (int t = tid; t < kCl * kTab; t += kThr) {
+        if (ms.merged.cnt[t] == 0u) continue;
+        const uint64_t kt = ms.merged.key[t];
+        uint32_t above = 0, at = 0;
+        for (int u = 0; u < kCl * kTab; ++u) {
+          const uint32_t cu = ms.merged.cnt[u];
+          const uint64_t ku = ms.merged.key[u];
+          above += (cu != 0u && ku > kt) ? cu : 0u;
+          at += (cu != 0u && ku == kt) ? cu : 0u;
+        }
+        if (above < Rin && Rin <= above + at) {
+          sh.thrk = kt;
+          sh.need = Rin - above;
+        }
+      }
+      __syncthreads();
+      const uint64_t thrk = sh.thrk;
+      if (tid < kTab) {
+        const uint64_t kt = ms.tkey[tid];
+        ms.state[tid] = (ms.tcnt[tid] == 0u) ? 0 : (kt > thrk ? 1 : (kt == thrk ? 2 : 0));
+      }
+      __syncthreads();
+      // members above the threshold fraction get their ticket, those below
+      // none; those at it are counted per warp segment (id order)
+      const int seg = (npos + kWarps - 1) / kWarps;
+      const int a0 = warp * seg, a1 = min(npos, a0 + seg);
+      uint32_t wat = 0;
+      for (int s0 = a0; s0 < a1; s0 += 32) {
+        const int sp = s0 + lane;
+        const int stt = (sp < a1) ? cls_state(low_of(sp)) : -1;
+        if (stt == 1) {
+          set_low(sp, thr);
+          grant_member(sp);
+          ++mine;
+        } else if (stt == 0) {
+          set_low(sp, thr);
+        }
+        wat += (uint32_t)__popc(__ballot_sync(0xffffffffu, stt == 2));
+      }
+      if (lane == 0) sh.wcnt[warp] = wat;
+      __syncthreads();
+      if (tid == 0) {
+        uint32_t t = 0;
+        for (int w = 0; w < kWarps; ++w) t += sh.wcnt[w];
+        sh.pub.n_eq = t;
+      }
+      cluster.sync();
+      if (tid == 0) {
+        uint32_t base = 0;
+        for (int r = 0; r < rank; ++r) base += *cluster.map_shared_rank(&sh.pub.n_eq, r);
+        sh.scan_base = base;
+      }
+      __syncthreads();
+      uint32_t base = sh.scan_base;
+      for (int w = 0; w < warp; ++w) base += sh.wcnt[w];
+      const uint32_t need = sh.need;
+      for (int s0 = a0; s0 < a1; s0 += 32) {
+        const int sp = s0 + lane;
+        const bool at = (sp < a1) && cls_state(low_of(sp)) == 2;
+        const unsigned msk = __ballot_sync(0xffffffffu, at);
+        if (at) {
+          const uint32_t rk = base + (uint32_t)__popc(msk & ((1u << lane) - 1u));
+          set_low(sp, thr);
+          if (rk < need) {
+            grant_member(sp);
+            ++mine;
+          }
+        }
+        base += (uint32_t)__popc(msk);
+      }
+      __syncthreads();
+    } else {
+      // the members marked in the tables become plain members again
+      for (int sp = tid; sp < npos; sp += kThr)
+        if (cls_state(low_of(sp)) >= 0) set_low(sp, thr);
+      __syncthreads();
+      const uint64_t gmin = sh.gmin, gmax = sh.gmax;
+      const bool one_key = (gmin == gmax);
+      uint64_t thrk = gmin, prefix = 0ull;
+      uint32_t need = Rin;
+      if (!one_key) {
+        for (int lvl = 0; lvl < 8; ++lvl) {
+          const int sft = 56 - 8 * lvl;
+          cluster.sync();  // peers are done reading this CTA's histogram
+          for (int i = tid; i < 256; i += kThr) sh.hist[i] = 0u;
+          __syncthreads();
+          for (int g = tid; g < ngroups; g += kThr)
+            for (int i = 0; i < 4; ++i) {
+              const int s = 4 * g + i;
+              if (!is_member(s)) continue;
+              const uint64_t key = exact_key(s);
+              if (lvl > 0 && (key >> (sft + 8)) != prefix) continue;
+              atomicAdd(&sh.hist[(key >> sft) & 255u], 1u);
+            }
+          __syncthreads();
+          if (tid < 64)
+            sh.pub.coarse[tid] = sh.hist[4 * tid] + sh.hist[4 * tid + 1] + sh.hist[4 * tid + 2] +
+                                 sh.hist[4 * tid + 3];
+          cluster.sync();
+          select_cluster(cluster, sh, 256, need);
+          prefix = (prefix << 8) | (uint64_t)sh.sel_bin;
+          need -= sh.sel_above;
+        }
+        thrk = prefix;
+      }
+      if (!one_key)
         for (int g = tid; g < ngroups; g += kThr)
           for (int i = 0; i < 4; ++i) {
             const int s = 4 * g + i;
-            if (!is_member(s)) continue;
-            const uint64_t key = exact_key(s);
-            if (lvl > 0 && (key >> (sft + 8)) != prefix) continue;
-            atomicAdd(&sh.hist[(key >> sft) & 255u], 1u);
+            if (is_member(s) && exact_key(s) > thrk) {
+              grant_member(s);
+              ++mine;
+            }
           }
-        __syncthreads();
-        if (tid < 64)
-          sh.pub.coarse[tid] = sh.hist[4 * tid] + sh.hist[4 * tid + 1] + sh.hist[4 * tid + 2] +
-                               sh.hist[4 * tid + 3];
-        cluster.sync();
-        select_cluster(cluster, sh, 256, need);
-        prefix = (prefix << 8) | (uint64_t)sh.sel_bin;
-        need -= sh.sel_above;
-      }
-      thrk = prefix;
+      __syncthreads();
+      // members granted above are no longer members (their low bits changed)
+      ordered_ranks(
+          cluster, sh, ngroups,
+          [&](int s) -> bool { return is_member(s) && (one_key || exact_key(s) == thrk); },
+          [&](int s, uint32_t rk) {
+            if (rk < need) {
+              grant_member(s);
+              ++mine;
+            }
+          });
     }
-    uint32_t mine = 0;
-    if (!one_key)
-      for (int g = tid; g < ngroups; g += kThr)
-        for (int i = 0; i < 4; ++i) {
-          const int s = 4 * g + i;
-          if (is_member(s) && exact_key(s) > thrk) {
-            grant_member(s);
-            ++mine;
-          }
-        }
-    __syncthreads();
-    // members granted above are no longer members (their low bits changed)
-    ordered_ranks(
-        cluster, sh, ngroups,
-        [&](int s) -> bool { return is_member(s) && (one_key || exact_key(s) == thrk); },
-        [&](int s, uint32_t rk) {
-          if (rk < need) {
-            grant_member(s);
-            ++mine;
-          }
-        });
     mine = block_reduce(mine, OpAddU32(), sh.wred32);
     if (tid == 0) sh.pub.n_grant = mine;
     cluster.sync();
@@ -943,42 +1159,61 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThr, 3)
   // before leaving
   cluster.barrier_arrive();
 
-  // ---- fused draft draw: the CTA whose range holds D scans its counts
+  // ---- fused draft draw: the CTA whose range holds D finds the block of 32
+  // groups holding it from the block sums, then the token inside it (warp 0)
   if (p.tokens && status == DSPARK_ST_OK) {
     const int b = row / p.depth, j = row % p.depth;
     const uint32_t req = p.request_ids ? p.request_ids[b] : (uint32_t)b;
     const uint32_t D = draw_u32(p.seed, req, (uint32_t)j, DSPARK_PURPOSE_PROPOSAL) >> 8;
-    if (D >= cbefore && D - cbefore < my_total) {
-      // one contiguous segment of slice positions per warp
-      const int ns = 4 * ngroups;
-      const int seg = (ns + kWarps - 1) / kWarps;
-      const int a0 = warp * seg, a1 = min(ns, a0 + seg);
-      uint32_t ssum = 0;
-      for (int s = a0 + lane; s < a1; s += 32) ssum += count_of(sh, slu, s, thr);
-      ssum = warp_reduce(ssum, OpAddU32());
-      if (lane == 0) sh.wred32[warp] = ssum;
-      __syncthreads();
-      uint32_t sb = cbefore;
-      for (int w2 = 0; w2 < warp; ++w2) sb += sh.wred32[w2];
-      if (D >= sb && D - sb < sh.wred32[warp]) {
-        uint32_t base = sb;
-        for (int s0 = a0; s0 < a1; s0 += 32) {
-          const int s = s0 + lane;
-          const uint32_t cv = (s < a1) ? count_of(sh, slu, s, thr) : 0u;
-          uint32_t incl = cv;
+    if (warp == 0 && D >= cbefore && D - cbefore < my_total) {
+      const uint32_t t = D - cbefore;
+      const int nblk = (ngroups + 31) / 32;
+      uint32_t base = 0;
+      int blk = -1;
+      for (int k0 = 0; k0 < nblk && blk < 0; k0 += 32) {
+        const int k = k0 + lane;
+        const uint32_t v = (k < nblk) ? sh.bsum[k] : 0u;
+        uint32_t incl = v;
 #pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += t;
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += u;
+        }
+        const bool hit = v > 0u && t - base < incl && t - base >= incl - v;
+        const unsigned msk = __ballot_sync(0xffffffffu, hit);
+        if (msk) {
+          const int l = __ffs(msk) - 1;
+          blk = k0 + l;
+          base += __shfl_sync(0xffffffffu, incl - v, l);
+        } else {
+          base += __shfl_sync(0xffffffffu, incl, 31);
+        }
+      }
+      if (blk >= 0) {
+        const int g = blk * 32 + lane;
+        uint32_t cv[4] = {0u, 0u, 0u, 0u};
+        uint32_t gs = 0;
+        if (g < ngroups)
+          for (int i = 0; i < 4; ++i) {
+            cv[i] = count_of(sh, slu, 4 * g + i, thr);
+            gs += cv[i];
           }
-          const uint32_t tile = __shfl_sync(0xffffffffu, incl, 31);
-          if (D - base < tile) {
-            const bool hit = cv > 0u && D - base < incl && D - base >= incl - cv;
-            const unsigned msk = __ballot_sync(0xffffffffu, hit);
-            if (lane == 0 && msk) p.tokens[row] = lo - off + s0 + __ffs(msk) - 1;
-            break;
+        uint32_t incl = gs;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += u;
+        }
+        const uint32_t tb = t - base;
+        if (gs > 0u && tb < incl && tb >= incl - gs) {
+          uint32_t cum = incl - gs;
+          for (int i = 0; i < 4; ++i) {
+            cum += cv[i];
+            if (tb < cum) {
+              p.tokens[row] = lo - off + 4 * g + i;
+              break;
+            }
           }
-          base += tile;
         }
       }
     }
