@@ -240,6 +240,9 @@ struct VSh2 {
   int timeout;
   int found;
   uint32_t near;
+  int dec;          // ratio decision of the row: 1 accept, 0 reject, -1 refuse (status in dst)
+  int dst;
+  uint32_t dflags;
 };
 
 struct OpMaxNaNv {
@@ -248,6 +251,10 @@ struct OpMaxNaNv {
     asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
     return r;
   }
+};
+
+struct OpAddF {
+  __device__ float operator()(float a, float b) const { return __fadd_rn(a, b); }
 };
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -371,6 +378,55 @@ __global__ void __cluster_dims__(kVCluster, 1, 1) __launch_bounds__(kVThreads, 3
               in ? __ldg(reinterpret_cast<const unsigned short*>(gbase) + s) : (uint16_t)0xFF80u;
       }
     }
+    // ratio mode: the inputs of the decision, fetched while the copies fly
+    float zx = 0.0f;
+    uint32_t cx = 0u, U = 0u;
+    const uint32_t* qrow = nullptr;  // dense counts row j
+    const int32_t* sids = nullptr;   // sparse row j
+    const uint32_t* scnt = nullptr;
+    int snnz = 0;
+    if (kMode == kRatio && j < depth) {
+      const int x = drafts[j];
+      const int64_t qr = (int64_t)b * depth + j;
+      if (p.top_k == 0) {
+        qrow = p.counts + qr * V;
+        if (tid == 0) cx = __ldg(qrow + x);
+      } else {
+        // canonical sparse row: 1 <= nnz <= top_k, ids strictly ascending in
+        // [0, V), counts > 0, total M
+        const int32_t* ids = p.ids + qr * p.top_k;
+        const uint32_t* cn = p.counts + qr * p.top_k;
+        const int nz = p.nnz[qr];
+        if (tid == 0) {
+          sh.q_ok = 1;
+          sh.q_c = 0u;
+        }
+        __syncthreads();
+        uint64_t tot = 0;
+        if (nz < 1 || nz > p.top_k) {
+          if (tid == 0) sh.q_ok = 0;
+        } else {
+          for (int i = tid; i < nz; i += kVThreads) {
+            const int id = ids[i];
+            const uint32_t cc = cn[i];
+            if (id < 0 || id >= V || cc == 0u || (i > 0 && ids[i - 1] >= id)) sh.q_ok = 0;
+            if (id == x) sh.q_c = cc;
+            tot += cc;
+          }
+        }
+        tot = block_reduce(tot, OpAddU64(), sh.wz);
+        if (tid == 0 && nz >= 1 && nz <= p.top_k && tot != (uint64_t)kM) sh.q_ok = 0;
+        __syncthreads();
+        if (tid == 0) cx = sh.q_c;
+        sids = ids;
+        scnt = cn;
+        snnz = nz;
+      }
+      if (tid == 0) {
+        zx = load_logit(zrow, kDt, x);
+        U = draw_u32(p.seed, req, (uint32_t)j, DSPARK_PURPOSE_ACCEPT) >> 8;
+      }
+    }
     if (n_int > 0) {
       if (tid == 0)
         for (int c = 0; c < kVTma; ++c)
@@ -394,24 +450,10 @@ __global__ void __cluster_dims__(kVCluster, 1, 1) __launch_bounds__(kVThreads, 3
         }
       }
     }
-    if (kMode == kRatio && mx > -INFINITY && mx < INFINITY) {
-      for (int g = tid; g < ng; g += kVThreads) {
-        float z[EPG];
-        group(g, z);
-#pragma unroll
-        for (int i = 0; i < EPG; ++i) sm += (z[i] == -INFINITY) ? 0.0f : expf(z[i] - mx);
-      }
-    }
-    // block merge
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-      const float m2 = __shfl_xor_sync(0xffffffffu, mx, o);
-      if (kMode == kRatio) {
-        const float s2 = __shfl_xor_sync(0xffffffffu, sm, o);
-        if (mx == mx && m2 == m2 && mx < INFINITY && m2 < INFINITY) ms_merge(mx, sm, m2, s2);
-        else mx = OpMaxNaNv()(mx, m2);
-      } else {
-        mx = OpMaxNaNv()(mx, m2);
+      mx = OpMaxNaNv()(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      if (kMode == kGreedy) {
         const float a2 = __shfl_xor_sync(0xffffffffu, amv, o);
         const int i2 = __shfl_xor_sync(0xffffffffu, ami, o);
         am_merge(amv, ami, a2, i2);
@@ -419,23 +461,31 @@ __global__ void __cluster_dims__(kVCluster, 1, 1) __launch_bounds__(kVThreads, 3
     }
     if (lane == 0) {
       sh.wm[warp] = mx;
-      sh.ws[warp] = sm;
       sh.wam[warp] = amv;
       sh.wai[warp] = ami;
     }
     __syncthreads();
-    if (tid == 0) {
-      float m = sh.wm[0], s = sh.ws[0], av = sh.wam[0];
-      int ai = sh.wai[0];
-      for (int w = 1; w < kVThreads / 32; ++w) {
-        if (kMode == kRatio) {
-          const float m2 = sh.wm[w], s2 = sh.ws[w];
-          if (m == m && m2 == m2 && m < INFINITY && m2 < INFINITY) ms_merge(m, s, m2, s2);
-          else m = OpMaxNaNv()(m, m2);
-        } else {
-          m = OpMaxNaNv()(m, sh.wm[w]);
-          am_merge(av, ai, sh.wam[w], sh.wai[w]);
+    float cm = sh.wm[0];  // the CTA's max
+    for (int w = 1; w < kVThreads / 32; ++w) cm = OpMaxNaNv()(cm, sh.wm[w]);
+    if (kMode == kRatio) {
+      // the sum of exp relative to the CTA's max: a plain sum
+      if (cm > -INFINITY && cm < INFINITY)
+        for (int g = tid; g < ng; g += kVThreads) {
+          float z[EPG];
+          group(g, z);
+#pragma unroll
+          for (int i = 0; i < EPG; ++i) sm += expf(__fsub_rn(z[i], cm));
         }
+      sm = warp_reduce(sm, OpAddF());
+      if (lane == 0) sh.ws[warp] = sm;
+      __syncthreads();
+    }
+    if (tid == 0) {
+      float m = cm, s = 0.0f, av = sh.wam[0];
+      int ai = sh.wai[0];
+      for (int w = 0; w < kVThreads / 32; ++w) {
+        if (kMode == kRatio) s += sh.ws[w];
+        else if (w > 0) am_merge(av, ai, sh.wam[w], sh.wai[w]);
       }
       VX& e = sh.x[xi];
       e.m = m;
@@ -467,6 +517,28 @@ __global__ void __cluster_dims__(kVCluster, 1, 1) __launch_bounds__(kVThreads, 3
       sh.AMV = av;
       sh.AMI = ai;
       sh.FL = fl;
+      if (kMode == kRatio && j < depth && !bad && m > -INFINITY && !(fl & 1u)) {
+        // the ratio test: accept iff U * c < p(x) * 2^48
+        int dec = 0, dst = DSPARK_ST_OK;
+        uint32_t dfl = 0;
+        if (p.top_k > 0 && !sh.q_ok) {
+          dec = -1;
+          dst = DSPARK_ST_BAD_Q;
+        } else if (cx == 0u) {
+          dec = -1;
+          dst = DSPARK_ST_BAD_DRAFT;
+        } else {
+          const float px = (zx == -INFINITY) ? 0.0f : __fdiv_rn(expf(zx - m), s);
+          const double uc = (double)((uint64_t)U * (uint64_t)cx);
+          const double p48 = (double)px * 281474976710656.0;
+          if (fabs(uc * 0x1p-48 - (double)px) <= 1e-6 * ((double)cx * 0x1p-24))
+            dfl = DSPARK_FLAG_AMBIG_ACCEPT;
+          dec = (uc < p48) ? 1 : 0;
+        }
+        sh.dec = dec;
+        sh.dst = dst;
+        sh.dflags = dfl;
+      }
     }
     xi ^= 1;
     __syncthreads();
@@ -492,67 +564,16 @@ __global__ void __cluster_dims__(kVCluster, 1, 1) __launch_bounds__(kVThreads, 3
       continue;
     }
 
-    // ---- ratio test of draft j
+    // ---- ratio test of draft j (decided above by thread 0)
     bool use_q = false;
     uint32_t purpose = DSPARK_PURPOSE_BONUS;
-    const uint32_t* qrow = nullptr;  // dense counts row j
-    const int32_t* sids = nullptr;   // sparse row j
-    const uint32_t* scnt = nullptr;
-    int snnz = 0;
     if (j < depth) {
-      const int x = drafts[j];
-      const int64_t qr = (int64_t)b * depth + j;
-      uint32_t c;
-      if (p.top_k == 0) {
-        qrow = p.counts + qr * V;
-        c = __ldg(qrow + x);
-      } else {
-        // canonical sparse row: 1 <= nnz <= top_k, ids strictly ascending in
-        // [0, V), counts > 0, total M
-        const int32_t* ids = p.ids + qr * p.top_k;
-        const uint32_t* cn = p.counts + qr * p.top_k;
-        const int nz = p.nnz[qr];
-        if (tid == 0) {
-          sh.q_ok = 1;
-          sh.q_c = 0u;
-        }
-        __syncthreads();
-        uint64_t tot = 0;
-        if (nz < 1 || nz > p.top_k) {
-          if (tid == 0) sh.q_ok = 0;
-        } else {
-          for (int i = tid; i < nz; i += kVThreads) {
-            const int id = ids[i];
-            const uint32_t cc = cn[i];
-            if (id < 0 || id >= V || cc == 0u || (i > 0 && ids[i - 1] >= id)) sh.q_ok = 0;
-            if (id == x) sh.q_c = cc;
-            tot += cc;
-          }
-        }
-        tot = block_reduce(tot, OpAddU64(), sh.wz);
-        if (tid == 0 && nz >= 1 && nz <= p.top_k && tot != (uint64_t)kM) sh.q_ok = 0;
-        __syncthreads();
-        if (!sh.q_ok) {
-          status = DSPARK_ST_BAD_Q;
-          break;
-        }
-        c = sh.q_c;
-        sids = ids;
-        scnt = cn;
-        snnz = nz;
-      }
-      if (c == 0u) {
-        status = DSPARK_ST_BAD_DRAFT;
+      if (sh.dec < 0) {
+        status = sh.dst;
         break;
       }
-      const float zx = load_logit(zrow, kDt, x);
-      const float px = (zx == -INFINITY) ? 0.0f : __fdiv_rn(expf(zx - M), S);
-      const uint32_t U = draw_u32(p.seed, req, (uint32_t)j, DSPARK_PURPOSE_ACCEPT) >> 8;
-      const double uc = (double)((uint64_t)U * (uint64_t)c);
-      const double p48 = (double)px * 281474976710656.0;
-      if (fabs(uc * 0x1p-48 - (double)px) <= 1e-6 * ((double)c * 0x1p-24))
-        flags |= DSPARK_FLAG_AMBIG_ACCEPT;
-      if (uc < p48) continue;  // accepted
+      flags |= sh.dflags;
+      if (sh.dec == 1) continue;  // accepted
       L = j;
       use_q = true;
       purpose = DSPARK_PURPOSE_RESIDUAL;
@@ -586,6 +607,8 @@ __global__ void __cluster_dims__(kVCluster, 1, 1) __launch_bounds__(kVThreads, 3
       return 0u;
     };
     const int nblk = (ng + 31) / 32;
+    const bool qvec = qrow != nullptr &&
+                      (reinterpret_cast<uintptr_t>(qrow + lo - off) & 15u) == 0u;
     for (int attempt = 0; attempt < 2; ++attempt) {
       const bool dense_q = use_q && qrow != nullptr;
       const bool sparse_qm = use_q && sids != nullptr;
@@ -594,17 +617,38 @@ __global__ void __cluster_dims__(kVCluster, 1, 1) __launch_bounds__(kVThreads, 3
         const int g = gb + tid;
         uint64_t gsum = 0;
         if (g < ng) {
+          // the counts first (128-bit loads for a full, aligned group), then
+          // the weights
+          uint32_t qv[EPG];
+#pragma unroll
+          for (int i = 0; i < EPG; ++i) qv[i] = 0u;
+          if (dense_q) {
+            if (qvec && g >= g_first && g <= g_last) {
+              const uint4* qp = reinterpret_cast<const uint4*>(qrow + lo - off) + g * (EPG / 4);
+#pragma unroll
+              for (int k = 0; k < EPG / 4; ++k) {
+                const uint4 t4 = __ldg(qp + k);
+                qv[4 * k] = t4.x;
+                qv[4 * k + 1] = t4.y;
+                qv[4 * k + 2] = t4.z;
+                qv[4 * k + 3] = t4.w;
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < EPG; ++i) {
+                const int s = g * EPG + i;
+                if (s >= off && s < off + n) qv[i] = __ldg(qrow + (lo - off + s));
+              }
+            }
+          }
           float z[EPG];
           group(g, z);
 #pragma unroll
           for (int i = 0; i < EPG; ++i) {
-            const int s = g * EPG + i;
-            const bool in = (s >= off && s < off + n);
             float r = pv(z[i]);
-            if (dense_q && in) {
-              const uint32_t q = __ldg(qrow + (lo - off + s));
-              cs += q;
-              r = fmaxf(__fsub_rn(r, (float)q * 0x1p-24f), 0.0f);
+            if (dense_q) {
+              cs += qv[i];
+              r = fmaxf(__fsub_rn(r, (float)qv[i] * 0x1p-24f), 0.0f);
             }
             gsum += wfix(r);
           }
