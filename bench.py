@@ -25,6 +25,7 @@ by rank), no collective on the data path; the time is the max over ranks.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -117,7 +118,47 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
+# ------------------------------------------------------- multi-rank
+def rank_request_ids(request_ids, rank, B):
+    """Request ids of a rank's B requests: every rank runs its own requests,
+    offset by rank * B, so the outputs equal those of one batch of all ranks'
+    requests (the RNG is keyed by request id) and no data is exchanged."""
+    return (np.asarray(request_ids, np.uint32) + np.uint32(rank * B)).astype(np.uint32)
+
+
+def max_over_ranks(values):
+    """In place: the element-wise max of a float tensor over all ranks."""
+    import torch
+    torch.distributed.all_reduce(values, op=torch.distributed.ReduceOp.MAX)
+    return values
+
+
 # ------------------------------------------------------------ our arm
+def profiled_traffic(wl, dom):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary (per draft row, scaled by the rows of one launch), or None when
+    there is none for it or its sources changed since the counters were taken."""
+    if dom != "q_build_sample" or wl.top_k != 0:
+        return None
+    try:
+        text = open(os.path.join(ROOT, "profiles", "q_dense_c4_b64.md")).read()
+        vals = {}
+        for line in text.splitlines():
+            if line.startswith(("traffic_bytes_per_row:", "sources_sha256_16:")):
+                k, v = line.split(":", 1)
+                vals[k] = v.strip()
+        h = hashlib.sha256()
+        for name in ("q_dense.cu", "common.cuh"):
+            with open(os.path.join(ROOT, "draft_sampling_verification_gb300", "csrc", name),
+                      "rb") as f:
+                h.update(f.read())
+        if h.hexdigest()[:16] != vals.get("sources_sha256_16"):
+            return None
+        return int(vals["traffic_bytes_per_row"]) * wl.B * wl.depth
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def algorithmic_bytes(wl, acc_greedy, acc_ratio):
     """Bytes each kernel must move per launch (what the method reads/writes)."""
     R_d = wl.B * wl.depth
@@ -152,7 +193,7 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     wl = W.by_name(args.workload, **({"B": args.batch} if args.batch else {}))
     B, depth, V = wl.B, wl.depth, wl.V
-    req_np = (wl.request_ids + np.uint32(rank * B)).astype(np.uint32)
+    req_np = rank_request_ids(wl.request_ids, rank, B)
 
     # inputs resident in HBM
     xd = torch.from_numpy(wl.draft).to(dev)
@@ -282,8 +323,7 @@ def run_ours(args, rank, world, local_rank):
 
     ms = elapsed_ms / args.steps
     if world > 1:
-        t = torch.tensor([ms, e2e["ms_per_step"] if e2e else 0.0], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        t = max_over_ranks(torch.tensor([ms, e2e["ms_per_step"] if e2e else 0.0], device=dev))
         ms, e2e_max = float(t[0]), float(t[1])
         if e2e:
             e2e["ms_per_step"] = e2e_max
@@ -396,7 +436,8 @@ def main():
                 "kernel_algorithmic_bytes": abytes,
             },
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
-                         "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                         "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": profiled_traffic(wl, dom),
                          "peak_source": "measured" if peaks else "fallback"},
             "clocks": clocks,
             "gpu_launches": len(per_kernel) * args.steps,
