@@ -29,6 +29,7 @@ SIGNATURES = {
     "dspark_target_probs": [_P, _I32, _I64, _I32, _I32, _P, _P, _P, _P],
     "dspark_debug_exp_weights": [_P, _I64, _P, _P, _P],
     "dspark_debug_philox": [_P, _U64, _I64, _P, _P],
+    "dspark_debug_alloc_scale": [_P, _I64, _P, _P, _P, _P, _P],
 }
 
 _lock = threading.Lock()

@@ -208,12 +208,82 @@ __device__ __forceinline__ uint32_t frac_bucket(const AllocSplit& a) {
   return (sh >= 64) ? 0u : (uint32_t)(a.rnum >> sh);
 }
 
-// Exact fraction as an FP64 bit pattern (monotone for r >= 0).
+// Exact fraction r = rnum * 2^-t as its FP64 bit pattern (monotone in r,
+// equal for equal r), built with integer operations: rnum < 2^53, so the
+// double is exact and normal for the t that occur (t <= ~90).
 __device__ __forceinline__ uint64_t frac_key(const AllocSplit& a) {
-  // 2^-t built from its bits (t <= 90 here, so the power is a normal double)
-  const double scale = __longlong_as_double((long long)(1023 - a.t) << 52);
-  const double r = __dmul_rn(__ull2double_rn(a.rnum), scale);
-  return (uint64_t)__double_as_longlong(r);
+  if (a.rnum == 0ull) return 0ull;
+  const int nb = 64 - __clzll((long long)a.rnum);        // bits of rnum, 1..53
+  const uint64_t mant = a.rnum << (53 - nb);              // [2^52, 2^53)
+  const uint64_t bexp = (uint64_t)(1023 + (nb - 1) - a.t);
+  return (bexp << 52) | (mant & ((1ull << 52) - 1ull));
+}
+
+// The allocation scale k = RN64(2^24 / RN64(S)) for S >= 1, exactly as the
+// FP64 operations would round it, with integer arithmetic only (FP64 is slow
+// on this GPU): k = mk * 2^ek with mk in [2^52, 2^53); also khi = RN32(k) and
+// klo = RN32(k - khi).
+struct AllocScale {
+  uint64_t mk;
+  int ek;
+  float khi, klo;
+};
+
+__device__ __forceinline__ float pow2f(int e) {  // 2^e for a normal float exponent
+  return __int_as_float((e + 127) << 23);
+}
+
+__device__ __forceinline__ AllocScale alloc_scale(uint64_t S) {
+  // RN64(S) = m * 2^E, m in [2^52, 2^53)
+  const int nb = 64 - __clzll((long long)S);
+  uint64_t m;
+  int E;
+  if (nb <= 53) {
+    m = S << (53 - nb);
+    E = nb - 53;
+  } else {
+    const int sh = nb - 53;
+    m = S >> sh;
+    const uint64_t rem = S & ((1ull << sh) - 1ull), half = 1ull << (sh - 1);
+    if (rem > half || (rem == half && (m & 1ull))) ++m;
+    E = sh;
+    if (m == (1ull << 53)) {
+      m >>= 1;
+      ++E;
+    }
+  }
+  // k = RN64(2^(24 - E) / m)
+  uint64_t t;
+  int ke;
+  if (m == (1ull << 52)) {
+    t = 1ull << 52;
+    ke = 24 - E - 104;
+  } else {
+    // q = floor(2^116 / m) in (2^63, 2^64); drop 11 bits with round-to-nearest-even
+    const unsigned __int128 num = (unsigned __int128)1 << 116;
+    const uint64_t q = (uint64_t)(num / m);
+    const uint64_t r = (uint64_t)(num - (unsigned __int128)q * m);
+    t = q >> 11;
+    const uint32_t d = (uint32_t)(q & 2047u);
+    if (d > 1024u || (d == 1024u && (r != 0ull || (t & 1ull)))) ++t;
+    ke = 11 - 116 + 24 - E;
+    if (t == (1ull << 53)) {
+      t >>= 1;
+      ++ke;
+    }
+  }
+  AllocScale o;
+  o.mk = t;
+  o.ek = ke;
+  // khi = RN32(k): the top 24 bits of t, rounded to nearest even
+  uint64_t hm = t >> 29;
+  const uint64_t dr = t & ((1ull << 29) - 1ull);
+  if (dr > (1ull << 28) || (dr == (1ull << 28) && (hm & 1ull))) ++hm;
+  o.khi = __fmul_rn((float)(uint32_t)hm, pow2f(ke + 29));  // hm <= 2^24: exact
+  // klo = RN32(k - khi) = RN32((t - hm 2^29) 2^ke), the difference exact in 64 bits
+  const long long diff = (long long)t - (long long)(hm << 29);
+  o.klo = __fmul_rn(__ll2float_rn(diff), pow2f(ke));
+  return o;
 }
 
 // ------------------------------------------------------------ logit loads

@@ -15,6 +15,19 @@ __global__ void exp_weights_kernel(const float* d, int64_t n, float* e_out, uint
   }
 }
 
+__global__ void alloc_scale_kernel(const uint64_t* S, int64_t n, uint64_t* mk, int32_t* ek,
+                                   float* khi, float* klo) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    dspark::AllocScale a = {0ull, 0, 0.0f, 0.0f};
+    if (S[i] != 0ull) a = dspark::alloc_scale(S[i]);
+    if (mk) mk[i] = a.mk;
+    if (ek) ek[i] = a.ek;
+    if (khi) khi[i] = a.khi;
+    if (klo) klo[i] = a.klo;
+  }
+}
+
 __global__ void philox_kernel(const uint4* ctr, uint64_t seed, int64_t n, uint4* out) {
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x)
@@ -40,6 +53,21 @@ int dspark_debug_exp_weights(const float* d, int64_t n, float* e_out, uint64_t* 
     return DSPARK_ERR_ALIGN;
   exp_weights_kernel<<<grid_for(n), 256, 0, static_cast<cudaStream_t>(stream)>>>(d, n, e_out,
                                                                                    E_out);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? 0 : (int)e;
+}
+
+int dspark_debug_alloc_scale(const uint64_t* S, int64_t n, uint64_t* mk_out, int32_t* ek_out,
+                             float* khi_out, float* klo_out, void* stream) {
+  if (n < 0) return DSPARK_ERR_SIZE;
+  if (n == 0) return 0;
+  if (!S) return DSPARK_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(S) & 7) || (reinterpret_cast<uintptr_t>(mk_out) & 7) ||
+      (reinterpret_cast<uintptr_t>(ek_out) & 3) || (reinterpret_cast<uintptr_t>(khi_out) & 3) ||
+      (reinterpret_cast<uintptr_t>(klo_out) & 3))
+    return DSPARK_ERR_ALIGN;
+  alloc_scale_kernel<<<grid_for(n), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      S, n, mk_out, ek_out, khi_out, klo_out);
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? 0 : (int)e;
 }

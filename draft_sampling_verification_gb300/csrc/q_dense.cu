@@ -74,21 +74,27 @@ struct __align__(16) Esc {
   uint32_t pad;
 };
 
-// Scalars a CTA publishes to its peers (read remotely field by field).
+// Values a CTA publishes for its peers to read (field by field).
 struct __align__(16) Pub {
-  float mx;         // max of the raw logits (NaN-propagating)
-  uint32_t flags1;  // after pass A: bit2 timeout
-  uint32_t F;       // sum of floors
-  uint32_t csum;    // sum of the counts written before member grants
-  uint64_t S;       // sum of E
   uint64_t kmin, kmax;
-  uint32_t ncand;   // members of the threshold bin
   uint32_t n_eq;    // id-order rank exchange
   uint32_t n_grant; // granted members (many-member path)
-  uint32_t flags2;  // after pass B: bit0 a finite logit overflowed to -inf
-  uint32_t flags3;  // after pass C: bit1 internal (escape list full)
   uint32_t flags4;  // many-member path: bit0 a table of fractions overflowed
+  uint32_t pad;
   uint32_t coarse[64];
+};
+
+// Scalars every CTA writes into every peer's copy before a cluster barrier
+// (slot = the writer's rank), so that after it each CTA reads local memory.
+struct __align__(16) Push {
+  uint64_t S[kCl];      // sum of E
+  float mx[kCl];        // max of the raw logits (NaN-propagating)
+  uint32_t fl1[kCl];    // after pass A: bit2 timeout
+  uint32_t fl2[kCl];    // after pass B: bit0 a finite logit overflowed to -inf
+  uint32_t F[kCl];      // sum of floors
+  uint32_t fl3[kCl];    // after pass C: bit1 internal (escape list full)
+  uint32_t csum[kCl];   // sum of the counts written before member grants
+  uint32_t ncand[kCl];  // members of the threshold bin
 };
 
 // Many-member path: member positions compacted per window, then the table of
@@ -116,6 +122,7 @@ struct DShared {
   uint32_t bsum[kBlkCap];  // count sum of each block of 32 groups
   Esc esc[kEscCap];
   Pub pub;
+  Push push;
   uint64_t mbar[kTma];
   uint64_t wred64[kWarps];
   uint32_t wred32[kWarps];
@@ -452,9 +459,9 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThr, 3)
   __syncthreads();
   if (warp == 0) {
     const float m2 = warp0_combine(sh.wredf, -INFINITY, OpMaxNaN());
-    if (lane == 0) {
-      sh.pub.mx = m2;
-      sh.pub.flags1 = sh.timeout ? 4u : 0u;
+    if (lane < kCl) {
+      *cluster.map_shared_rank(&sh.push.mx[rank], lane) = m2;
+      *cluster.map_shared_rank(&sh.push.fl1[rank], lane) = sh.timeout ? 4u : 0u;
     }
   }
   cluster.sync();  // S1
@@ -462,8 +469,8 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThr, 3)
     float mm = -INFINITY;
     uint32_t fl = 0;
     if (lane < kCl) {
-      mm = *cluster.map_shared_rank(&sh.pub.mx, lane);
-      fl = *cluster.map_shared_rank(&sh.pub.flags1, lane);
+      mm = sh.push.mx[lane];
+      fl = sh.push.fl1[lane];
     }
     mm = warp_reduce(mm, OpMaxNaN());
     fl = warp_reduce(fl, OpOrU32());
@@ -534,9 +541,9 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThr, 3)
   if (warp == 0) {
     const uint64_t s2 = warp0_combine(sh.wred64, (uint64_t)0, OpAddU64());
     const uint32_t o2 = warp0_combine(sh.wred32, 0u, OpOrU32());
-    if (lane == 0) {
-      sh.pub.S = s2;
-      sh.pub.flags2 = o2;
+    if (lane < kCl) {
+      *cluster.map_shared_rank(&sh.push.S[rank], lane) = s2;
+      *cluster.map_shared_rank(&sh.push.fl2[rank], lane) = o2;
     }
   }
   cluster.sync();  // S2
@@ -544,19 +551,17 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThr, 3)
     uint64_t sv = 0;
     uint32_t fl = 0;
     if (lane < kCl) {
-      sv = *cluster.map_shared_rank(&sh.pub.S, lane);
-      fl = *cluster.map_shared_rank(&sh.pub.flags2, lane);
+      sv = sh.push.S[lane];
+      fl = sh.push.fl2[lane];
     }
     sv = warp_reduce(sv, OpAddU64());
     fl = warp_reduce(fl, OpOrU32());
     if (lane == 0) {
-      const double kd = __ddiv_rn(16777216.0, __ull2double_rn(sv));
-      const uint64_t kbits = (uint64_t)__double_as_longlong(kd);
-      sh.mk = (kbits & ((1ull << 52) - 1ull)) | (1ull << 52);
-      sh.ek = (int)((kbits >> 52) & 0x7FF) - 1075;
-      const float khi = __double2float_rn(kd);
-      sh.khi = khi;
-      sh.klo = __double2float_rn(__dsub_rn(kd, (double)khi));
+      const AllocScale ks = alloc_scale(sv);  // sv >= 2^40: the max has weight 2^40
+      sh.mk = ks.mk;
+      sh.ek = ks.ek;
+      sh.khi = ks.khi;
+      sh.klo = ks.klo;
       sh.status = (fl & 1u) ? DSPARK_ST_NONFINITE : DSPARK_ST_OK;
     }
   }
@@ -596,19 +601,22 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThr, 3)
         atomicAdd(&sh.hist[counted ? fs.b : kBins + (tid & 15)], 1u);
       }
       gmask |= any_open ? (1u << it) : 0u;
-      reinterpret_cast<uint4*>(slu)[g] = make_uint4(w[0], w[1], w[2], w[3]);
+      // a group with an open element keeps its four weights for the refinement
+      reinterpret_cast<uint4*>(slu)[g] =
+          any_open ? make_uint4(__float_as_uint(ee[0]), __float_as_uint(ee[1]),
+                                __float_as_uint(ee[2]), __float_as_uint(ee[3]))
+                   : make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
-  // the open elements (about 1 in 2000): E again from the logit, the exact split
+  // the flagged groups: the certified elements get their word (counted above),
+  // the open ones (about 1 in 2000) the exact split
   for (uint32_t m2 = gmask; m2 != 0u; m2 &= m2 - 1u) {
     const int g = tid + kThr * (__ffs(m2) - 1);
     for (int i = 0; i < 4; ++i) {
       const int s = 4 * g + i;
-      if (s < off || s >= off + n) continue;
-      const float x = load_logit(xrow, p.dtype, (int64_t)(lo - off + s));
-      const float Ef = weight40(__fsub_rn(scale ? __fmul_rn(x, invT) : x, m));
+      const float Ef = __uint_as_float(slu[s]);
       const FloatSplit fs = float_split(Ef, khi, klo);
-      if (!(fs.cert || fs.zero)) slu[s] = exact_word(Ef, mk, ek, sh, s, &F, &internal);
+      slu[s] = (fs.cert || fs.zero) ? fs.word : exact_word(Ef, mk, ek, sh, s, &F, &internal);
     }
   }
   F = warp_reduce(F, OpAddU32());
@@ -628,9 +636,9 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThr, 3)
   if (warp == 0) {
     const uint32_t f2 = warp0_combine(sh.wred32, 0u, OpAddU32());
     const uint32_t i2 = warp0_combine(sh.wred32b, 0u, OpOrU32());
-    if (lane == 0) {
-      sh.pub.F = f2;
-      sh.pub.flags3 = i2 ? 2u : 0u;
+    if (lane < kCl) {
+      *cluster.map_shared_rank(&sh.push.F[rank], lane) = f2;
+      *cluster.map_shared_rank(&sh.push.fl3[rank], lane) = i2 ? 2u : 0u;
     }
   }
   cluster.sync();  // S3
@@ -644,8 +652,8 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThr, 3)
   if (warp == 2) {
     uint32_t fa = 0, fl = 0;
     if (lane < kCl) {
-      fa = *cluster.map_shared_rank(&sh.pub.F, lane);
-      fl = *cluster.map_shared_rank(&sh.pub.flags3, lane);
+      fa = sh.push.F[lane];
+      fl = sh.push.fl3[lane];
     }
     fa = warp_reduce(fa, OpAddU32());
     fl = warp_reduce(fl, OpOrU32());
@@ -799,16 +807,17 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThr, 3)
   for (uint32_t j = tid; j < min(my_cand, (uint32_t)kCandCap); j += kThr)
     sh.cand[j].key = exact_key(sh.cand[j].s);
   __syncthreads();
-  if (tid == 0) {
-    sh.pub.csum = (status == DSPARK_ST_OK) ? sh.wred32[0] : 0u;
-    sh.pub.ncand = my_cand;
+  if (warp == 0 && lane < kCl) {
+    *cluster.map_shared_rank(&sh.push.csum[rank], lane) =
+        (status == DSPARK_ST_OK) ? sh.wred32[0] : 0u;
+    *cluster.map_shared_rank(&sh.push.ncand[rank], lane) = my_cand;
   }
   cluster.sync();  // S4
   if (warp == 0) {
     uint32_t nc = 0, over = 0;
     if (lane < kCl) {
-      const uint32_t cs = *cluster.map_shared_rank(&sh.pub.csum, lane);
-      nc = *cluster.map_shared_rank(&sh.pub.ncand, lane);
+      const uint32_t cs = sh.push.csum[lane];
+      nc = sh.push.ncand[lane];
       sh.peers_csum[lane] = cs;
       sh.peers_ncand[lane] = nc;
       sh.grants[lane] = 0u;

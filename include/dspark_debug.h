@@ -1,8 +1,8 @@
 /*
- * dspark_debug.h -- element-wise entry points of libdspark.so that expose two
- * building blocks of the q path for exhaustive checks against a reference:
- * the deterministic exponential behind the draft weights and the Philox
- * generator behind every draw.  Same conventions as dspark.h (device
+ * dspark_debug.h -- element-wise entry points of libdspark.so that expose
+ * three building blocks of the q path for exhaustive checks against a
+ * reference: the deterministic exponential behind the draft weights, the
+ * allocation scale k, and the Philox generator behind every draw.  Same conventions as dspark.h (device
  * pointers, caller-owned buffers, asynchronous on `stream`, 0 / <0 / >0
  * return codes).
  */
@@ -25,6 +25,18 @@ extern "C" {
  */
 int dspark_debug_exp_weights(const float* d, int64_t n, float* e_out, uint64_t* E_out,
                              void* stream);
+
+/*
+ * For each weight sum S[i] >= 1 (u64): the allocation scale
+ * k = RN64(2^24 / RN64(S)) ("PP1 q transport and scheduling design",
+ * Distribution contract and precision: FP64 floor pass), returned as
+ * mk_out[i] * 2^ek_out[i] with mk in [2^52, 2^53), plus khi_out[i] = RN32(k)
+ * and klo_out[i] = RN32(k - khi) -- the values the dense q kernel computes
+ * with integer arithmetic.  S[i] == 0 gives all-zero outputs.  Any output
+ * may be NULL.
+ */
+int dspark_debug_alloc_scale(const uint64_t* S, int64_t n, uint64_t* mk_out, int32_t* ek_out,
+                             float* khi_out, float* klo_out, void* stream);
 
 /*
  * Philox4x32-10 (Salmon et al., SC'11) of n counters: out[i][0..3] =

@@ -126,3 +126,38 @@ def test_library_exp_weights_bit_exact(oracle, lo, hi, step):
     assert np.array_equal(e.view(np.uint32), ref.view(np.uint32))
     refE = np.floor(ref.astype(np.float64) * 2.0 ** 40).astype(np.uint64)
     assert np.array_equal(E, refE)
+
+
+def test_library_alloc_scale_matches_fp64():
+    """k = RN64(2^24 / RN64(S)), khi = RN32(k), klo = RN32(k - khi) from the
+    kernels' integer arithmetic equal numpy's FP64 / FP32 roundings."""
+    rng = np.random.default_rng(5)
+    S = [rng.integers(1 << 40, 1 << 57, size=20000, dtype=np.uint64)]
+    edges = []
+    for e in range(40, 58):
+        for d in (-3, -2, -1, 0, 1, 2, 3):
+            edges.append((1 << e) + d)
+        edges.append((1 << e) + (1 << max(0, e - 53)))      # a tie at the 53-bit rounding
+        edges.append((1 << e) + 3 * (1 << max(0, e - 54)))
+    S.append(np.array(edges, np.uint64))
+    S.append(np.array([1, 2, 3, 129280 << 40, (1 << 57) - 1], np.uint64))
+    S = np.concatenate(S)
+    St = torch.from_numpy(S.view(np.int64)).cuda()
+    mk = torch.empty_like(St)
+    ek = torch.empty(S.size, dtype=torch.int32, device="cuda")
+    khi = torch.empty(S.size, dtype=torch.float32, device="cuda")
+    klo = torch.empty(S.size, dtype=torch.float32, device="cuda")
+    _call("dspark_debug_alloc_scale", ctypes.c_void_p(St.data_ptr()), S.size,
+          ctypes.c_void_p(mk.data_ptr()), ctypes.c_void_p(ek.data_ptr()),
+          ctypes.c_void_p(khi.data_ptr()), ctypes.c_void_p(klo.data_ptr()), None)
+    torch.cuda.synchronize()
+    kd = np.float64(2.0 ** 24) / S.astype(np.float64)
+    bits = kd.view(np.uint64)
+    ref_mk = (bits & np.uint64((1 << 52) - 1)) | np.uint64(1 << 52)
+    ref_ek = ((bits >> np.uint64(52)) & np.uint64(0x7FF)).astype(np.int64) - 1075
+    ref_khi = kd.astype(np.float32)
+    ref_klo = (kd - ref_khi.astype(np.float64)).astype(np.float32)
+    assert np.array_equal(mk.cpu().numpy().view(np.uint64), ref_mk)
+    assert np.array_equal(ek.cpu().numpy().astype(np.int64), ref_ek)
+    assert np.array_equal(khi.cpu().numpy().view(np.uint32), ref_khi.view(np.uint32))
+    assert np.array_equal(klo.cpu().numpy().view(np.uint32), ref_klo.view(np.uint32))
