@@ -1,9 +1,13 @@
 """Benchmark of the draft-sampling / verification hot path on GB300.
 
-One step = the whole path over one batch: dspark_q_build_sample (the dyadic24
-q from the draft logits and the draft draw from it, one launch), then the
-verification modes of the workload (dspark_verify_greedy and/or
-dspark_verify_ratio).  Default workload:
+One step = the whole path over one batch: the q build with the draft draw
+and the workload's verification modes.  With `--schedule auto` (default) a
+dense-q step runs the one-launch dspark_spec_step where the library's
+automatic choice is that schedule (small batches), and otherwise
+dspark_q_build_sample (q and the draft draw, one launch) followed by
+dspark_verify (every verification mode in one pass, one launch) -- the two
+kernels dspark_spec_step's separate schedule enqueues, called one by one
+here so that each is timed.  Default workload:
 C4 -- B = 256 requests, depth 5, V = 129,280, fp32 draft / bf16 target logits,
 Zipf rows with 10 % grammar masks and 1 % tied-remainder rows, dense q,
 greedy and ratio verification (every step of the path but the top-k support,
@@ -38,8 +42,7 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-CONFIG_NAMES = {"c1": "configs[0]", "c2": "configs[1]", "c3": "configs[2]", "c4": "configs[3]",
-                "c5": "configs[4]"}
+L2_BYTES = 129 * 1024 * 1024
 METRIC = "verify rows/s at V=129280 (B x 6 rows)"
 
 
@@ -54,6 +57,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--schedule", default="auto", choices=["auto", "one", "separate"],
+                    help="dense q: one persistent launch, or q build then one verify pass")
     return ap.parse_args()
 
 
@@ -148,7 +153,7 @@ def profiled_traffic(wl, dom):
                 k, v = line.split(":", 1)
                 vals[k] = v.strip()
         h = hashlib.sha256()
-        for name in ("q_dense.cu", "common.cuh"):
+        for name in ("q_dense.cu", "q_dense.cuh", "common.cuh"):
             with open(os.path.join(ROOT, "draft_sampling_verification_gb300", "csrc", name),
                       "rb") as f:
                 h.update(f.read())
@@ -171,14 +176,13 @@ def algorithmic_bytes(wl, acc_greedy, acc_ratio):
     else:
         q_bytes = R_d * V * 4 * 2 + R_d * 4
         q_row = V * 4
-    out = {"q_build_sample": q_bytes}
-    if acc_greedy is not None:
-        out["verify_greedy"] = int(((acc_greedy + 1) * V * esz_t).sum())
-    if acc_ratio is not None:
-        rows = ((acc_ratio + 1) * V * esz_t).sum()
-        resid = (acc_ratio < wl.depth).sum() * q_row
-        out["verify_ratio"] = int(rows + resid)
-    return out
+    # one verification pass: a request's target rows up to the later of the
+    # modes' deciding rows, and the q row of a ratio rejection (residual)
+    accs = [a for a in (acc_greedy, acc_ratio) if a is not None]
+    acc = np.maximum.reduce(accs) if len(accs) > 1 else accs[0]
+    rows = ((acc.astype(np.int64) + 1) * V * esz_t).sum()
+    resid = (acc_ratio < wl.depth).sum() * q_row if acc_ratio is not None else 0
+    return {"q_build_sample": q_bytes, "verify": int(rows + resid)}
 
 
 def run_ours(args, rank, world, local_rank):
@@ -195,12 +199,16 @@ def run_ours(args, rank, world, local_rank):
     B, depth, V = wl.B, wl.depth, wl.V
     req_np = rank_request_ids(wl.request_ids, rank, B)
 
-    # inputs resident in HBM
+    # inputs resident in HBM; a small step's inputs are rotated over enough
+    # copies (> 3 x L2 in all) that each step reads them from HBM
     xd = torch.from_numpy(wl.draft).to(dev)
     if wl.target_dtype == "f32":
         xt = torch.from_numpy(wl.target).to(dev)
     else:
         xt = torch.from_numpy(wl.target.view(np.int16)).to(dev).view(torch.bfloat16)
+    in_bytes = wl.draft.nbytes + wl.target.nbytes
+    n_copies = max(1, -(-3 * L2_BYTES // in_bytes)) if in_bytes < 3 * L2_BYTES else 1
+    copies = [(xd, xt)] + [(xd.clone(), xt.clone()) for _ in range(n_copies - 1)]
     temps = torch.from_numpy(wl.temperature).to(dev)
     req = torch.from_numpy(req_np.view(np.int32)).to(dev)
     rows_d = B * depth
@@ -220,27 +228,35 @@ def run_ours(args, rank, world, local_rank):
                 torch.empty(B, dtype=torch.int32, device=dev),
                 torch.empty(B, dtype=torch.int32, device=dev)) for m in wl.modes}
     stream = torch.cuda.current_stream(dev)
-    kernels = ["q_build_sample"] + ["verify_" + m for m in wl.modes]
+    if top_k > 0:
+        one_launch = False
+    elif args.schedule == "auto":
+        one_launch = ds.dspark_spec_step_schedule(B, depth) == ds.SCHEDULE_ONE_LAUNCH
+    else:
+        one_launch = args.schedule == "one"
+    work = torch.empty(B + 1, dtype=torch.int32, device=dev)
+    kernels = ["spec_step"] if one_launch else ["q_build_sample", "verify"]
     sst.zero_()
+    g = outs.get("greedy")
+    g = (g[0], g[1], g[3]) if g else None
+    r = outs.get("ratio")
 
     def step(x_d, x_t, marks=None):
         if marks:
             marks[0].record(stream)
+        if one_launch:
+            ds.dspark_spec_step(x_d, x_t, B, depth, temps, wl.seed, req, counts, tok, qst, g, r,
+                                work, stream, ds.SCHEDULE_ONE_LAUNCH)
+            if marks:
+                marks[1].record(stream)
+            return
         ds.dspark_q_build_sample(x_d, B, depth, temps, top_k, wl.seed, req, counts, ids, nnz,
                                  tok, qst, stream)
-        k = 1
         if marks:
-            marks[k].record(stream)
-        for m in wl.modes:
-            a, c, f, s = outs[m]
-            if m == "greedy":
-                ds.dspark_verify_greedy(x_t, B, depth, tok, a, c, s, stream)
-            else:
-                ds.dspark_verify_ratio(x_t, B, depth, tok, counts, ids, nnz, top_k, wl.seed, req,
-                                       a, c, f, s, stream)
-            k += 1
-            if marks:
-                marks[k].record(stream)
+            marks[1].record(stream)
+        ds.dspark_verify(x_t, B, depth, tok, g, r, counts, ids, nnz, top_k, wl.seed, req, stream)
+        if marks:
+            marks[2].record(stream)
 
     def barrier():
         if world > 1:
@@ -254,6 +270,8 @@ def run_ours(args, rank, world, local_rank):
         assert int((outs[m][3] != 0).sum()) == 0, "refused requests in bench"
     acc = {m: outs[m][0].cpu().numpy() for m in wl.modes}
     abytes = algorithmic_bytes(wl, acc.get("greedy"), acc.get("ratio"))
+    if one_launch:
+        abytes = {"spec_step": sum(abytes.values())}
 
     # ---- device-timed region (inputs resident)
     clocks = ClockSampler(local_rank)
@@ -268,7 +286,7 @@ def run_ours(args, rank, world, local_rank):
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for s in range(args.steps):
-        step(xd, xt, marks[s])
+        step(*copies[s % n_copies], marks[s])
     t_end.record(stream)
     torch.cuda.synchronize()
     clock_info = clocks.stop()
@@ -327,7 +345,10 @@ def run_ours(args, rank, world, local_rank):
         ms, e2e_max = float(t[0]), float(t[1])
         if e2e:
             e2e["ms_per_step"] = e2e_max
-    return wl, ms, per_kernel, abytes, clock_info, e2e
+    l2 = ("inputs larger than L2 (%.2f GB per step)" % (in_bytes / 1e9) if n_copies == 1 else
+          "inputs rotated over %d copies (%.2f GB in all, > 3 x L2)" % (
+              n_copies, n_copies * in_bytes / 1e9))
+    return wl, ms, per_kernel, abytes, clock_info, e2e, l2
 
 
 # ------------------------------------------------------------ CPU oracle
@@ -387,7 +408,7 @@ def run_reference(args, rank, world):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": secs * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64+u64", "data": "synthetic (seeded generators)",
-        "config": {"workload": "%s (%s)" % (wl.name, CONFIG_NAMES.get(args.workload[:2], "")),
+        "config": {"workload": wl.name, "B_per_gpu": wl.B, "depth": wl.depth, "V": wl.V,
                    "sample_per_step": "%d of %d requests" % (per_step, wl.B)},
         "cpu_baseline": {"value": value, "unit": "verify rows/s", "cores": 1, "kind": "oracle",
                          "sample": "%d requests per step of %s" % (per_step, wl.name)},
@@ -408,7 +429,7 @@ def main():
     import torch
     if world > 1:
         torch.distributed.init_process_group("nccl")
-    wl, ms, per_kernel, abytes, clocks, e2e = run_ours(args, rank, world, local_rank)
+    wl, ms, per_kernel, abytes, clocks, e2e, l2 = run_ours(args, rank, world, local_rank)
     if rank == 0:
         peaks = load_peaks()
         rows = wl.B * (wl.depth + 1) * world
@@ -423,12 +444,11 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32+u64", "data": "synthetic (seeded generators)",
             "config": {
-                "workload": "%s (%s)" % (wl.name, CONFIG_NAMES.get(args.workload[:2], "")),
+                "workload": wl.name,
                 "B_per_gpu": wl.B, "depth": wl.depth, "V": wl.V, "q": "top-%d" % wl.top_k
                 if wl.top_k else "dense", "verify": list(wl.modes),
                 "parallelism": "dp%d (independent requests)" % world,
-                "l2": "inputs larger than L2 (%.2f GB per step)" % (
-                    (wl.draft.nbytes + wl.target.nbytes) / 1e9),
+                "l2": l2,
                 "draft_positions_per_s": wl.B * wl.depth * world / (ms * 1e-3),
                 "step_algorithmic_bytes": step_bytes,
                 "step_achieved_gbs": step_bytes / (ms * 1e-3) / 1e9,

@@ -22,10 +22,13 @@ F32, BF16 = 0, 1
 ST_OK, ST_NONFINITE, ST_ZERO_MASS, ST_ALLOC_INCONSISTENT = 0, 1, 2, 3
 ST_BAD_TEMPERATURE, ST_BAD_Q, ST_BAD_DRAFT, ST_TIMEOUT, ST_INTERNAL = 4, 5, 6, 7, 8
 FLAG_AMBIG_ACCEPT, FLAG_NEAR_BOUNDARY, FLAG_DEGENERATE = 1, 2, 4
+SCHEDULE_AUTO, SCHEDULE_ONE_LAUNCH, SCHEDULE_SEPARATE = 0, 1, 2
 
 __all__ = ["dspark_q_build", "dspark_q_build_sample", "dspark_draft_sample", "dspark_verify_greedy",
-           "dspark_verify_ratio", "dspark_target_probs", "q_build", "draft_sample",
-           "verify_greedy", "verify_ratio", "target_probs", "q_build_sample", "version"]
+           "dspark_verify_ratio", "dspark_verify", "dspark_target_probs", "dspark_spec_step",
+           "dspark_spec_step_schedule", "q_build",
+           "draft_sample", "verify_greedy", "verify_ratio", "target_probs", "q_build_sample",
+           "spec_step", "version"]
 
 
 def version() -> str:
@@ -133,10 +136,59 @@ def dspark_verify_ratio(target_logits, B, depth, draft_tokens, counts, sparse_id
           _i32(committed), _i32(flags), _i32(req_status), _stream(stream))
 
 
+def dspark_verify(target_logits, B, depth, draft_tokens, greedy_out=None, ratio_out=None,
+                  counts=None, sparse_ids=None, nnz=None, top_k=0, seed=0, request_ids=None,
+                  stream=None):
+    """Both verification modes in one pass.  greedy_out = (accept_len,
+    committed, status) or None; ratio_out = (accept_len, committed, flags,
+    status) or None, with counts / sparse_ids / nnz / top_k / seed /
+    request_ids as in dspark_verify_ratio."""
+    rows, V, ld = _rows(target_logits)
+    if rows != B * (depth + 1):
+        raise ValueError("target_logits must hold B*(depth+1) rows")
+    g = greedy_out or (None, None, None)
+    r = ratio_out or (None, None, None, None)
+    _call("dspark_verify", _ptr(target_logits), _dtype_code(target_logits), ld, int(B),
+          int(depth), V, _i32(draft_tokens), _i32(counts), _i32(sparse_ids), _i32(nnz),
+          int(top_k), int(seed) & (2 ** 64 - 1), _i32(request_ids), _i32(g[0]), _i32(g[1]),
+          _i32(g[2]), _i32(r[0]), _i32(r[1]), _i32(r[2]), _i32(r[3]), _stream(stream))
+
+
+def dspark_spec_step_schedule(B, depth):
+    """The schedule dspark_spec_step takes with SCHEDULE_AUTO (host only)."""
+    rc = _lib.load().dspark_spec_step_schedule(int(B), int(depth))
+    if rc < 0:
+        raise ValueError("dspark_spec_step_schedule: error %d" % rc)
+    return rc
+
+
 def dspark_target_probs(target_logits, p_out, argmax, row_status, stream=None):
     rows, V, ld = _rows(target_logits)
     _call("dspark_target_probs", _ptr(target_logits), _dtype_code(target_logits), ld, rows, V,
           _ptr(p_out), _i32(argmax), _i32(row_status), _stream(stream))
+
+
+def dspark_spec_step(draft_logits, target_logits, B, depth, temperature, seed, request_ids, counts,
+                     draft_tokens, row_status, greedy_out=None, ratio_out=None, workspace=None,
+                     stream=None, schedule=0):
+    """greedy_out = (accept_len, committed, status) or None; ratio_out =
+    (accept_len, committed, flags, status) or None; workspace: >= B + 1 int32
+    (allocated here when None); schedule: SCHEDULE_AUTO, SCHEDULE_ONE_LAUNCH
+    or SCHEDULE_SEPARATE."""
+    rd, V, ld_d = _rows(draft_logits)
+    rt, Vt, ld_t = _rows(target_logits)
+    if rd != B * depth or rt != B * (depth + 1) or Vt != V:
+        raise ValueError("draft_logits must hold B*depth rows and target_logits B*(depth+1) rows "
+                         "of the same V")
+    g = greedy_out or (None, None, None)
+    r = ratio_out or (None, None, None, None)
+    if workspace is None:
+        workspace = _empty((B + 1,), torch.int32, draft_logits.device)
+    _call("dspark_spec_step", _ptr(draft_logits), _dtype_code(draft_logits), ld_d,
+          _ptr(target_logits), _dtype_code(target_logits), ld_t, int(B), int(depth), V,
+          _ptr(temperature), int(seed) & (2 ** 64 - 1), _i32(request_ids), _i32(counts),
+          _i32(draft_tokens), _i32(row_status), _i32(g[0]), _i32(g[1]), _i32(g[2]), _i32(r[0]),
+          _i32(r[1]), _i32(r[2]), _i32(r[3]), _i32(workspace), int(schedule), _stream(stream))
 
 
 # --------------------------------------------------- allocating helpers
@@ -177,6 +229,29 @@ def q_build_sample(draft_logits, B, depth, seed, temperature=None, top_k=0, requ
     dspark_q_build_sample(draft_logits, B, depth, temperature, top_k, seed, request_ids, counts,
                           ids, nnz, tokens, status, stream)
     return {"counts": counts, "ids": ids, "nnz": nnz, "status": status, "top_k": top_k}, tokens
+
+
+def spec_step(draft_logits, target_logits, B, depth, seed, temperature=None, request_ids=None,
+              modes=("greedy", "ratio"), stream=None, schedule=0):
+    """Fused q build + draft draw + verification (dense q).  Returns (q dict,
+    tokens [B, depth], {mode: outputs as verify_greedy / verify_ratio})."""
+    rows, V, _ = _rows(draft_logits)
+    dev = draft_logits.device
+    counts = _empty((rows, V), torch.int32, dev)
+    status = _empty((rows,), torch.int32, dev)
+    tokens = _empty((B, depth), torch.int32, dev)
+    outs = {}
+    if "greedy" in modes:
+        outs["greedy"] = (_empty((B,), torch.int32, dev), _empty((B, depth + 1), torch.int32, dev),
+                          _empty((B,), torch.int32, dev))
+    if "ratio" in modes:
+        outs["ratio"] = (_empty((B,), torch.int32, dev), _empty((B, depth + 1), torch.int32, dev),
+                         _empty((B,), torch.int32, dev), _empty((B,), torch.int32, dev))
+    dspark_spec_step(draft_logits, target_logits, B, depth, temperature, seed, request_ids, counts,
+                     tokens, status, outs.get("greedy"), outs.get("ratio"), stream=stream,
+                     schedule=schedule)
+    q = {"counts": counts, "ids": None, "nnz": None, "status": status, "top_k": 0}
+    return q, tokens, outs
 
 
 def draft_sample(q, B, depth, V, seed, request_ids=None, stream=None):

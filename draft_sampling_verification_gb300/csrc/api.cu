@@ -24,6 +24,20 @@ cudaError_t launch_verify(int mode, const void* z, int dtype, int64_t ld, int B,
                           const int32_t* nnz, int top_k, uint64_t seed,
                           const uint32_t* request_ids, int32_t* accept_len, int32_t* committed,
                           uint32_t* flags, int32_t* status, cudaStream_t stream);
+cudaError_t launch_verify_modes(const void* z, int dtype, int64_t ld, int B, int depth, int V,
+                                const int32_t* drafts, const uint32_t* counts, const int32_t* ids,
+                                const int32_t* nnz, int top_k, uint64_t seed,
+                                const uint32_t* request_ids, int32_t* g_acc, int32_t* g_com,
+                                int32_t* g_st, int32_t* r_acc, int32_t* r_com, uint32_t* r_flags,
+                                int32_t* r_st, cudaStream_t stream);
+int spec_step_schedule(int B, int depth);
+cudaError_t launch_spec_step(const void* xd, int d_dtype, int64_t ld_d, const void* xt,
+                             int t_dtype, int64_t ld_t, int B, int depth, int V,
+                             const float* temperature, uint64_t seed,
+                             const uint32_t* request_ids, uint32_t* counts, int32_t* tokens,
+                             int32_t* row_status, int32_t* g_acc, int32_t* g_com, int32_t* g_st,
+                             int32_t* r_acc, int32_t* r_com, uint32_t* r_flags, int32_t* r_st,
+                             uint32_t* workspace, int schedule, cudaStream_t stream);
 cudaError_t launch_target_probs(const void* z, int dtype, int64_t ld, int n_rows, int V,
                                 float* p_out, int32_t* argmax, int32_t* status,
                                 cudaStream_t stream);
@@ -176,6 +190,84 @@ int dspark_verify_ratio(const void* target_logits, int32_t dtype, int64_t ld, in
                                              draft_tokens, counts, sparse_ids, nnz, top_k, seed,
                                              request_ids, accept_len, committed, flags,
                                              req_status, static_cast<cudaStream_t>(stream)));
+}
+
+int dspark_verify(const void* target_logits, int32_t dtype, int64_t ld, int32_t B, int32_t depth,
+                  int32_t V, const int32_t* draft_tokens, const uint32_t* counts,
+                  const int32_t* sparse_ids, const int32_t* nnz, int32_t top_k, uint64_t seed,
+                  const uint32_t* request_ids, int32_t* greedy_accept_len,
+                  int32_t* greedy_committed, int32_t* greedy_status, int32_t* ratio_accept_len,
+                  int32_t* ratio_committed, uint32_t* ratio_flags, int32_t* ratio_status,
+                  void* stream) {
+  const bool g = greedy_accept_len || greedy_committed || greedy_status;
+  const bool r = ratio_accept_len || ratio_committed || ratio_status;
+  if (!g && !r) return DSPARK_ERR_NULL;
+  if (g && (!greedy_accept_len || !greedy_committed || !greedy_status)) return DSPARK_ERR_NULL;
+  int e = g ? check_verify(target_logits, dtype, ld, B, depth, V, draft_tokens,
+                           greedy_accept_len, greedy_committed, greedy_status)
+            : check_verify(target_logits, dtype, ld, B, depth, V, draft_tokens, ratio_accept_len,
+                           ratio_committed, ratio_status);
+  if (e != 0) return e > 0 ? 0 : e;  // > 0: empty batch
+  if (r) {
+    const int e2 = check_verify(target_logits, dtype, ld, B, depth, V, draft_tokens,
+                                ratio_accept_len, ratio_committed, ratio_status);
+    if (e2 < 0) return e2;
+    if (int e3 = check_topk(top_k, V)) return e3;
+    if (!counts) return DSPARK_ERR_NULL;
+    if (top_k > 0 && (!sparse_ids || !nnz)) return DSPARK_ERR_NULL;
+    if (!aligned(counts, 4) || (ratio_flags && !aligned(ratio_flags, 4)) ||
+        (request_ids && !aligned(request_ids, 4)) || (sparse_ids && !aligned(sparse_ids, 4)) ||
+        (nnz && !aligned(nnz, 4)))
+      return DSPARK_ERR_ALIGN;
+  }
+  return launch_result(dspark::launch_verify_modes(
+      target_logits, dtype, ld, B, depth, V, draft_tokens, r ? counts : nullptr,
+      r ? sparse_ids : nullptr, r ? nnz : nullptr, r ? top_k : 0, seed, request_ids,
+      g ? greedy_accept_len : nullptr, greedy_committed, greedy_status,
+      r ? ratio_accept_len : nullptr, ratio_committed, ratio_flags, ratio_status,
+      static_cast<cudaStream_t>(stream)));
+}
+
+int dspark_spec_step_schedule(int32_t B, int32_t depth) {
+  if (B < 0 || depth < 1 || depth > DSPARK_MAX_DEPTH) return DSPARK_ERR_SIZE;
+  return dspark::spec_step_schedule(B, depth);
+}
+
+int dspark_spec_step(const void* draft_logits, int32_t draft_dtype, int64_t ld_draft,
+                     const void* target_logits, int32_t target_dtype, int64_t ld_target,
+                     int32_t B, int32_t depth, int32_t V, const float* temperature, uint64_t seed,
+                     const uint32_t* request_ids, uint32_t* counts, int32_t* draft_tokens,
+                     int32_t* row_status, int32_t* greedy_accept_len, int32_t* greedy_committed,
+                     int32_t* greedy_status, int32_t* ratio_accept_len, int32_t* ratio_committed,
+                     uint32_t* ratio_flags, int32_t* ratio_status, uint32_t* workspace,
+                     int32_t schedule, void* stream) {
+  if (int e = check_common(draft_dtype, V, ld_draft)) return e;
+  if (int e = check_common(target_dtype, V, ld_target)) return e;
+  if (depth < 1 || depth > DSPARK_MAX_DEPTH) return DSPARK_ERR_SIZE;
+  if (B < 0 || (int64_t)B * depth > kMaxGridRows) return DSPARK_ERR_SIZE;
+  if (schedule < DSPARK_SCHEDULE_AUTO || schedule > DSPARK_SCHEDULE_SEPARATE)
+    return DSPARK_ERR_ARG;
+  if (B == 0) return 0;
+  const bool g = greedy_accept_len || greedy_committed || greedy_status;
+  const bool r = ratio_accept_len || ratio_committed || ratio_status;
+  if (!draft_logits || !target_logits || !counts || !draft_tokens || !row_status || !workspace)
+    return DSPARK_ERR_NULL;
+  if (!g && !r) return DSPARK_ERR_NULL;
+  if (g && (!greedy_accept_len || !greedy_committed || !greedy_status)) return DSPARK_ERR_NULL;
+  if (r && (!ratio_accept_len || !ratio_committed || !ratio_status)) return DSPARK_ERR_NULL;
+  const void* four[] = {counts, draft_tokens, row_status, greedy_accept_len, greedy_committed,
+                        greedy_status, ratio_accept_len, ratio_committed, ratio_flags,
+                        ratio_status, temperature, request_ids, workspace};
+  for (const void* q : four)
+    if (q && !aligned(q, 4)) return DSPARK_ERR_ALIGN;
+  if (!aligned(draft_logits, esize(draft_dtype)) || !aligned(target_logits, esize(target_dtype)))
+    return DSPARK_ERR_ALIGN;
+  return launch_result(dspark::launch_spec_step(
+      draft_logits, draft_dtype, ld_draft, target_logits, target_dtype, ld_target, B, depth, V,
+      temperature, seed, request_ids, counts, draft_tokens, row_status,
+      g ? greedy_accept_len : nullptr, greedy_committed, greedy_status,
+      r ? ratio_accept_len : nullptr, ratio_committed, ratio_flags, ratio_status, workspace,
+      schedule, static_cast<cudaStream_t>(stream)));
 }
 
 int dspark_target_probs(const void* target_logits, int32_t dtype, int64_t ld, int32_t n_rows,

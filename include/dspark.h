@@ -77,6 +77,7 @@ extern "C" {
 #define DSPARK_ERR_TOPK (-4)         /* top_k < 0, > V or > DSPARK_MAX_TOPK  */
 #define DSPARK_ERR_ALIGN (-5)        /* pointer not aligned to its element   */
 #define DSPARK_ERR_DEVICE (-6)       /* no usable sm_103 device current      */
+#define DSPARK_ERR_ARG (-7)          /* an enumerated argument out of range  */
 
 /* device statuses (per draft row, or per request) */
 #define DSPARK_ST_OK 0
@@ -149,8 +150,9 @@ int dspark_q_build_sample(const void* draft_logits, int32_t dtype, int64_t ld, i
 /*
  * dspark_draft_sample -- one token per draft row from its q
  * ("PP1 q transport and scheduling design", Distribution contract and
- * precision: "a uniform 24-bit integer and exact integer cumulative counts
- * (first cumulative count strictly greater than the draw)").
+ * precision: the draw is a uniform 24-bit integer compared with exact integer
+ * cumulative counts; the token is the first whose cumulative count exceeds
+ * it).
  *
  * Row r = b*depth + j (request b, position j): D = Philox(seed; request id,
  * j, PROPOSAL) word 0 >> 8; token = the first id, in ascending order, whose
@@ -220,6 +222,74 @@ int dspark_verify_ratio(const void* target_logits, int32_t dtype, int64_t ld, in
                         int32_t top_k, uint64_t seed, const uint32_t* request_ids,
                         int32_t* accept_len, int32_t* committed, uint32_t* flags,
                         int32_t* req_status, void* stream);
+
+/*
+ * dspark_verify -- greedy and/or ratio verification in one pass over the
+ * target rows: each output set is exactly that of dspark_verify_greedy /
+ * dspark_verify_ratio with the same arguments (same pages and rules).  A
+ * request's rows are read until both requested modes have decided.
+ * Greedy outputs: greedy_accept_len[B], greedy_committed[B][depth+1],
+ * greedy_status[B] -- all three or none; ratio outputs: ratio_accept_len[B],
+ * ratio_committed[B][depth+1], ratio_status[B] (all three or none),
+ * ratio_flags[B] (may be NULL), with counts / sparse_ids / nnz / top_k /
+ * seed / request_ids as in dspark_verify_ratio (ignored without ratio
+ * outputs).  At least one mode must be given (DSPARK_ERR_NULL otherwise).
+ */
+int dspark_verify(const void* target_logits, int32_t dtype, int64_t ld, int32_t B, int32_t depth,
+                  int32_t V, const int32_t* draft_tokens, const uint32_t* counts,
+                  const int32_t* sparse_ids, const int32_t* nnz, int32_t top_k, uint64_t seed,
+                  const uint32_t* request_ids, int32_t* greedy_accept_len,
+                  int32_t* greedy_committed, int32_t* greedy_status, int32_t* ratio_accept_len,
+                  int32_t* ratio_committed, uint32_t* ratio_flags, int32_t* ratio_status,
+                  void* stream);
+
+/*
+ * dspark_spec_step -- the whole speculative step in one call, dense q only:
+ * dspark_q_build_sample (top_k = 0) of the B*depth draft rows, then
+ * dspark_verify_greedy and/or dspark_verify_ratio of the B*(depth+1) target
+ * rows with the drafts and q just built ("PP1 q transport and scheduling
+ * design", Distribution contract and precision; "DeepSeek-V4.1 DSpark",
+ * State and sampling contracts).  Every output is exactly that of the
+ * separate calls in sequence on the same stream with the same arguments,
+ * whichever schedule runs; both modes share one read of each target row.
+ *
+ * draft_logits / draft_dtype / ld_draft and target_logits / target_dtype /
+ * ld_target as in those calls (either dtype for either side).  q outputs:
+ * counts[B*depth][V], draft_tokens[B][depth], row_status[B*depth] (all
+ * required).  Greedy outputs: greedy_accept_len[B], greedy_committed[B][depth+1],
+ * greedy_status[B] -- all three or none; ratio outputs: ratio_accept_len[B],
+ * ratio_committed[B][depth+1], ratio_status[B] (all three or none) and
+ * ratio_flags[B] (may be NULL).  At least one mode must be given
+ * (DSPARK_ERR_NULL otherwise).  Same limits as the separate calls.
+ * workspace: B + 1 words of device memory owned by the caller (required);
+ * the one-launch schedule zeroes it on `stream` and keeps the work counter
+ * and the finished-row count of each request there, so calls that may
+ * overlap need separate workspaces.
+ * schedule: DSPARK_SCHEDULE_SEPARATE enqueues dspark_q_build_sample's kernel
+ * and dspark_verify's;
+ * DSPARK_SCHEDULE_ONE_LAUNCH runs one persistent kernel whose clusters take
+ * q rows and verifications from a shared counter, a request's verification
+ * waiting (at most 2 s, else DSPARK_ST_TIMEOUT for that request) until its
+ * rows are finished; DSPARK_SCHEDULE_AUTO takes the one launch when B >= 2
+ * and the B*(depth+1) work items fit in one wave of resident clusters, the
+ * two kernels otherwise.  Any other value: DSPARK_ERR_ARG.
+ */
+#define DSPARK_SCHEDULE_AUTO 0
+#define DSPARK_SCHEDULE_ONE_LAUNCH 1
+#define DSPARK_SCHEDULE_SEPARATE 2
+/* The schedule dspark_spec_step takes for DSPARK_SCHEDULE_AUTO with this
+ * B and depth (host only, nothing launched); DSPARK_ERR_SIZE for B < 0 or
+ * depth outside [1, DSPARK_MAX_DEPTH]. */
+int dspark_spec_step_schedule(int32_t B, int32_t depth);
+
+int dspark_spec_step(const void* draft_logits, int32_t draft_dtype, int64_t ld_draft,
+                     const void* target_logits, int32_t target_dtype, int64_t ld_target,
+                     int32_t B, int32_t depth, int32_t V, const float* temperature, uint64_t seed,
+                     const uint32_t* request_ids, uint32_t* counts, int32_t* draft_tokens,
+                     int32_t* row_status, int32_t* greedy_accept_len, int32_t* greedy_committed,
+                     int32_t* greedy_status, int32_t* ratio_accept_len, int32_t* ratio_committed,
+                     uint32_t* ratio_flags, int32_t* ratio_status, uint32_t* workspace,
+                     int32_t schedule, void* stream);
 
 /*
  * dspark_target_probs -- the target distribution p of n_rows logit rows at

@@ -62,3 +62,29 @@ def test_sample_and_verify_argument_errors(lib):
     assert lib.dspark_target_probs(P, 0, 8, 1, 0, None, None, P, None) == -2
     assert lib.dspark_debug_philox(P, 0, -1, P, None) == -2
     assert lib.dspark_debug_exp_weights(None, 4, None, None, None) == -1
+
+
+def test_spec_step_argument_errors(lib):
+    f = lib.dspark_spec_step
+    f.argtypes = _lib.SIGNATURES["dspark_spec_step"]
+    # draft, dt, ld, target, dt, ld, B, depth, V, temps, seed, req, counts, tok, rst,
+    # g_acc, g_com, g_st, r_acc, r_com, r_fl, r_st, workspace, schedule, stream
+    ok = [P, 0, 8, P, 1, 8, 1, 5, 8, None, 0, None, P, P, P, P, P, P, P, P, None, P, P, 0, None]
+
+    def call(**kw):
+        a = list(ok)
+        names = {"V": 8, "depth": 7, "B": 6, "workspace": 22, "schedule": 23, "g_com": 16,
+                 "r_acc": 18, "ld_t": 5}
+        for k, v in kw.items():
+            a[names[k]] = v
+        return f(*a)
+
+    assert call(V=0) == -2
+    assert call(depth=0) == -2
+    assert call(depth=9) == -2
+    assert call(ld_t=4) == -2
+    assert call(schedule=3) == -7
+    assert call(schedule=-1) == -7
+    assert call(workspace=None) == -1
+    assert call(g_com=None) == -1          # greedy outputs: all three or none
+    assert call(B=0) == 0                  # empty batch: nothing enqueued
