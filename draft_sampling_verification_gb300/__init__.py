@@ -26,7 +26,7 @@ SCHEDULE_AUTO, SCHEDULE_ONE_LAUNCH, SCHEDULE_SEPARATE = 0, 1, 2
 
 __all__ = ["dspark_q_build", "dspark_q_build_sample", "dspark_draft_sample", "dspark_verify_greedy",
            "dspark_verify_ratio", "dspark_verify", "dspark_target_probs", "dspark_spec_step",
-           "dspark_spec_step_schedule", "q_build",
+           "dspark_spec_step_schedule", "dspark_spec_step_noalloc", "q_build",
            "draft_sample", "verify_greedy", "verify_ratio", "target_probs", "q_build_sample",
            "spec_step", "version"]
 
@@ -152,6 +152,25 @@ def dspark_verify(target_logits, B, depth, draft_tokens, greedy_out=None, ratio_
           int(depth), V, _i32(draft_tokens), _i32(counts), _i32(sparse_ids), _i32(nnz),
           int(top_k), int(seed) & (2 ** 64 - 1), _i32(request_ids), _i32(g[0]), _i32(g[1]),
           _i32(g[2]), _i32(r[0]), _i32(r[1]), _i32(r[2]), _i32(r[3]), _stream(stream))
+
+
+def dspark_spec_step_noalloc(draft_logits, target_logits, B, depth, temperature, seed,
+                             request_ids, counts, draft_tokens, row_status, greedy_out=None,
+                             ratio_out=None, stream=None, schedule=0):
+    """dspark_spec_step with the library's own device scratch array instead
+    of a workspace (calls on one device must not overlap)."""
+    rd, V, ld_d = _rows(draft_logits)
+    rt, Vt, ld_t = _rows(target_logits)
+    if rd != B * depth or rt != B * (depth + 1) or Vt != V:
+        raise ValueError("draft_logits must hold B*depth rows and target_logits B*(depth+1) rows "
+                         "of the same V")
+    g = greedy_out or (None, None, None)
+    r = ratio_out or (None, None, None, None)
+    _call("dspark_spec_step_noalloc", _ptr(draft_logits), _dtype_code(draft_logits), ld_d,
+          _ptr(target_logits), _dtype_code(target_logits), ld_t, int(B), int(depth), V,
+          _ptr(temperature), int(seed) & (2 ** 64 - 1), _i32(request_ids), _i32(counts),
+          _i32(draft_tokens), _i32(row_status), _i32(g[0]), _i32(g[1]), _i32(g[2]), _i32(r[0]),
+          _i32(r[1]), _i32(r[2]), _i32(r[3]), int(schedule), _stream(stream))
 
 
 def dspark_spec_step_schedule(B, depth):

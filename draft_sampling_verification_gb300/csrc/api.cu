@@ -31,6 +31,7 @@ cudaError_t launch_verify_modes(const void* z, int dtype, int64_t ld, int B, int
                                 int32_t* g_st, int32_t* r_acc, int32_t* r_com, uint32_t* r_flags,
                                 int32_t* r_st, cudaStream_t stream);
 int spec_step_schedule(int B, int depth);
+uint32_t* static_spec_workspace();
 cudaError_t launch_spec_step(const void* xd, int d_dtype, int64_t ld_d, const void* xt,
                              int t_dtype, int64_t ld_t, int B, int depth, int V,
                              const float* temperature, uint64_t seed,
@@ -233,14 +234,15 @@ int dspark_spec_step_schedule(int32_t B, int32_t depth) {
   return dspark::spec_step_schedule(B, depth);
 }
 
-int dspark_spec_step(const void* draft_logits, int32_t draft_dtype, int64_t ld_draft,
-                     const void* target_logits, int32_t target_dtype, int64_t ld_target,
-                     int32_t B, int32_t depth, int32_t V, const float* temperature, uint64_t seed,
-                     const uint32_t* request_ids, uint32_t* counts, int32_t* draft_tokens,
-                     int32_t* row_status, int32_t* greedy_accept_len, int32_t* greedy_committed,
-                     int32_t* greedy_status, int32_t* ratio_accept_len, int32_t* ratio_committed,
-                     uint32_t* ratio_flags, int32_t* ratio_status, uint32_t* workspace,
-                     int32_t schedule, void* stream) {
+static int spec_step_impl(const void* draft_logits, int32_t draft_dtype, int64_t ld_draft,
+                          const void* target_logits, int32_t target_dtype, int64_t ld_target,
+                          int32_t B, int32_t depth, int32_t V, const float* temperature,
+                          uint64_t seed, const uint32_t* request_ids, uint32_t* counts,
+                          int32_t* draft_tokens, int32_t* row_status, int32_t* greedy_accept_len,
+                          int32_t* greedy_committed, int32_t* greedy_status,
+                          int32_t* ratio_accept_len, int32_t* ratio_committed,
+                          uint32_t* ratio_flags, int32_t* ratio_status, uint32_t* workspace,
+                          bool static_workspace, int32_t schedule, void* stream) {
   if (int e = check_common(draft_dtype, V, ld_draft)) return e;
   if (int e = check_common(target_dtype, V, ld_target)) return e;
   if (depth < 1 || depth > DSPARK_MAX_DEPTH) return DSPARK_ERR_SIZE;
@@ -250,8 +252,9 @@ int dspark_spec_step(const void* draft_logits, int32_t draft_dtype, int64_t ld_d
   if (B == 0) return 0;
   const bool g = greedy_accept_len || greedy_committed || greedy_status;
   const bool r = ratio_accept_len || ratio_committed || ratio_status;
-  if (!draft_logits || !target_logits || !counts || !draft_tokens || !row_status || !workspace)
+  if (!draft_logits || !target_logits || !counts || !draft_tokens || !row_status)
     return DSPARK_ERR_NULL;
+  if (!workspace && !static_workspace) return DSPARK_ERR_NULL;
   if (!g && !r) return DSPARK_ERR_NULL;
   if (g && (!greedy_accept_len || !greedy_committed || !greedy_status)) return DSPARK_ERR_NULL;
   if (r && (!ratio_accept_len || !ratio_committed || !ratio_status)) return DSPARK_ERR_NULL;
@@ -262,12 +265,47 @@ int dspark_spec_step(const void* draft_logits, int32_t draft_dtype, int64_t ld_d
     if (q && !aligned(q, 4)) return DSPARK_ERR_ALIGN;
   if (!aligned(draft_logits, esize(draft_dtype)) || !aligned(target_logits, esize(target_dtype)))
     return DSPARK_ERR_ALIGN;
+  if (static_workspace) {
+    if (B > DSPARK_SPEC_STATIC_MAX_B) return DSPARK_ERR_SIZE;
+    if ((workspace = dspark::static_spec_workspace()) == nullptr) return DSPARK_ERR_DEVICE;
+  }
   return launch_result(dspark::launch_spec_step(
       draft_logits, draft_dtype, ld_draft, target_logits, target_dtype, ld_target, B, depth, V,
       temperature, seed, request_ids, counts, draft_tokens, row_status,
       g ? greedy_accept_len : nullptr, greedy_committed, greedy_status,
       r ? ratio_accept_len : nullptr, ratio_committed, ratio_flags, ratio_status, workspace,
       schedule, static_cast<cudaStream_t>(stream)));
+}
+
+int dspark_spec_step(const void* draft_logits, int32_t draft_dtype, int64_t ld_draft,
+                     const void* target_logits, int32_t target_dtype, int64_t ld_target,
+                     int32_t B, int32_t depth, int32_t V, const float* temperature, uint64_t seed,
+                     const uint32_t* request_ids, uint32_t* counts, int32_t* draft_tokens,
+                     int32_t* row_status, int32_t* greedy_accept_len, int32_t* greedy_committed,
+                     int32_t* greedy_status, int32_t* ratio_accept_len, int32_t* ratio_committed,
+                     uint32_t* ratio_flags, int32_t* ratio_status, uint32_t* workspace,
+                     int32_t schedule, void* stream) {
+  return spec_step_impl(draft_logits, draft_dtype, ld_draft, target_logits, target_dtype,
+                        ld_target, B, depth, V, temperature, seed, request_ids, counts,
+                        draft_tokens, row_status, greedy_accept_len, greedy_committed,
+                        greedy_status, ratio_accept_len, ratio_committed, ratio_flags,
+                        ratio_status, workspace, false, schedule, stream);
+}
+
+int dspark_spec_step_noalloc(const void* draft_logits, int32_t draft_dtype, int64_t ld_draft,
+                             const void* target_logits, int32_t target_dtype, int64_t ld_target,
+                             int32_t B, int32_t depth, int32_t V, const float* temperature,
+                             uint64_t seed, const uint32_t* request_ids, uint32_t* counts,
+                             int32_t* draft_tokens, int32_t* row_status,
+                             int32_t* greedy_accept_len, int32_t* greedy_committed,
+                             int32_t* greedy_status, int32_t* ratio_accept_len,
+                             int32_t* ratio_committed, uint32_t* ratio_flags,
+                             int32_t* ratio_status, int32_t schedule, void* stream) {
+  return spec_step_impl(draft_logits, draft_dtype, ld_draft, target_logits, target_dtype,
+                        ld_target, B, depth, V, temperature, seed, request_ids, counts,
+                        draft_tokens, row_status, greedy_accept_len, greedy_committed,
+                        greedy_status, ratio_accept_len, ratio_committed, ratio_flags,
+                        ratio_status, nullptr, true, schedule, stream);
 }
 
 int dspark_target_probs(const void* target_logits, int32_t dtype, int64_t ld, int32_t n_rows,

@@ -18,6 +18,8 @@
 //               finished row increments the request's counter in the
 //               workspace; the verifying cluster waits on it with a bounded
 //               wait).  It pays off only while all items fit in one wave.
+#include <mutex>
+
 #include "q_dense.cuh"
 #include "verify.cuh"
 
@@ -282,6 +284,39 @@ cudaError_t launch_spec_step(const void* xd, int d_dtype, int64_t ld_d, const vo
   if (e != cudaSuccess) return e;
   kern<<<ncl * qdense::kCl, qdense::kThr, smem, stream>>>(qp, vp, wp);
   return cudaGetLastError();
+}
+
+// ---- the no-allocation variant's scratch
+//
+// A file-scope device array stands in for the caller's workspace: one copy
+// per device (each device's module has its own), its address looked up once
+// per device with cudaGetSymbolAddress and cached.  Every call on a device
+// uses the same array, so calls that may overlap (other streams, other host
+// threads) race on it.  The one-launch schedule zeroes the words it uses on
+// the stream before its kernel, as with a caller's workspace.
+constexpr int kMaxDevices = 64;
+static __device__ __align__(256) uint32_t g_spec_workspace[DSPARK_SPEC_STATIC_MAX_B + 1];
+
+// The calling thread's current device's copy of the array; nullptr if the
+// device or the lookup fails.
+uint32_t* static_spec_workspace() {
+  static std::mutex mu;
+  static uint32_t* addr[kMaxDevices] = {};
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_spec_workspace) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    addr[dev] = static_cast<uint32_t*>(p);
+  }
+  return addr[dev];
 }
 
 }  // namespace dspark

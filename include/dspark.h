@@ -292,6 +292,40 @@ int dspark_spec_step(const void* draft_logits, int32_t draft_dtype, int64_t ld_d
                      int32_t schedule, void* stream);
 
 /*
+ * dspark_spec_step_noalloc -- dspark_spec_step without the caller's
+ * workspace.  The pages have no counterpart: this is a deployment
+ * convenience for callers that cannot hand over device memory (for instance
+ * while building a CUDA graph around the step).
+ *
+ * Arguments, outputs and statuses are those of dspark_spec_step, which this
+ * call makes with a scratch array of DSPARK_SPEC_STATIC_MAX_B + 1 words
+ * that the library holds as a file-scope __device__ variable (one copy per
+ * device); nothing is allocated, by this call or any library it calls.
+ * - B > DSPARK_SPEC_STATIC_MAX_B: DSPARK_ERR_SIZE, nothing enqueued.
+ * - The array's address is looked up with cudaGetSymbolAddress on the first
+ *   call on each device and cached; make that first call (any B >= 1)
+ *   before capturing a stream into a graph, so that the capture sees no
+ *   lookup.  A failed lookup returns DSPARK_ERR_DEVICE.
+ * - Every call on a device shares the one array: two calls that may run at
+ *   the same time (different streams, host threads or graphs in flight)
+ *   race on it and their outputs are undefined.  Order them on one stream,
+ *   or use dspark_spec_step with separate workspaces.
+ * - What must start at zero (the work counter and the per-request row
+ *   counters) is zeroed on `stream` by the one-launch schedule before its
+ *   kernel, so a call needs nothing from the one before it.
+ */
+#define DSPARK_SPEC_STATIC_MAX_B 65535
+int dspark_spec_step_noalloc(const void* draft_logits, int32_t draft_dtype, int64_t ld_draft,
+                             const void* target_logits, int32_t target_dtype, int64_t ld_target,
+                             int32_t B, int32_t depth, int32_t V, const float* temperature,
+                             uint64_t seed, const uint32_t* request_ids, uint32_t* counts,
+                             int32_t* draft_tokens, int32_t* row_status,
+                             int32_t* greedy_accept_len, int32_t* greedy_committed,
+                             int32_t* greedy_status, int32_t* ratio_accept_len,
+                             int32_t* ratio_committed, uint32_t* ratio_flags,
+                             int32_t* ratio_status, int32_t schedule, void* stream);
+
+/*
  * dspark_target_probs -- the target distribution p of n_rows logit rows at
  * T = 1 ("PP1 q transport and scheduling design": the full target p after
  * the unchanged target processors, T = 1, top_p = 1), with the argmax

@@ -88,3 +88,20 @@ def test_spec_step_argument_errors(lib):
     assert call(workspace=None) == -1
     assert call(g_com=None) == -1          # greedy outputs: all three or none
     assert call(B=0) == 0                  # empty batch: nothing enqueued
+
+
+def test_spec_step_noalloc_host_checks(lib):
+    """The no-allocation entry refuses a batch beyond its scratch array, and
+    bad arguments, on the host (before any device lookup)."""
+    f = lib.dspark_spec_step_noalloc
+    # same arguments as dspark_spec_step minus the workspace
+    a = [P, 0, 8, P, 1, 8, 1, 5, 8, None, 0, None, P, P, P, P, P, P, P, P, None, P, 0, None]
+    big = list(a)
+    big[6] = 65536                      # B > DSPARK_SPEC_STATIC_MAX_B
+    assert f(*big) == -2
+    bad = list(a)
+    bad[22] = 5                         # schedule
+    assert f(*bad) == -7
+    empty = list(a)
+    empty[6] = 0
+    assert f(*empty) == 0
