@@ -7,10 +7,10 @@
 #include "dspark.h"
 
 namespace dspark {
-cudaError_t launch_q_build(const void* x, int dtype, int64_t ld, int n_rows, int V,
-                           const float* temperature, int top_k, uint32_t* counts, int32_t* ids,
-                           int32_t* nnz, int32_t* status, int32_t* tokens, uint64_t seed,
-                           const uint32_t* request_ids, int depth, cudaStream_t stream);
+cudaError_t launch_q_topk(const void* x, int dtype, int64_t ld, int n_rows, int V,
+                          const float* temperature, int top_k, uint32_t* counts, int32_t* ids,
+                          int32_t* nnz, int32_t* status, int32_t* tokens, uint64_t seed,
+                          const uint32_t* request_ids, int depth, cudaStream_t stream);
 cudaError_t launch_q_dense(const void* x, int dtype, int64_t ld, int n_rows, int V,
                            const float* temperature, uint32_t* counts, int32_t* status,
                            int32_t* tokens, uint64_t seed, const uint32_t* request_ids, int depth,
@@ -89,9 +89,9 @@ int dspark_q_build(const void* draft_logits, int32_t dtype, int64_t ld, int32_t 
     return launch_result(dspark::launch_q_dense(draft_logits, dtype, ld, n_rows, V, temperature,
                                                 counts, row_status, nullptr, 0ull, nullptr, 1,
                                                 static_cast<cudaStream_t>(stream)));
-  return launch_result(dspark::launch_q_build(draft_logits, dtype, ld, n_rows, V, temperature,
-                                              top_k, counts, sparse_ids, nnz, row_status, nullptr,
-                                              0ull, nullptr, 1, static_cast<cudaStream_t>(stream)));
+  return launch_result(dspark::launch_q_topk(draft_logits, dtype, ld, n_rows, V, temperature,
+                                             top_k, counts, sparse_ids, nnz, row_status, nullptr,
+                                             0ull, nullptr, 1, static_cast<cudaStream_t>(stream)));
 }
 
 int dspark_q_build_sample(const void* draft_logits, int32_t dtype, int64_t ld, int32_t B,
@@ -116,10 +116,10 @@ int dspark_q_build_sample(const void* draft_logits, int32_t dtype, int64_t ld, i
                                                 counts, row_status, draft_tokens, seed,
                                                 request_ids, depth,
                                                 static_cast<cudaStream_t>(stream)));
-  return launch_result(dspark::launch_q_build(draft_logits, dtype, ld, B * depth, V, temperature,
-                                              top_k, counts, sparse_ids, nnz, row_status,
-                                              draft_tokens, seed, request_ids, depth,
-                                              static_cast<cudaStream_t>(stream)));
+  return launch_result(dspark::launch_q_topk(draft_logits, dtype, ld, B * depth, V, temperature,
+                                             top_k, counts, sparse_ids, nnz, row_status,
+                                             draft_tokens, seed, request_ids, depth,
+                                             static_cast<cudaStream_t>(stream)));
 }
 
 int dspark_draft_sample(const uint32_t* counts, const int32_t* sparse_ids, const int32_t* nnz,

@@ -76,6 +76,35 @@ def test_q_build_strided_unaligned(oracle, ld_pad, offset, dtype):
     compare_q(qs, oracle.q_build(xr, None, 64))
 
 
+@pytest.mark.parametrize("top_k", [1, 256, 1024])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_q_topk_stream_orders(oracle, top_k, dtype):
+    """Top-k rows whose order defeats the streaming filter (ascending: every
+    element is a candidate, so the buffer is cut back many times) or makes it
+    trivial (descending), with exact ties straddling every cut, at the full
+    vocabulary and the largest k."""
+    rng = np.random.default_rng(top_k)
+    V = 129280
+    asc = np.sort(rng.normal(0, 3, V)).astype(np.float32)
+    tied = np.round(asc * 2) / 2                     # long runs of equal values
+    x = np.stack([asc, asc[::-1], tied, tied[::-1],
+                  np.repeat(np.arange(V // 640, dtype=np.float32), 640)[:V]])
+    q, view = run_q(x, [1.0, 1.0, 0.7, 1.3, 1.0], top_k, dtype=dtype)
+    xr = view.float().cpu().numpy()
+    compare_q(q, oracle.q_build(xr, [1.0, 1.0, 0.7, 1.3, 1.0], top_k))
+
+
+def test_q_topk_batch_invariance():
+    rng = np.random.default_rng(19)
+    V = 129280
+    x = rows_for(V, rng, n_each=1)
+    full, _ = run_q(x, None, 256)
+    for r in (0, 2, x.shape[0] - 1):
+        alone, _ = run_q(x[r:r + 1], None, 256)
+        for key in ("counts", "ids", "nnz", "status"):
+            assert torch.equal(alone[key][0], full[key][r]), key
+
+
 def test_q_build_uniform_full_vocab_closed_form():
     V = 129280
     q, _ = run_q(np.zeros((3, V), np.float32), [1.0, 0.5, 2.0], 0)
