@@ -139,27 +139,39 @@ def max_over_ranks(values):
 
 
 # ------------------------------------------------------------ our arm
+# ncu summaries under profiles/: the kernel they cover, the sources it is
+# built from, and the unit its traffic is given per
+PROFILES = {
+    ("q_build_sample", "dense"): ("q_dense_c4_b64.md", ("q_dense.cu", "q_dense.cuh", "common.cuh"),
+                                  "traffic_bytes_per_row"),
+    ("q_build_sample", "topk"): ("q_topk_c3_b64.md", ("q_topk.cu", "common.cuh"),
+                                 "traffic_bytes_per_row"),
+}
+
+
 def profiled_traffic(wl, dom):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
     summary (per draft row, scaled by the rows of one launch), or None when
     there is none for it or its sources changed since the counters were taken."""
-    if dom != "q_build_sample" or wl.top_k != 0:
+    entry = PROFILES.get((dom, "topk" if wl.top_k else "dense"))
+    if entry is None:
         return None
+    fname, sources, unit = entry
     try:
-        text = open(os.path.join(ROOT, "profiles", "q_dense_c4_b64.md")).read()
+        text = open(os.path.join(ROOT, "profiles", fname)).read()
         vals = {}
         for line in text.splitlines():
-            if line.startswith(("traffic_bytes_per_row:", "sources_sha256_16:")):
+            if line.startswith((unit + ":", "sources_sha256_16:")):
                 k, v = line.split(":", 1)
                 vals[k] = v.strip()
         h = hashlib.sha256()
-        for name in ("q_dense.cu", "q_dense.cuh", "common.cuh"):
+        for name in sources:
             with open(os.path.join(ROOT, "draft_sampling_verification_gb300", "csrc", name),
                       "rb") as f:
                 h.update(f.read())
         if h.hexdigest()[:16] != vals.get("sources_sha256_16"):
             return None
-        return int(vals["traffic_bytes_per_row"]) * wl.B * wl.depth
+        return int(vals[unit]) * wl.B * wl.depth
     except (OSError, KeyError, ValueError):
         return None
 
