@@ -183,9 +183,19 @@ __device__ RowStat slice_stat(const void* row, int dtype, int lo, int n, VShared
 // draw computes exact 46-bit fixed-point weights of row L once, keeps the
 // mass of every block of 32 groups, and the CTA holding the draw finds its
 // block from those sums and its token with one warp.
+//
+// Cluster size: bf16 rows take 4-CTA clusters (a 64 KB slice per CTA, three
+// CTAs per SM), so twice as many requests walk their row chains at once as
+// with 8-CTA clusters; fp32 rows keep 8 (a 64 KB slice as well).
+template <int kDt>
+constexpr int verify_cluster() {
+  return kDt == DSPARK_BF16 ? 4 : 8;
+}
+
 template <bool kG, bool kR, int kDt>
-__global__ void __cluster_dims__(kVCluster, 1, 1) __launch_bounds__(kVThreads, 3)
+__global__ void __cluster_dims__(verify_cluster<kDt>(), 1, 1) __launch_bounds__(kVThreads, 3)
     verify_kernel(VParams p) {
+  constexpr int NC = verify_cluster<kDt>();
   __shared__ VSh2 sh;
   __shared__ uint64_t mbar[kVTma];
   extern __shared__ __align__(128) unsigned char vbuf[];
@@ -195,7 +205,7 @@ __global__ void __cluster_dims__(kVCluster, 1, 1) __launch_bounds__(kVThreads, 3
   }
   __syncthreads();
   uint32_t phase = 0;
-  verify_request<kG, kR, kDt>(p, blockIdx.x / kVCluster, sh, vbuf, mbar, phase, nullptr, nullptr);
+  verify_request<kG, kR, kDt, NC>(p, blockIdx.x / NC, sh, vbuf, mbar, phase, nullptr, nullptr);
 }
 
 // ------------------------------------------------------------ target p
@@ -245,8 +255,8 @@ __global__ void __cluster_dims__(kVCluster, 1, 1) __launch_bounds__(kVThreads, 2
   }
 }
 
-static int verify_chunk(int V) {
-  int c = (V + kVCluster - 1) / kVCluster;
+static int verify_chunk(int V, int nc) {
+  int c = (V + nc - 1) / nc;
   return (c + 7) & ~7;
 }
 
@@ -277,7 +287,9 @@ cudaError_t launch_verify_modes(const void* z, int dtype, int64_t ld, int B, int
   p.r_committed = r_com;
   p.r_flags = r_flags;
   p.r_status = r_st;
-  p.chunk = verify_chunk(V);
+  const int nc = (dtype == DSPARK_BF16) ? verify_cluster<DSPARK_BF16>()
+                                        : verify_cluster<DSPARK_F32>();
+  p.chunk = verify_chunk(V, nc);
   // the slice buffer: chunk elements plus one 16-byte group of slack
   const int esz = (dtype == DSPARK_F32) ? 4 : 2;
   const int smem = p.chunk * esz + 32;
@@ -287,7 +299,7 @@ cudaError_t launch_verify_modes(const void* z, int dtype, int64_t ld, int B, int
     e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    kern<<<B * kVCluster, kVThreads, smem, stream>>>(p);
+    kern<<<B * nc, kVThreads, smem, stream>>>(p);
     return cudaGetLastError();
   };
   const bool g = g_acc != nullptr, r = r_acc != nullptr;
@@ -327,7 +339,7 @@ cudaError_t launch_target_probs(const void* z, int dtype, int64_t ld, int n_rows
   p.p_out = p_out;
   p.argmax = argmax;
   p.status = status;
-  p.chunk = verify_chunk(V);
+  p.chunk = verify_chunk(V, kVCluster);
   target_probs_kernel<<<n_rows * kVCluster, kVThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }

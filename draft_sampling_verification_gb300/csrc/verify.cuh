@@ -123,7 +123,7 @@ __device__ __forceinline__ void am_merge(float& v, int& i, float v2, int i2) {
 // drafts_sm (shared memory of every CTA) when given, else from p.drafts; the
 // count of draft j in its dense q row from cnt_sm when given, else from
 // p.counts.
-template <bool kG, bool kR, int kDt>
+template <bool kG, bool kR, int kDt, int NC = kVCluster>
 __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh,
                                                unsigned char* vbuf, uint64_t* mbar,
                                                uint32_t& phase, const int32_t* drafts_sm,
@@ -336,7 +336,7 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
       int ai = 0x7FFFFFFF;
       uint32_t fl = 0;
       bool bad = false;
-      for (int r = 0; r < kVCluster; ++r) {
+      for (int r = 0; r < NC; ++r) {
         const VX* e = cluster.map_shared_rank(&sh.x[xi], r);
         const float m2 = e->m;
         fl |= e->fl;
@@ -522,7 +522,7 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
       cluster.sync();
       if (tid == 0) {
         uint64_t before = 0, Z = 0, CS = 0;
-        for (int r = 0; r < kVCluster; ++r) {
+        for (int r = 0; r < NC; ++r) {
           const VX* e = cluster.map_shared_rank(&sh.x[xi], r);
           const uint64_t zr = e->z;
           if (r < rank) before += zr;
