@@ -57,6 +57,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-wire", action="store_true",
+                    help="skip the received-q (pack + validate) measurement")
     ap.add_argument("--schedule", default="auto", choices=["auto", "one", "separate"],
                     help="dense q: one persistent launch, or q build then one verify pass")
     return ap.parse_args()
@@ -351,6 +353,49 @@ def run_ours(args, rank, world, local_rank):
         d2h = h_tok.numel() * 4 + sum(t.numel() * 4 for m in wl.modes for t in h_res[m])
         e2e = {"ms_per_step": e2e_ms, "h2d": h2d, "d2h": d2h}
 
+    # ---- the received-q path on this step's q rows: the sender's pack
+    #      (wire values + checksums), the receiver's validation (values,
+    #      support, mass, the proposed tokens, the checksums); not part of the
+    #      step above
+    wire = None
+    if not args.no_wire:
+        width = counts.shape[1]
+        qf = torch.empty((rows_d, width), dtype=torch.float32, device=dev)
+        cs = torch.empty((rows_d,), dtype=torch.int64, device=dev)
+        rec = torch.empty((rows_d, width), dtype=torch.int32, device=dev)
+        wst = torch.empty((rows_d,), dtype=torch.int32, device=dev)
+        toks = tok.reshape(-1)
+
+        def wire_step(ev=None):
+            if ev:
+                ev[0].record(stream)
+            ds.dspark_q_pack(counts, ids, nnz, top_k, V, qf, cs, stream)
+            if ev:
+                ev[1].record(stream)
+            ds.dspark_q_validate(qf, ids, nnz, top_k, V, toks, cs, rec, wst, stream)
+            if ev:
+                ev[2].record(stream)
+
+        for _ in range(max(3, args.warmup)):
+            wire_step()
+        torch.cuda.synchronize()
+        assert int((wst != 0).sum()) == 0 and torch.equal(rec, counts), "wire round trip"
+        wev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+        for s_ in range(args.steps):
+            wire_step(wev[s_])
+        torch.cuda.synchronize()
+        pack_ms = sum(e[0].elapsed_time(e[1]) for e in wev) / args.steps
+        val_ms = sum(e[1].elapsed_time(e[2]) for e in wev) / args.steps
+        entries = rows_d * width
+        # pack: counts (and ids) read, q written, checksums written;
+        # validate: q (and ids) read, counts written, tokens, checksums and
+        # statuses
+        per = 4 * entries + (4 * entries if top_k else 0)
+        pack_b = per + 4 * entries + 8 * rows_d
+        val_b = per + 4 * entries + 16 * rows_d
+        wire = {"pack_ms": pack_ms, "validate_ms": val_ms, "pack_bytes": pack_b,
+                "validate_bytes": val_b}
+
     ms = elapsed_ms / args.steps
     if world > 1:
         t = max_over_ranks(torch.tensor([ms, e2e["ms_per_step"] if e2e else 0.0], device=dev))
@@ -360,7 +405,7 @@ def run_ours(args, rank, world, local_rank):
     l2 = ("inputs larger than L2 (%.2f GB per step)" % (in_bytes / 1e9) if n_copies == 1 else
           "inputs rotated over %d copies (%.2f GB in all, > 3 x L2)" % (
               n_copies, n_copies * in_bytes / 1e9))
-    return wl, ms, per_kernel, abytes, clock_info, e2e, l2
+    return wl, ms, per_kernel, abytes, clock_info, e2e, l2, wire
 
 
 # ------------------------------------------------------------ CPU oracle
@@ -441,7 +486,7 @@ def main():
     import torch
     if world > 1:
         torch.distributed.init_process_group("nccl")
-    wl, ms, per_kernel, abytes, clocks, e2e, l2 = run_ours(args, rank, world, local_rank)
+    wl, ms, per_kernel, abytes, clocks, e2e, l2, wire = run_ours(args, rank, world, local_rank)
     if rank == 0:
         peaks = load_peaks()
         rows = wl.B * (wl.depth + 1) * world
@@ -478,6 +523,18 @@ def main():
             line["e2e"] = {"value": rows / (e2e["ms_per_step"] * 1e-3), "unit": "verify rows/s",
                            "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                            "ms_per_step": e2e["ms_per_step"]}
+        if wire:
+            gbs_p = wire["pack_bytes"] / (wire["pack_ms"] * 1e-3) / 1e9
+            gbs_v = wire["validate_bytes"] / (wire["validate_ms"] * 1e-3) / 1e9
+            line["received_q"] = {
+                "what": "q_pack + q_validate on this step's q rows, timed apart from the step",
+                "pack_ms": round(wire["pack_ms"], 4), "validate_ms": round(wire["validate_ms"], 4),
+                "pack_algorithmic_bytes": wire["pack_bytes"],
+                "validate_algorithmic_bytes": wire["validate_bytes"],
+                "roofline": {"bound": "hbm", "unit": "GB/s", "peak": peak,
+                             "pack_achieved": gbs_p, "pack_frac": gbs_p / peak,
+                             "validate_achieved": gbs_v, "validate_frac": gbs_v / peak},
+            }
         if not args.no_cpu:
             line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
         print(json.dumps(line))

@@ -21,12 +21,14 @@ M = 1 << 24
 F32, BF16 = 0, 1
 ST_OK, ST_NONFINITE, ST_ZERO_MASS, ST_ALLOC_INCONSISTENT = 0, 1, 2, 3
 ST_BAD_TEMPERATURE, ST_BAD_Q, ST_BAD_DRAFT, ST_TIMEOUT, ST_INTERNAL = 4, 5, 6, 7, 8
+ST_BAD_CHECKSUM = 9
 FLAG_AMBIG_ACCEPT, FLAG_NEAR_BOUNDARY, FLAG_DEGENERATE = 1, 2, 4
 SCHEDULE_AUTO, SCHEDULE_ONE_LAUNCH, SCHEDULE_SEPARATE = 0, 1, 2
 
 __all__ = ["dspark_q_build", "dspark_q_build_sample", "dspark_draft_sample", "dspark_verify_greedy",
            "dspark_verify_ratio", "dspark_verify", "dspark_target_probs", "dspark_spec_step",
-           "dspark_spec_step_schedule", "dspark_spec_step_noalloc", "q_build",
+           "dspark_spec_step_schedule", "dspark_spec_step_noalloc", "dspark_q_pack",
+           "dspark_q_validate", "q_build",
            "draft_sample", "verify_greedy", "verify_ratio", "target_probs", "q_build_sample",
            "spec_step", "version"]
 
@@ -181,6 +183,23 @@ def dspark_spec_step_schedule(B, depth):
     return rc
 
 
+def dspark_q_pack(counts, sparse_ids, nnz, top_k, V, q_out, checksum_out, stream=None):
+    """counts [n_rows, V] (dense) or [n_rows, top_k] with sparse_ids / nnz;
+    q_out float32 of the same shape; checksum_out int64 [n_rows] (holding the
+    uint64 checksums)."""
+    _call("dspark_q_pack", _i32(counts), _i32(sparse_ids), _i32(nnz), int(top_k),
+          counts.shape[0], int(V), _ptr(q_out), _ptr(checksum_out), _stream(stream))
+
+
+def dspark_q_validate(q, sparse_ids, nnz, top_k, V, tokens, expect, counts_out, row_status,
+                      stream=None):
+    """q float32 [n_rows, width]; tokens int32 [n_rows] or None; expect int64
+    [n_rows] or None; counts_out int32 [n_rows, width] or None."""
+    n_rows = q.shape[0]
+    _call("dspark_q_validate", _ptr(q), _i32(sparse_ids), _i32(nnz), int(top_k), n_rows, int(V),
+          _i32(tokens), _ptr(expect), _i32(counts_out), _i32(row_status), _stream(stream))
+
+
 def dspark_target_probs(target_logits, p_out, argmax, row_status, stream=None):
     rows, V, ld = _rows(target_logits)
     _call("dspark_target_probs", _ptr(target_logits), _dtype_code(target_logits), ld, rows, V,
@@ -271,6 +290,25 @@ def spec_step(draft_logits, target_logits, B, depth, seed, temperature=None, req
                      schedule=schedule)
     q = {"counts": counts, "ids": None, "nnz": None, "status": status, "top_k": 0}
     return q, tokens, outs
+
+
+def q_pack(q, V, stream=None):
+    """Wire form of a q dict from q_build: (q float32 of the counts' shape,
+    checksums int64 [n_rows] holding the uint64 bit patterns)."""
+    counts = q["counts"]
+    qf = _empty(counts.shape, torch.float32, counts.device)
+    cs = _empty((counts.shape[0],), torch.int64, counts.device)
+    dspark_q_pack(counts, q["ids"], q["nnz"], q["top_k"], V, qf, cs, stream)
+    return qf, cs
+
+
+def q_validate(qf, V, ids=None, nnz=None, top_k=0, tokens=None, expect=None, stream=None):
+    """Validation of received q rows: (status int32 [n_rows], recovered counts
+    int32 of qf's shape)."""
+    counts = _empty(qf.shape, torch.int32, qf.device)
+    st = _empty((qf.shape[0],), torch.int32, qf.device)
+    dspark_q_validate(qf, ids, nnz, top_k, V, tokens, expect, counts, st, stream)
+    return st, counts
 
 
 def draft_sample(q, B, depth, V, seed, request_ids=None, stream=None):

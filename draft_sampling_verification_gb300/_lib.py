@@ -30,6 +30,8 @@ SIGNATURES = {
     "dspark_verify": [_P, _I32, _I64, _I32, _I32, _I32, _P, _P, _P, _P, _I32, _U64, _P, _P, _P,
                       _P, _P, _P, _P, _P, _P],
     "dspark_spec_step_schedule": [_I32, _I32],
+    "dspark_q_pack": [_P, _P, _P, _I32, _I32, _I32, _P, _P, _P],
+    "dspark_q_validate": [_P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _P, _P],
     "dspark_spec_step_noalloc": [_P, _I32, _I64, _P, _I32, _I64, _I32, _I32, _I32, _P, _U64, _P,
                                  _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I32, _P],
     "dspark_spec_step": [_P, _I32, _I64, _P, _I32, _I64, _I32, _I32, _I32, _P, _U64, _P, _P, _P,

@@ -31,6 +31,12 @@ cudaError_t launch_verify_modes(const void* z, int dtype, int64_t ld, int B, int
                                 int32_t* g_st, int32_t* r_acc, int32_t* r_com, uint32_t* r_flags,
                                 int32_t* r_st, cudaStream_t stream);
 int spec_step_schedule(int B, int depth);
+cudaError_t launch_q_pack(const uint32_t* counts, const int32_t* ids, const int32_t* nnz,
+                          int top_k, int n_rows, int V, float* q, uint64_t* checksum,
+                          cudaStream_t stream);
+cudaError_t launch_q_validate(const float* q, const int32_t* ids, const int32_t* nnz, int top_k,
+                              int n_rows, int V, const int32_t* tokens, const uint64_t* expect,
+                              uint32_t* counts, int32_t* status, cudaStream_t stream);
 uint32_t* static_spec_workspace();
 cudaError_t launch_spec_step(const void* xd, int d_dtype, int64_t ld_d, const void* xt,
                              int t_dtype, int64_t ld_t, int B, int depth, int V,
@@ -306,6 +312,42 @@ int dspark_spec_step_noalloc(const void* draft_logits, int32_t draft_dtype, int6
                         draft_tokens, row_status, greedy_accept_len, greedy_committed,
                         greedy_status, ratio_accept_len, ratio_committed, ratio_flags,
                         ratio_status, nullptr, true, schedule, stream);
+}
+
+int dspark_q_pack(const uint32_t* counts, const int32_t* sparse_ids, const int32_t* nnz,
+                  int32_t top_k, int32_t n_rows, int32_t V, float* q_out,
+                  uint64_t* checksum_out, void* stream) {
+  if (V < 1 || V > DSPARK_MAX_V) return DSPARK_ERR_SIZE;
+  if (int e = check_topk(top_k, V)) return e;
+  if (n_rows < 0 || n_rows > kMaxGridRows) return DSPARK_ERR_SIZE;
+  if (n_rows == 0) return 0;
+  if (!counts || !q_out || !checksum_out) return DSPARK_ERR_NULL;
+  if (top_k > 0 && (!sparse_ids || !nnz)) return DSPARK_ERR_NULL;
+  if (!aligned(counts, 4) || !aligned(q_out, 4) || !aligned(checksum_out, 8) ||
+      (sparse_ids && !aligned(sparse_ids, 4)) || (nnz && !aligned(nnz, 4)))
+    return DSPARK_ERR_ALIGN;
+  return launch_result(dspark::launch_q_pack(counts, top_k > 0 ? sparse_ids : nullptr,
+                                             top_k > 0 ? nnz : nullptr, top_k, n_rows, V, q_out,
+                                             checksum_out, static_cast<cudaStream_t>(stream)));
+}
+
+int dspark_q_validate(const float* q, const int32_t* sparse_ids, const int32_t* nnz,
+                      int32_t top_k, int32_t n_rows, int32_t V, const int32_t* tokens,
+                      const uint64_t* expect, uint32_t* counts_out, int32_t* row_status,
+                      void* stream) {
+  if (V < 1 || V > DSPARK_MAX_V) return DSPARK_ERR_SIZE;
+  if (int e = check_topk(top_k, V)) return e;
+  if (n_rows < 0 || n_rows > kMaxGridRows) return DSPARK_ERR_SIZE;
+  if (n_rows == 0) return 0;
+  if (!q || !row_status) return DSPARK_ERR_NULL;
+  if (top_k > 0 && (!sparse_ids || !nnz)) return DSPARK_ERR_NULL;
+  if (!aligned(q, 4) || !aligned(row_status, 4) || (counts_out && !aligned(counts_out, 4)) ||
+      (tokens && !aligned(tokens, 4)) || (expect && !aligned(expect, 8)) ||
+      (sparse_ids && !aligned(sparse_ids, 4)) || (nnz && !aligned(nnz, 4)))
+    return DSPARK_ERR_ALIGN;
+  return launch_result(dspark::launch_q_validate(
+      q, top_k > 0 ? sparse_ids : nullptr, top_k > 0 ? nnz : nullptr, top_k, n_rows, V, tokens,
+      expect, counts_out, row_status, static_cast<cudaStream_t>(stream)));
 }
 
 int dspark_target_probs(const void* target_logits, int32_t dtype, int64_t ld, int32_t n_rows,

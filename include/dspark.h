@@ -89,6 +89,7 @@ extern "C" {
 #define DSPARK_ST_BAD_DRAFT 6        /* draft id out of range or q(x) == 0   */
 #define DSPARK_ST_TIMEOUT 7          /* a bounded wait inside a kernel expired */
 #define DSPARK_ST_INTERNAL 8         /* an internal capacity was exceeded    */
+#define DSPARK_ST_BAD_CHECKSUM 9     /* a received q row's checksum differs  */
 
 /* verification flags (per request, ratio verification) */
 #define DSPARK_FLAG_AMBIG_ACCEPT 1u  /* |u*q - p| <= 1e-6 * q at a tested row */
@@ -336,6 +337,50 @@ int dspark_spec_step_noalloc(const void* draft_logits, int32_t draft_dtype, int6
 int dspark_target_probs(const void* target_logits, int32_t dtype, int64_t ld, int32_t n_rows,
                         int32_t V, float* p_out, int32_t* argmax, int32_t* row_status,
                         void* stream);
+
+/*
+ * dspark_q_pack -- the wire form of q rows ("PP1 q transport and scheduling
+ * design", Distribution contract and precision: q is sent as little-endian
+ * FP32 q(v) = c_v / M, every such value exact; Versioned v2 message design:
+ * the per-position reply carries the q values, the sparse ids and a
+ * checksum).
+ *
+ * Dense (top_k == 0): counts[n_rows][V] -> q_out[n_rows][V].  Sparse
+ * (top_k > 0): counts[n_rows][top_k] with sparse_ids / nnz as built by
+ * dspark_q_build -> q_out[n_rows][top_k] (q = 0 past nnz; the ids are sent
+ * as they are).  checksum_out[n_rows]: Fletcher-64 of the row's payload
+ * words -- a dense row's V FP32 bit patterns in id order, a sparse row's nnz
+ * int32 ids followed by their nnz FP32 bit patterns -- with A = sum w_i and
+ * B = sum (n - i) w_i modulo 2^32 - 1, checksum = B << 32 | A.  (The pages
+ * ask for a checksum but name none: this is one with published test
+ * vectors.)
+ */
+int dspark_q_pack(const uint32_t* counts, const int32_t* sparse_ids, const int32_t* nnz,
+                  int32_t top_k, int32_t n_rows, int32_t V, float* q_out,
+                  uint64_t* checksum_out, void* stream);
+
+/*
+ * dspark_q_validate -- validation of received q rows before they are used
+ * (same sections: the receiver recovers c = q * M, requires an integer,
+ * checks the mass in uint64, and refuses the listed malformations).
+ *
+ * q[n_rows][width] FP32 (width = V dense, top_k sparse), with
+ * sparse_ids[n_rows][top_k] and nnz[n_rows] for sparse rows.  tokens[n_rows]
+ * (may be NULL): the token proposed from each row, which must have q > 0.
+ * expect[n_rows] (may be NULL): the checksums the rows must have.
+ * counts_out[n_rows][width] (may be NULL): the recovered counts, all zero
+ * for a refused row.  row_status[n_rows], first failing check in this order:
+ *   BAD_Q        sparse nnz outside [1, top_k] (the payload's size);
+ *   BAD_CHECKSUM the row's checksum differs from expect;
+ *   BAD_Q        a value not finite, negative, above 1 or not a multiple of
+ *                2^-24; the counts not summing to M; sparse ids not strictly
+ *                ascending in [0, V) (duplicates, padding) or a listed zero;
+ *   BAD_DRAFT    the proposed token outside [0, V) or with q = 0.
+ */
+int dspark_q_validate(const float* q, const int32_t* sparse_ids, const int32_t* nnz,
+                      int32_t top_k, int32_t n_rows, int32_t V, const int32_t* tokens,
+                      const uint64_t* expect, uint32_t* counts_out, int32_t* row_status,
+                      void* stream);
 
 /* Library build identifier (static string, host). */
 const char* dspark_version(void);

@@ -658,3 +658,115 @@ done:
     free(scratch);
     return st;
 }
+
+/* =========================================================================
+ * Received q: wire form, byte checksum and validation ("PP1 q transport and
+ * scheduling design", Distribution contract and precision: q sent as
+ * little-endian FP32 q = c / M, counts recovered by multiplying by M and
+ * required to be integers, the mass checked in uint64; Versioned v2 message
+ * design: per-position reply with q values, sparse ids and a checksum, and
+ * the list of refusals).
+ *
+ * Readings (the pages fix no checksum algorithm and no sparse byte order):
+ *   - payload words: dense row = the V FP32 bit patterns in id order;
+ *     sparse row = the nnz int32 ids, then their nnz FP32 bit patterns;
+ *   - byte checksum = Fletcher-64 of the payload words (A and B summed modulo
+ *     2^32 - 1 from zero, checksum = B << 32 | A);
+ *   - validation order: a sparse entry count outside [1, top_k] (BAD_Q: the
+ *     payload's size), then the checksum (if one is given), then the row's
+ *     values and support (BAD_Q), then the proposed token (BAD_DRAFT; a
+ *     negative token is one outside [0, V)).
+ * ========================================================================= */
+#define OR_BAD_CHECKSUM 9
+
+uint64_t oracle_fletcher64(const uint32_t* words, int64_t n)
+{
+    const uint64_t mod = 0xFFFFFFFFull;
+    uint64_t a = 0, b = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        a = (a + words[i]) % mod;
+        b = (b + a) % mod;
+    }
+    return (b << 32) | a;
+}
+
+static uint32_t or_f32_bits(float v) { uint32_t u; memcpy(&u, &v, 4); return u; }
+
+/* Wire form of one q row.  Dense (top_k == 0): q[v] = counts[v] / M for the
+ * V ids.  Sparse: q[i] = counts[i] / M for the nnz entries, and q = 0 past
+ * them.  Returns the checksum of the row's payload. */
+uint64_t oracle_q_pack_row(const uint32_t* counts, const int32_t* ids, int32_t nnz,
+                           int32_t top_k, int32_t V, float* q)
+{
+    int64_t n = top_k > 0 ? nnz : V;
+    if (n < 0) n = 0;
+    for (int64_t i = 0; i < n; ++i) q[i] = (float)((double)counts[i] / (double)OR_M);
+    if (top_k > 0)
+        for (int64_t i = n; i < top_k; ++i) q[i] = 0.0f;
+    uint32_t* words = (uint32_t*)malloc(sizeof(uint32_t) * (size_t)(2 * n + 1));
+    if (!words) return 0;
+    int64_t w = 0;
+    if (top_k > 0)
+        for (int64_t i = 0; i < n; ++i) words[w++] = (uint32_t)ids[i];
+    for (int64_t i = 0; i < n; ++i) words[w++] = or_f32_bits(q[i]);
+    uint64_t cs = oracle_fletcher64(words, w);
+    free(words);
+    return cs;
+}
+
+/* Validation of one received q row.  counts_out (may be NULL) gets the
+ * recovered counts (dense [V] or sparse [top_k], zeros past nnz and on a
+ * refusal).  token: the proposed token, checked when has_token.  expect: the
+ * checksum the row must have, checked when has_expect. */
+int oracle_q_validate_row(const float* q, const int32_t* ids, int32_t nnz, int32_t top_k,
+                          int32_t V, int has_token, int32_t token, int has_expect,
+                          uint64_t expect, uint32_t* counts_out)
+{
+    int64_t cap = top_k > 0 ? top_k : V;
+    if (counts_out) memset(counts_out, 0, sizeof(uint32_t) * (size_t)cap);
+    if (top_k > 0 && (nnz < 1 || nnz > top_k)) return OR_BAD_Q;
+    int64_t n = top_k > 0 ? nnz : V;
+    if (has_expect) {
+        uint32_t* words = (uint32_t*)malloc(sizeof(uint32_t) * (size_t)(2 * n + 1));
+        if (!words) return -1;
+        int64_t w = 0;
+        if (top_k > 0)
+            for (int64_t i = 0; i < n; ++i) words[w++] = (uint32_t)ids[i];
+        for (int64_t i = 0; i < n; ++i) words[w++] = or_f32_bits(q[i]);
+        uint64_t cs = oracle_fletcher64(words, w);
+        free(words);
+        if (cs != expect) return OR_BAD_CHECKSUM;
+    }
+    /* values: finite, not negative, dyadic (q * M an integer, at most M) */
+    uint32_t* c = (uint32_t*)calloc((size_t)cap, sizeof(uint32_t));
+    if (!c) return -1;
+    uint64_t total = 0;
+    int st = OR_OK;
+    for (int64_t i = 0; i < n && st == OR_OK; ++i) {
+        double v = (double)q[i];
+        if (!isfinite(v) || v < 0.0) { st = OR_BAD_Q; break; }
+        double cm = v * (double)OR_M;
+        if (cm != floor(cm) || cm > (double)OR_M) { st = OR_BAD_Q; break; }
+        c[i] = (uint32_t)cm;
+        total += c[i];
+        if (top_k > 0) {
+            /* canonical support: ids strictly ascending in [0, V), no zero
+             * entries listed */
+            if (ids[i] < 0 || ids[i] >= V || c[i] == 0) st = OR_BAD_Q;
+            if (i > 0 && ids[i - 1] >= ids[i]) st = OR_BAD_Q;
+        }
+    }
+    if (st == OR_OK && total != (uint64_t)OR_M) st = OR_BAD_Q;
+    if (st == OR_OK && has_token) {
+        if (token < 0 || token >= V) st = OR_BAD_DRAFT;
+        else if (top_k == 0) { if (c[token] == 0) st = OR_BAD_DRAFT; }
+        else {
+            int found = 0;
+            for (int64_t i = 0; i < n; ++i) if (ids[i] == token) found = 1;
+            if (!found) st = OR_BAD_DRAFT;
+        }
+    }
+    if (st == OR_OK && counts_out) memcpy(counts_out, c, sizeof(uint32_t) * (size_t)cap);
+    free(c);
+    return st;
+}

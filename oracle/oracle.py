@@ -25,6 +25,7 @@ _lib = None
 
 M = 1 << 24
 OK, NONFINITE, ZERO_MASS, ALLOC_INCONSISTENT, BAD_TEMPERATURE, BAD_Q, BAD_DRAFT = range(7)
+BAD_CHECKSUM = 9
 FLAG_AMBIG_ACCEPT, FLAG_NEAR_BOUNDARY, FLAG_DEGENERATE = 1, 2, 4
 PURPOSE_PROPOSAL, PURPOSE_ACCEPT, PURPOSE_RESIDUAL, PURPOSE_BONUS = 0, 1, 2, 3
 
@@ -71,6 +72,10 @@ def lib():
                 "oracle_verify_greedy_req": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, _P, _P]),
                 "oracle_verify_ratio_req": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, _P, _P, _P,
                                                            _I32, _U64, _U32, _P, _P, _P]),
+                "oracle_fletcher64": (_U64, [_P, _I64]),
+                "oracle_q_pack_row": (_U64, [_P, _P, _I32, _I32, _I32, _P]),
+                "oracle_q_validate_row": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, ctypes.c_int,
+                                                         _I32, ctypes.c_int, _U64, _P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -272,3 +277,49 @@ def verify_ratio(z, drafts, counts, ids, nnz, top_k, seed, request_ids=None):
         com[b] = cm
         flags[b] = fl.value
     return acc, com, flags, status
+
+
+# ------------------------------------------------------------ received q (wire)
+def fletcher64(words) -> int:
+    """Fletcher-64 of 32-bit words (A, B modulo 2^32 - 1; B << 32 | A)."""
+    w = _c(words, np.uint32)
+    return int(lib().oracle_fletcher64(_ptr(w), w.size))
+
+
+def q_pack(counts, ids=None, nnz=None, top_k=0):
+    """counts [n_rows, V] (dense) or [n_rows, top_k] with ids / nnz (sparse).
+    Returns (q fp32 of the same shape, checksum uint64 [n_rows])."""
+    counts = _c(counts, np.uint32)
+    n_rows = counts.shape[0]
+    q = np.zeros(counts.shape, np.float32)
+    cs = np.zeros(n_rows, np.uint64)
+    V = counts.shape[1]
+    for r in range(n_rows):
+        ir = None if ids is None else _c(ids[r], np.int32)
+        nz = 0 if nnz is None else int(nnz[r])
+        qr = np.zeros(V, np.float32)
+        cs[r] = lib().oracle_q_pack_row(_ptr(counts[r]), _ptr(ir), nz, top_k, V, _ptr(qr))
+        q[r] = qr
+    return q, cs
+
+
+def q_validate(q, ids=None, nnz=None, top_k=0, V=None, tokens=None, expect=None):
+    """Validation of received q rows.  Returns (status int32 [n_rows],
+    recovered counts uint32 of q's shape)."""
+    q = _c(q, np.float32)
+    n_rows, width = q.shape
+    V = width if V is None else V
+    st = np.zeros(n_rows, np.int32)
+    counts = np.zeros(q.shape, np.uint32)
+    for r in range(n_rows):
+        ir = None if ids is None else _c(ids[r], np.int32)
+        nz = 0 if nnz is None else int(nnz[r])
+        has_tok = tokens is not None
+        tok = int(tokens[r]) if has_tok else 0
+        has = expect is not None
+        ex = int(expect[r]) if has else 0
+        cr = np.zeros(width, np.uint32)
+        st[r] = lib().oracle_q_validate_row(_ptr(q[r]), _ptr(ir), nz, top_k, V, int(has_tok), tok,
+                                            int(has), ex, _ptr(cr))
+        counts[r] = cr
+    return st, counts
