@@ -59,6 +59,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-wire", action="store_true",
                     help="skip the received-q (pack + validate) measurement")
+    ap.add_argument("--no-match", action="store_true",
+                    help="skip the stochastic (match) verification measurement")
     ap.add_argument("--schedule", default="auto", choices=["auto", "one", "separate"],
                     help="dense q: one persistent launch, or q build then one verify pass")
     return ap.parse_args()
@@ -396,6 +398,34 @@ def run_ours(args, rank, world, local_rank):
         wire = {"pack_ms": pack_ms, "validate_ms": val_ms, "pack_bytes": pack_b,
                 "validate_bytes": val_b}
 
+    # ---- stochastic (match) verification of this step's drafts, timed apart
+    #      from the step: per request, the target rows up to the deciding row
+    match = None
+    if not args.no_match:
+        mo = [torch.empty(B, dtype=torch.int32, device=dev),
+              torch.empty((B, depth + 1), dtype=torch.int32, device=dev),
+              torch.empty(B, dtype=torch.int32, device=dev),
+              torch.empty(B, dtype=torch.int32, device=dev)]
+
+        def match_step():
+            ds.dspark_verify_match(xt, B, depth, tok, wl.seed, req, *mo, stream)
+
+        for _ in range(max(3, args.warmup)):
+            match_step()
+        torch.cuda.synchronize()
+        assert int((mo[3] != 0).sum()) == 0, "refused requests in the match verification"
+        esz_t = xt.element_size()
+        rows_read = (mo[0].to(torch.int64) + 1).sum().item()
+        me0 = torch.cuda.Event(enable_timing=True)
+        me1 = torch.cuda.Event(enable_timing=True)
+        me0.record(stream)
+        for _ in range(args.steps):
+            match_step()
+        me1.record(stream)
+        torch.cuda.synchronize()
+        match = {"ms": me0.elapsed_time(me1) / args.steps, "bytes": int(rows_read * V * esz_t),
+                 "mean_accept": float(mo[0].float().mean().item())}
+
     ms = elapsed_ms / args.steps
     if world > 1:
         t = max_over_ranks(torch.tensor([ms, e2e["ms_per_step"] if e2e else 0.0], device=dev))
@@ -405,7 +435,7 @@ def run_ours(args, rank, world, local_rank):
     l2 = ("inputs larger than L2 (%.2f GB per step)" % (in_bytes / 1e9) if n_copies == 1 else
           "inputs rotated over %d copies (%.2f GB in all, > 3 x L2)" % (
               n_copies, n_copies * in_bytes / 1e9))
-    return wl, ms, per_kernel, abytes, clock_info, e2e, l2, wire
+    return wl, ms, per_kernel, abytes, clock_info, e2e, l2, wire, match
 
 
 # ------------------------------------------------------------ CPU oracle
@@ -486,7 +516,8 @@ def main():
     import torch
     if world > 1:
         torch.distributed.init_process_group("nccl")
-    wl, ms, per_kernel, abytes, clocks, e2e, l2, wire = run_ours(args, rank, world, local_rank)
+    wl, ms, per_kernel, abytes, clocks, e2e, l2, wire, match = run_ours(args, rank, world,
+                                                                        local_rank)
     if rank == 0:
         peaks = load_peaks()
         rows = wl.B * (wl.depth + 1) * world
@@ -534,6 +565,16 @@ def main():
                 "roofline": {"bound": "hbm", "unit": "GB/s", "peak": peak,
                              "pack_achieved": gbs_p, "pack_frac": gbs_p / peak,
                              "validate_achieved": gbs_v, "validate_frac": gbs_v / peak},
+            }
+        if match:
+            gbs_m = match["bytes"] / (match["ms"] * 1e-3) / 1e9
+            line["match_verify"] = {
+                "what": "dspark_verify_match of this step's drafts, timed apart from the step",
+                "ms": round(match["ms"], 4), "verify_rows_per_s": wl.B * (wl.depth + 1) * world /
+                (match["ms"] * 1e-3), "mean_accept_len": round(match["mean_accept"], 3),
+                "algorithmic_bytes": match["bytes"],
+                "roofline": {"bound": "hbm", "unit": "GB/s", "peak": peak, "achieved": gbs_m,
+                             "frac": gbs_m / peak},
             }
         if not args.no_cpu:
             line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)

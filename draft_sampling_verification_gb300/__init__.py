@@ -24,11 +24,12 @@ ST_BAD_TEMPERATURE, ST_BAD_Q, ST_BAD_DRAFT, ST_TIMEOUT, ST_INTERNAL = 4, 5, 6, 7
 ST_BAD_CHECKSUM = 9
 FLAG_AMBIG_ACCEPT, FLAG_NEAR_BOUNDARY, FLAG_DEGENERATE = 1, 2, 4
 SCHEDULE_AUTO, SCHEDULE_ONE_LAUNCH, SCHEDULE_SEPARATE = 0, 1, 2
+PURPOSE_PROPOSAL, PURPOSE_ACCEPT, PURPOSE_RESIDUAL, PURPOSE_BONUS, PURPOSE_MATCH = 0, 1, 2, 3, 4
 
 __all__ = ["dspark_q_build", "dspark_q_build_sample", "dspark_draft_sample", "dspark_verify_greedy",
            "dspark_verify_ratio", "dspark_verify", "dspark_target_probs", "dspark_spec_step",
            "dspark_spec_step_schedule", "dspark_spec_step_noalloc", "dspark_q_pack",
-           "dspark_q_validate", "q_build",
+           "dspark_q_validate", "dspark_verify_match", "verify_match", "q_build",
            "draft_sample", "verify_greedy", "verify_ratio", "target_probs", "q_build_sample",
            "spec_step", "version"]
 
@@ -183,6 +184,16 @@ def dspark_spec_step_schedule(B, depth):
     return rc
 
 
+def dspark_verify_match(target_logits, B, depth, draft_tokens, seed, request_ids, accept_len,
+                        committed, flags, req_status, stream=None):
+    rows, V, ld = _rows(target_logits)
+    if rows != B * (depth + 1):
+        raise ValueError("target_logits must hold B*(depth+1) rows")
+    _call("dspark_verify_match", _ptr(target_logits), _dtype_code(target_logits), ld, int(B),
+          int(depth), V, _i32(draft_tokens), int(seed) & (2 ** 64 - 1), _i32(request_ids),
+          _i32(accept_len), _i32(committed), _i32(flags), _i32(req_status), _stream(stream))
+
+
 def dspark_q_pack(counts, sparse_ids, nnz, top_k, V, q_out, checksum_out, stream=None):
     """counts [n_rows, V] (dense) or [n_rows, top_k] with sparse_ids / nnz;
     q_out float32 of the same shape; checksum_out int64 [n_rows] (holding the
@@ -290,6 +301,19 @@ def spec_step(draft_logits, target_logits, B, depth, seed, temperature=None, req
                      schedule=schedule)
     q = {"counts": counts, "ids": None, "nnz": None, "status": status, "top_k": 0}
     return q, tokens, outs
+
+
+def verify_match(target_logits, draft_tokens, seed, request_ids=None, stream=None):
+    """Stochastic verification; returns (accept_len, committed, flags, status)."""
+    B, depth = draft_tokens.shape
+    dev = target_logits.device
+    acc = _empty((B,), torch.int32, dev)
+    com = _empty((B, depth + 1), torch.int32, dev)
+    fl = _empty((B,), torch.int32, dev)
+    st = _empty((B,), torch.int32, dev)
+    dspark_verify_match(target_logits, B, depth, draft_tokens, seed, request_ids, acc, com, fl, st,
+                        stream)
+    return acc, com, fl, st
 
 
 def q_pack(q, V, stream=None):

@@ -31,6 +31,11 @@ cudaError_t launch_verify_modes(const void* z, int dtype, int64_t ld, int B, int
                                 int32_t* g_st, int32_t* r_acc, int32_t* r_com, uint32_t* r_flags,
                                 int32_t* r_st, cudaStream_t stream);
 int spec_step_schedule(int B, int depth);
+cudaError_t launch_verify_match(const void* z, int dtype, int64_t ld, int B, int depth, int V,
+                                const int32_t* drafts, uint64_t seed,
+                                const uint32_t* request_ids, int32_t* accept_len,
+                                int32_t* committed, uint32_t* flags, int32_t* status,
+                                cudaStream_t stream);
 cudaError_t launch_q_pack(const uint32_t* counts, const int32_t* ids, const int32_t* nnz,
                           int top_k, int n_rows, int V, float* q, uint64_t* checksum,
                           cudaStream_t stream);
@@ -197,6 +202,21 @@ int dspark_verify_ratio(const void* target_logits, int32_t dtype, int64_t ld, in
                                              draft_tokens, counts, sparse_ids, nnz, top_k, seed,
                                              request_ids, accept_len, committed, flags,
                                              req_status, static_cast<cudaStream_t>(stream)));
+}
+
+int dspark_verify_match(const void* target_logits, int32_t dtype, int64_t ld, int32_t B,
+                        int32_t depth, int32_t V, const int32_t* draft_tokens, uint64_t seed,
+                        const uint32_t* request_ids, int32_t* accept_len, int32_t* committed,
+                        uint32_t* flags, int32_t* req_status, void* stream) {
+  const int e = check_verify(target_logits, dtype, ld, B, depth, V, draft_tokens, accept_len,
+                             committed, req_status);
+  if (e != 0) return e > 0 ? 0 : e;
+  if ((flags && !aligned(flags, 4)) || (request_ids && !aligned(request_ids, 4)))
+    return DSPARK_ERR_ALIGN;
+  return launch_result(dspark::launch_verify_match(target_logits, dtype, ld, B, depth, V,
+                                                   draft_tokens, seed, request_ids, accept_len,
+                                                   committed, flags, req_status,
+                                                   static_cast<cudaStream_t>(stream)));
 }
 
 int dspark_verify(const void* target_logits, int32_t dtype, int64_t ld, int32_t B, int32_t depth,

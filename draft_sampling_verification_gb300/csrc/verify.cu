@@ -192,7 +192,7 @@ constexpr int verify_cluster() {
   return kDt == DSPARK_BF16 ? 4 : 8;
 }
 
-template <bool kG, bool kR, int kDt>
+template <bool kG, bool kR, int kDt, bool kMatch = false>
 __global__ void __cluster_dims__(verify_cluster<kDt>(), 1, 1) __launch_bounds__(kVThreads, 3)
     verify_kernel(VParams p) {
   constexpr int NC = verify_cluster<kDt>();
@@ -205,7 +205,8 @@ __global__ void __cluster_dims__(verify_cluster<kDt>(), 1, 1) __launch_bounds__(
   }
   __syncthreads();
   uint32_t phase = 0;
-  verify_request<kG, kR, kDt, NC>(p, blockIdx.x / NC, sh, vbuf, mbar, phase, nullptr, nullptr);
+  verify_request<kG, kR, kDt, NC, kMatch>(p, blockIdx.x / NC, sh, vbuf, mbar, phase, nullptr,
+                                          nullptr);
 }
 
 // ------------------------------------------------------------ target p
@@ -311,6 +312,51 @@ cudaError_t launch_verify_modes(const void* z, int dtype, int64_t ld, int B, int
   if (g && r) return go(verify_kernel<true, true, DSPARK_BF16>);
   if (g) return go(verify_kernel<true, false, DSPARK_BF16>);
   return go(verify_kernel<false, true, DSPARK_BF16>);
+}
+
+// The match mode: its outputs take the ratio mode's slots.
+cudaError_t launch_verify_match(const void* z, int dtype, int64_t ld, int B, int depth, int V,
+                                const int32_t* drafts, uint64_t seed,
+                                const uint32_t* request_ids, int32_t* accept_len,
+                                int32_t* committed, uint32_t* flags, int32_t* status,
+                                cudaStream_t stream) {
+  VParams p;
+  p.z = z;
+  p.dtype = dtype;
+  p.ld = ld;
+  p.B = B;
+  p.depth = depth;
+  p.V = V;
+  p.drafts = drafts;
+  p.counts = nullptr;
+  p.ids = nullptr;
+  p.nnz = nullptr;
+  p.top_k = 0;
+  p.seed = seed;
+  p.request_ids = request_ids;
+  p.g_accept_len = nullptr;
+  p.g_committed = nullptr;
+  p.g_status = nullptr;
+  p.r_accept_len = accept_len;
+  p.r_committed = committed;
+  p.r_flags = flags;
+  p.r_status = status;
+  const int nc = (dtype == DSPARK_BF16) ? verify_cluster<DSPARK_BF16>()
+                                        : verify_cluster<DSPARK_F32>();
+  p.chunk = verify_chunk(V, nc);
+  const int esz = (dtype == DSPARK_F32) ? 4 : 2;
+  const int smem = p.chunk * esz + 32;
+  auto go = [&](auto kern) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    kern<<<B * nc, kVThreads, smem, stream>>>(p);
+    return cudaGetLastError();
+  };
+  return dtype == DSPARK_F32 ? go(verify_kernel<false, false, DSPARK_F32, true>)
+                             : go(verify_kernel<false, false, DSPARK_BF16, true>);
 }
 
 cudaError_t launch_verify(int mode, const void* z, int dtype, int64_t ld, int B, int depth, int V,

@@ -69,6 +69,9 @@ struct VSh2 {
   int timeout;
   int found;
   uint32_t near;
+  int m_pick;       // match mode: the row's drawn token, pushed by the CTA that drew it
+  int m_st;
+  uint32_t m_flags;
   int dec;          // ratio decision of the row: 1 accept, 0 reject, -1 refuse (status in dst)
   int dst;
   uint32_t dflags;
@@ -123,7 +126,10 @@ __device__ __forceinline__ void am_merge(float& v, int& i, float v2, int i2) {
 // drafts_sm (shared memory of every CTA) when given, else from p.drafts; the
 // count of draft j in its dense q row from cnt_sm when given, else from
 // p.counts.
-template <bool kG, bool kR, int kDt, int NC = kVCluster>
+// kMatch: the stochastic (match) mode instead of the ratio mode, with the same
+// outputs (r_*): every row draws from its own p (purpose MATCH) and a draw
+// equal to the proposal accepts it.
+template <bool kG, bool kR, int kDt, int NC = kVCluster, bool kMatch = false>
 __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh,
                                                unsigned char* vbuf, uint64_t* mbar,
                                                uint32_t& phase, const int32_t* drafts_sm,
@@ -147,10 +153,19 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
     const int x = draft(j);
     if (x < 0 || x >= V) st0 = DSPARK_ST_BAD_DRAFT;
   }
-  if (tid == 0) sh.timeout = 0;
+  if (tid == 0) {
+    sh.timeout = 0;
+    // read only after a push (every draw has exactly one drawing CTA); a
+    // missing push would stop the request uniformly
+    sh.m_pick = -1;
+    sh.m_st = DSPARK_ST_INTERNAL;
+    sh.m_flags = 0u;
+  }
   __syncthreads();
   int st_g = st0, st_r = st0;  // per-mode statuses
-  bool need_g = kG && st0 == DSPARK_ST_OK, need_r = kR && st0 == DSPARK_ST_OK;
+  static_assert(!(kR && kMatch), "the ratio and the match mode share the r_* outputs");
+  constexpr bool kD = kR || kMatch;  // a mode that draws from p (needs the row sums)
+  bool need_g = kG && st0 == DSPARK_ST_OK, need_r = kD && st0 == DSPARK_ST_OK;
   int L_g = depth, pick_g = -1;
   int xi = 0;
   int L = depth, pick = -1;  // ratio mode
@@ -302,7 +317,7 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
     __syncthreads();
     float cm = sh.wm[0];  // the CTA's max
     for (int w = 1; w < kVThreads / 32; ++w) cm = OpMaxNaNv()(cm, sh.wm[w]);
-    if (kR && need_r) {
+    if (kD && need_r) {
       // the sum of exp relative to the CTA's max: a plain sum
       if (cm > -INFINITY && cm < INFINITY)
         for (int g = tid; g < ng; g += kVThreads) {
@@ -319,7 +334,7 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
       float m = cm, s = 0.0f, av = sh.wam[0];
       int ai = sh.wai[0];
       for (int w = 0; w < kVThreads / 32; ++w) {
-        if (kR && need_r) s += sh.ws[w];
+        if (kD && need_r) s += sh.ws[w];
         if (kG && need_g && w > 0) am_merge(av, ai, sh.wam[w], sh.wai[w]);
       }
       VX& e = sh.x[xi];
@@ -341,7 +356,7 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
         const float m2 = e->m;
         fl |= e->fl;
         if (!(m2 < INFINITY)) bad = true;  // NaN or +inf in that slice
-        if (kR && need_r) ms_merge(m, s, bad ? -INFINITY : m2, bad ? 0.0f : e->s);
+        if (kD && need_r) ms_merge(m, s, bad ? -INFINITY : m2, bad ? 0.0f : e->s);
         else m = fmaxf(m, m2);
         if (kG && need_g) am_merge(av, ai, e->amv, e->ami);
       }
@@ -391,12 +406,16 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
       pick_g = sh.AMI;
       need_g = false;
     }
-    if (!(kR && need_r)) continue;
+    if (!(kD && need_r)) continue;
 
-    // ---- ratio test of draft j (decided above by thread 0)
+    // ---- ratio test of draft j (decided above by thread 0), or the match
+    //      mode's draw from p_j
     bool use_q = false;
     uint32_t purpose = DSPARK_PURPOSE_BONUS;
-    if (j < depth) {
+    if (kMatch) {
+      L = j;
+      purpose = DSPARK_PURPOSE_MATCH;
+    } else if (j < depth) {
       if (sh.dec < 0) {
         st_r = sh.dst;
         need_r = false;
@@ -639,6 +658,24 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
       }
       break;
     }
+    if (kMatch) {
+      // only the CTA that drew the token knows it: it pushes the token, the
+      // status and the boundary flag to every CTA, so that all of them take
+      // the same decision (and the same barriers) below
+      if (writer == rank && tid == 0)
+        for (int r = 0; r < NC; ++r) {
+          VSh2* peer = cluster.map_shared_rank(&sh, r);
+          peer->m_pick = pick;
+          peer->m_st = st_r;
+          peer->m_flags = flags;
+        }
+      cluster.sync();
+      pick = sh.m_pick;
+      st_r = sh.m_st;
+      flags |= sh.m_flags;
+      // a draw equal to the proposal accepts it, and the next row draws
+      if (st_r == DSPARK_ST_OK && j < depth && pick == draft(j)) continue;
+    }
     need_r = false;
   }
 
@@ -658,7 +695,7 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
     p.g_status[b] = st_g;
   }
   const bool i_write = drawn ? (writer == rank) : (rank == 0);
-  if (kR && i_write && tid == 0) {
+  if (kD && i_write && tid == 0) {
     int32_t* com = p.r_committed + (int64_t)b * (depth + 1);
     if (st_r != DSPARK_ST_OK) {
       p.r_accept_len[b] = 0;

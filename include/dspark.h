@@ -69,6 +69,7 @@ extern "C" {
 #define DSPARK_PURPOSE_ACCEPT 1u
 #define DSPARK_PURPOSE_RESIDUAL 2u
 #define DSPARK_PURPOSE_BONUS 3u
+#define DSPARK_PURPOSE_MATCH 4u       /* the stochastic verifier's draw of row j */
 
 /* host-side argument errors */
 #define DSPARK_ERR_NULL (-1)         /* a required pointer is NULL           */
@@ -223,6 +224,30 @@ int dspark_verify_ratio(const void* target_logits, int32_t dtype, int64_t ld, in
                         int32_t top_k, uint64_t seed, const uint32_t* request_ids,
                         int32_t* accept_len, int32_t* committed, uint32_t* flags,
                         int32_t* req_status, void* stream);
+
+/*
+ * dspark_verify_match -- stochastic verification ("DeepSeek-V4.1 DSpark",
+ * State and sampling contracts: each row draws from the target's own
+ * distribution with independent noise, a matching proposal is accepted and
+ * the first mismatch stops verification; it keeps the target distribution
+ * and is not the ratio test).
+ *
+ * p_j = softmax of target row j at T = 1.  For j = 0, 1, ...: the token t_j
+ * is drawn from p_j with w = Philox(seed; request id, j, MATCH) word 0 (t =
+ * w/2^32 * Z over p's weights, the first id whose cumulative weight exceeds
+ * t -- the bonus draw of dspark_verify_ratio); if j < depth and t_j equals
+ * draft j the proposal is accepted and row j+1 draws, else L = j and t_j is
+ * committed (the correction, or the bonus when L == depth).  committed as in
+ * dspark_verify_greedy.  Rows after the deciding row are not read.
+ * Refusals: a draft id outside [0, V) (BAD_DRAFT); NONFINITE / ZERO_MASS for
+ * a read row.  A draw within 1e-6 of a cumulative boundary sets
+ * DSPARK_FLAG_NEAR_BOUNDARY in flags[b] (flags may be NULL).  No q is needed.
+ * Outputs: accept_len[B], committed[B][depth+1], flags[B], req_status[B].
+ */
+int dspark_verify_match(const void* target_logits, int32_t dtype, int64_t ld, int32_t B,
+                        int32_t depth, int32_t V, const int32_t* draft_tokens, uint64_t seed,
+                        const uint32_t* request_ids, int32_t* accept_len, int32_t* committed,
+                        uint32_t* flags, int32_t* req_status, void* stream);
 
 /*
  * dspark_verify -- greedy and/or ratio verification in one pass over the

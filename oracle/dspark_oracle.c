@@ -770,3 +770,52 @@ int oracle_q_validate_row(const float* q, const int32_t* ids, int32_t nnz, int32
     free(c);
     return st;
 }
+
+/* =========================================================================
+ * Stochastic (match) verification ("DeepSeek-V4.1 DSpark", State and
+ * sampling contracts): every verify row draws a token from the target's own
+ * p with independent noise, a proposal is accepted when the draw equals it,
+ * and verification stops at the first mismatch, committing that row's draw
+ * (the draw of row depth when every proposal matched).  This keeps p's
+ * distribution; it is not the ratio test.  Reading: the draw of row j uses
+ * the purpose MATCH = 4 and the same inverse-CDF pick over p as the bonus
+ * draw; refusals as in the other verifiers (draft ids up front, then each
+ * row read).
+ * ========================================================================= */
+#define OR_PURPOSE_MATCH 4u
+
+int oracle_verify_match_req(const float* z, int64_t ld, int32_t V, int32_t depth,
+                            const int32_t* drafts, uint64_t seed, uint32_t request,
+                            int32_t* accept_len, int32_t* committed, uint32_t* flags)
+{
+    uint32_t fl = 0;
+    or_discard(depth, accept_len, committed);
+    if (flags) *flags = 0;
+    for (int32_t j = 0; j < depth; ++j)
+        if (drafts[j] < 0 || drafts[j] >= V) return OR_BAD_DRAFT;
+    double* p = (double*)malloc(sizeof(double) * (size_t)V);
+    if (!p) return -1;
+    int st = OR_OK;
+    int32_t L = depth, pick = -1;
+    for (int32_t j = 0; j <= depth; ++j) {
+        st = oracle_target_row(z + (int64_t)j * ld, V, p, NULL);
+        if (st != OR_OK) break;
+        uint32_t w = oracle_draw_u32(seed, request, (uint32_t)j, OR_PURPOSE_MATCH);
+        int32_t t = oracle_residual_pick(p, NULL, V, w, &fl);
+        if (j < depth && t == drafts[j]) continue;
+        L = j;
+        pick = t;
+        break;
+    }
+    if (st == OR_OK) {
+        *accept_len = L;
+        for (int32_t i = 0; i < L; ++i) committed[i] = drafts[i];
+        committed[L] = pick;
+    } else {
+        or_discard(depth, accept_len, committed);
+        fl = 0;
+    }
+    if (flags) *flags = fl;
+    free(p);
+    return st;
+}

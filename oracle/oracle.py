@@ -27,7 +27,7 @@ M = 1 << 24
 OK, NONFINITE, ZERO_MASS, ALLOC_INCONSISTENT, BAD_TEMPERATURE, BAD_Q, BAD_DRAFT = range(7)
 BAD_CHECKSUM = 9
 FLAG_AMBIG_ACCEPT, FLAG_NEAR_BOUNDARY, FLAG_DEGENERATE = 1, 2, 4
-PURPOSE_PROPOSAL, PURPOSE_ACCEPT, PURPOSE_RESIDUAL, PURPOSE_BONUS = 0, 1, 2, 3
+PURPOSE_PROPOSAL, PURPOSE_ACCEPT, PURPOSE_RESIDUAL, PURPOSE_BONUS, PURPOSE_MATCH = 0, 1, 2, 3, 4
 
 _P = ctypes.c_void_p
 _I32, _I64, _U32, _U64, _F32, _F64 = (ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32,
@@ -72,6 +72,8 @@ def lib():
                 "oracle_verify_greedy_req": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, _P, _P]),
                 "oracle_verify_ratio_req": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, _P, _P, _P,
                                                            _I32, _U64, _U32, _P, _P, _P]),
+                "oracle_verify_match_req": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, _U64, _U32,
+                                                           _P, _P, _P]),
                 "oracle_fletcher64": (_U64, [_P, _I64]),
                 "oracle_q_pack_row": (_U64, [_P, _P, _I32, _I32, _I32, _P]),
                 "oracle_q_validate_row": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, ctypes.c_int,
@@ -323,3 +325,29 @@ def q_validate(q, ids=None, nnz=None, top_k=0, V=None, tokens=None, expect=None)
                                             int(has), ex, _ptr(cr))
         counts[r] = cr
     return st, counts
+
+
+# ------------------------------------------------------- stochastic (match)
+def verify_match(z, drafts, seed, request_ids=None):
+    """z: [B, depth+1, V] fp32; drafts [B, depth].  Returns (accept_len,
+    committed, flags, status)."""
+    z = _c(z, np.float32)
+    drafts = _c(drafts, np.int32)
+    B, rows, V = z.shape
+    depth = rows - 1
+    req = np.arange(B, dtype=np.uint32) if request_ids is None else _c(request_ids, np.uint32)
+    acc = np.zeros(B, np.int32)
+    com = np.full((B, depth + 1), -1, np.int32)
+    flags = np.zeros(B, np.uint32)
+    status = np.zeros(B, np.int32)
+    a = ctypes.c_int32(0)
+    fl = ctypes.c_uint32(0)
+    for b in range(B):
+        cm = np.zeros(depth + 1, np.int32)
+        status[b] = lib().oracle_verify_match_req(_ptr(z[b]), V, V, depth, _ptr(drafts[b]), seed,
+                                                  int(req[b]), ctypes.byref(a), _ptr(cm),
+                                                  ctypes.byref(fl))
+        acc[b] = a.value
+        com[b] = cm
+        flags[b] = fl.value
+    return acc, com, flags, status
