@@ -61,6 +61,8 @@ def parse():
                     help="skip the received-q (pack + validate) measurement")
     ap.add_argument("--no-match", action="store_true",
                     help="skip the stochastic (match) verification measurement")
+    ap.add_argument("--no-chain", action="store_true",
+                    help="skip the Markov-conditioned draft chain measurement")
     ap.add_argument("--schedule", default="auto", choices=["auto", "one", "separate"],
                     help="dense q: one persistent launch, or q build then one verify pass")
     return ap.parse_args()
@@ -426,6 +428,38 @@ def run_ours(args, rank, world, local_rank):
         match = {"ms": me0.elapsed_time(me1) / args.steps, "bytes": int(rows_read * V * esz_t),
                  "mean_accept": float(mo[0].float().mean().item())}
 
+    # ---- the Markov-conditioned draft chain on this step's draft rows, with
+    #      a synthetic bias table of 64 rows (dense q only), timed apart
+    chain = None
+    if not args.no_chain and top_k == 0:
+        gbias = torch.Generator(device=dev)
+        gbias.manual_seed(1234)
+        bias = torch.randn((64, V), generator=gbias, device=dev, dtype=torch.float32)
+        anchors = torch.from_numpy((req_np % V).astype(np.int32)).to(dev)
+        cws = torch.empty((rows_d * V,), dtype=torch.float32, device=dev)
+        ctok = torch.empty((B, depth), dtype=torch.int32, device=dev)
+        cst = torch.empty((rows_d,), dtype=torch.int32, device=dev)
+        cmg = torch.empty((B, depth), dtype=torch.float32, device=dev)
+
+        def chain_step():
+            ds.dspark_q_chain_sample(xd, B, depth, temps, bias, anchors, wl.seed, req, cws,
+                                     counts, ctok, cst, cmg, stream)
+
+        for _ in range(max(3, args.warmup)):
+            chain_step()
+        torch.cuda.synchronize()
+        assert int((cst != 0).sum()) == 0, "refused rows in the chain"
+        ce0 = torch.cuda.Event(enable_timing=True)
+        ce1 = torch.cuda.Event(enable_timing=True)
+        ce0.record(stream)
+        for _ in range(args.steps):
+            chain_step()
+        ce1.record(stream)
+        torch.cuda.synchronize()
+        # the method's bytes: base logits and the bias row read, counts written
+        chain = {"ms": ce0.elapsed_time(ce1) / args.steps,
+                 "bytes": rows_d * V * (wl.draft.itemsize + 4 + 4)}
+
     ms = elapsed_ms / args.steps
     if world > 1:
         t = max_over_ranks(torch.tensor([ms, e2e["ms_per_step"] if e2e else 0.0], device=dev))
@@ -435,7 +469,7 @@ def run_ours(args, rank, world, local_rank):
     l2 = ("inputs larger than L2 (%.2f GB per step)" % (in_bytes / 1e9) if n_copies == 1 else
           "inputs rotated over %d copies (%.2f GB in all, > 3 x L2)" % (
               n_copies, n_copies * in_bytes / 1e9))
-    return wl, ms, per_kernel, abytes, clock_info, e2e, l2, wire, match
+    return wl, ms, per_kernel, abytes, clock_info, e2e, l2, wire, match, chain
 
 
 # ------------------------------------------------------------ CPU oracle
@@ -516,8 +550,8 @@ def main():
     import torch
     if world > 1:
         torch.distributed.init_process_group("nccl")
-    wl, ms, per_kernel, abytes, clocks, e2e, l2, wire, match = run_ours(args, rank, world,
-                                                                        local_rank)
+    wl, ms, per_kernel, abytes, clocks, e2e, l2, wire, match, chain = run_ours(
+        args, rank, world, local_rank)
     if rank == 0:
         peaks = load_peaks()
         rows = wl.B * (wl.depth + 1) * world
@@ -575,6 +609,17 @@ def main():
                 "algorithmic_bytes": match["bytes"],
                 "roofline": {"bound": "hbm", "unit": "GB/s", "peak": peak, "achieved": gbs_m,
                              "frac": gbs_m / peak},
+            }
+        if chain:
+            gbs_c = chain["bytes"] / (chain["ms"] * 1e-3) / 1e9
+            line["markov_chain"] = {
+                "what": "dspark_q_chain_sample on this step's draft rows (64-row bias table), "
+                        "timed apart from the step",
+                "ms": round(chain["ms"], 4),
+                "draft_positions_per_s": wl.B * wl.depth * world / (chain["ms"] * 1e-3),
+                "algorithmic_bytes": chain["bytes"],
+                "roofline": {"bound": "hbm", "unit": "GB/s", "peak": peak, "achieved": gbs_c,
+                             "frac": gbs_c / peak},
             }
         if not args.no_cpu:
             line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)

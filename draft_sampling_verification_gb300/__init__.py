@@ -29,7 +29,8 @@ PURPOSE_PROPOSAL, PURPOSE_ACCEPT, PURPOSE_RESIDUAL, PURPOSE_BONUS, PURPOSE_MATCH
 __all__ = ["dspark_q_build", "dspark_q_build_sample", "dspark_draft_sample", "dspark_verify_greedy",
            "dspark_verify_ratio", "dspark_verify", "dspark_target_probs", "dspark_spec_step",
            "dspark_spec_step_schedule", "dspark_spec_step_noalloc", "dspark_q_pack",
-           "dspark_q_validate", "dspark_verify_match", "verify_match", "q_build",
+           "dspark_q_validate", "dspark_verify_match", "verify_match", "dspark_q_chain_sample",
+           "q_chain_sample", "q_build",
            "draft_sample", "verify_greedy", "verify_ratio", "target_probs", "q_build_sample",
            "spec_step", "version"]
 
@@ -194,6 +195,21 @@ def dspark_verify_match(target_logits, B, depth, draft_tokens, seed, request_ids
           _i32(accept_len), _i32(committed), _i32(flags), _i32(req_status), _stream(stream))
 
 
+def dspark_q_chain_sample(draft_logits, B, depth, temperature, bias, anchors, seed,
+                          request_ids, workspace, counts, draft_tokens, row_status, margins=None,
+                          stream=None):
+    """draft_logits [B*depth, V] (or [B, depth, V]); bias [n_bias, V] fp32 or None;
+    anchors int32 [B]; workspace fp32 with B*depth*V elements."""
+    rows, V, ld = _rows(draft_logits)
+    if rows != B * depth:
+        raise ValueError("draft_logits must hold B*depth rows")
+    nb, bld = (0, V) if bias is None else (bias.shape[0], bias.stride(0))
+    _call("dspark_q_chain_sample", _ptr(draft_logits), _dtype_code(draft_logits), ld, int(B),
+          int(depth), V, _ptr(temperature), _ptr(bias), bld, nb, _i32(anchors),
+          int(seed) & (2 ** 64 - 1), _i32(request_ids), _ptr(workspace), _i32(counts),
+          _i32(draft_tokens), _i32(row_status), _ptr(margins), _stream(stream))
+
+
 def dspark_q_pack(counts, sparse_ids, nnz, top_k, V, q_out, checksum_out, stream=None):
     """counts [n_rows, V] (dense) or [n_rows, top_k] with sparse_ids / nnz;
     q_out float32 of the same shape; checksum_out int64 [n_rows] (holding the
@@ -314,6 +330,23 @@ def verify_match(target_logits, draft_tokens, seed, request_ids=None, stream=Non
     dspark_verify_match(target_logits, B, depth, draft_tokens, seed, request_ids, acc, com, fl, st,
                         stream)
     return acc, com, fl, st
+
+
+def q_chain_sample(draft_logits, B, depth, seed, anchors, bias=None, temperature=None,
+                   request_ids=None, stream=None):
+    """The Markov-conditioned draft chain; returns (q dict, tokens [B, depth],
+    margins [B, depth])."""
+    rows, V, _ = _rows(draft_logits)
+    dev = draft_logits.device
+    ws = _empty((rows * V,), torch.float32, dev)
+    counts = _empty((rows, V), torch.int32, dev)
+    status = _empty((rows,), torch.int32, dev)
+    tokens = _empty((B, depth), torch.int32, dev)
+    margins = _empty((B, depth), torch.float32, dev)
+    dspark_q_chain_sample(draft_logits, B, depth, temperature, bias, anchors, seed, request_ids,
+                          ws, counts, tokens, status, margins, stream)
+    q = {"counts": counts, "ids": None, "nnz": None, "status": status, "top_k": 0}
+    return q, tokens, margins
 
 
 def q_pack(q, V, stream=None):

@@ -31,6 +31,12 @@ cudaError_t launch_verify_modes(const void* z, int dtype, int64_t ld, int B, int
                                 int32_t* g_st, int32_t* r_acc, int32_t* r_com, uint32_t* r_flags,
                                 int32_t* r_st, cudaStream_t stream);
 int spec_step_schedule(int B, int depth);
+cudaError_t launch_q_chain(const void* x, int dtype, int64_t ld, int B, int depth, int V,
+                           const float* temperature, const float* bias, int64_t bias_ld,
+                           int n_bias, const int32_t* anchors, uint64_t seed,
+                           const uint32_t* request_ids, float* workspace, uint32_t* counts,
+                           int32_t* tokens, int32_t* status, float* margins,
+                           cudaStream_t stream);
 cudaError_t launch_verify_match(const void* z, int dtype, int64_t ld, int B, int depth, int V,
                                 const int32_t* drafts, uint64_t seed,
                                 const uint32_t* request_ids, int32_t* accept_len,
@@ -332,6 +338,30 @@ int dspark_spec_step_noalloc(const void* draft_logits, int32_t draft_dtype, int6
                         draft_tokens, row_status, greedy_accept_len, greedy_committed,
                         greedy_status, ratio_accept_len, ratio_committed, ratio_flags,
                         ratio_status, nullptr, true, schedule, stream);
+}
+
+int dspark_q_chain_sample(const void* draft_logits, int32_t dtype, int64_t ld, int32_t B,
+                          int32_t depth, int32_t V, const float* temperature, const float* bias,
+                          int64_t bias_ld, int32_t n_bias, const int32_t* anchors, uint64_t seed,
+                          const uint32_t* request_ids, float* workspace, uint32_t* counts,
+                          int32_t* draft_tokens, int32_t* row_status, float* margins,
+                          void* stream) {
+  if (int e = check_common(dtype, V, ld)) return e;
+  if (depth < 1 || depth > DSPARK_MAX_DEPTH) return DSPARK_ERR_SIZE;
+  if (B < 0 || (int64_t)B * depth > kMaxGridRows) return DSPARK_ERR_SIZE;
+  if (bias && (n_bias < 1 || bias_ld < V)) return DSPARK_ERR_SIZE;
+  if (B == 0) return 0;
+  if (!draft_logits || !anchors || !workspace || !counts || !draft_tokens || !row_status)
+    return DSPARK_ERR_NULL;
+  const void* four[] = {anchors, workspace, counts, draft_tokens, row_status, margins,
+                        temperature, request_ids, bias};
+  for (const void* q : four)
+    if (q && !aligned(q, 4)) return DSPARK_ERR_ALIGN;
+  if (!aligned(draft_logits, esize(dtype))) return DSPARK_ERR_ALIGN;
+  return launch_result(dspark::launch_q_chain(
+      draft_logits, dtype, ld, B, depth, V, temperature, bias, bias_ld, bias ? n_bias : 1,
+      anchors, seed, request_ids, workspace, counts, draft_tokens, row_status, margins,
+      static_cast<cudaStream_t>(stream)));
 }
 
 int dspark_q_pack(const uint32_t* counts, const int32_t* sparse_ids, const int32_t* nnz,

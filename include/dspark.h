@@ -364,6 +364,35 @@ int dspark_target_probs(const void* target_logits, int32_t dtype, int64_t ld, in
                         void* stream);
 
 /*
+ * dspark_q_chain_sample -- the Markov-conditioned draft chain ("Remote DSpark
+ * drafter -- wire and state contract", section 2: the sequential Markov step
+ * adds the bias row of the previous sampled token, the anchor at step 0;
+ * section 6.3: margin = top1 - top2 of (base + Markov) logits at each step).
+ *
+ * For each request b the rows j = 0 .. depth-1 run in order: z_v =
+ * RN32(x_v + bias[prev mod n_bias][v]) (z = x when bias is NULL; prev =
+ * anchors[b] at j = 0, else the token drawn at row j-1), then the dense q of
+ * z with temperature[b*depth + j] and the draft draw of that row, exactly as
+ * dspark_q_build_sample on z.  margins[b*depth + j] (may be NULL): z's
+ * largest finite value minus its second largest (0 when they are equal,
+ * FLT_MAX with fewer than two finite values, 0 on a refused row).  A row
+ * after a refused row is refused with the same status (no token to condition
+ * on); an anchor outside [0, V) refuses the request with BAD_DRAFT.
+ *
+ * draft_logits [B*depth][ld] (fp32 or bf16); bias [n_bias][bias_ld] fp32
+ * (bias_ld >= V, n_bias >= 1) or NULL; anchors[B]; workspace: B*depth*V fp32
+ * of device memory owned by the caller (z rows; overwritten); counts
+ * [B*depth][V], draft_tokens[B][depth], row_status[B*depth] as in
+ * dspark_q_build_sample.
+ */
+int dspark_q_chain_sample(const void* draft_logits, int32_t dtype, int64_t ld, int32_t B,
+                          int32_t depth, int32_t V, const float* temperature, const float* bias,
+                          int64_t bias_ld, int32_t n_bias, const int32_t* anchors, uint64_t seed,
+                          const uint32_t* request_ids, float* workspace, uint32_t* counts,
+                          int32_t* draft_tokens, int32_t* row_status, float* margins,
+                          void* stream);
+
+/*
  * dspark_q_pack -- the wire form of q rows ("PP1 q transport and scheduling
  * design", Distribution contract and precision: q is sent as little-endian
  * FP32 q(v) = c_v / M, every such value exact; Versioned v2 message design:

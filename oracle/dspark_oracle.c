@@ -38,6 +38,7 @@
  * re-type its formula (closed forms, exhaustive enumeration, library
  * cross-checks, an independent rational re-derivation on tiny vocabularies).
  */
+#include <float.h>
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -818,4 +819,77 @@ int oracle_verify_match_req(const float* z, int64_t ld, int32_t V, int32_t depth
     if (flags) *flags = fl;
     free(p);
     return st;
+}
+
+/* =========================================================================
+ * Markov-conditioned draft chain ("Remote DSpark drafter -- wire and state
+ * contract", section 2: the sequential Markov step adds the bias row of the
+ * previous sampled token to the base logits, the anchor at step 0; section
+ * 6.3: the optional margin is top1 - top2 of (base + Markov) logits at each
+ * step).  Readings: z_v = RN32(x_v + bias[prev mod n_bias][v]); the dense q
+ * of z with the row's temperature, then the draft draw of that row; the
+ * margin is z's largest finite value minus its second largest (equal values
+ * give 0), FLT_MAX when fewer than two are finite, 0 for a refused row; a row
+ * after a refused row is refused with the same status (the chain has no
+ * token to condition on); an anchor outside [0, V) refuses the request with
+ * BAD_DRAFT.
+ * ========================================================================= */
+int oracle_q_chain_request(const float* x, int64_t ld, int32_t V, int32_t depth,
+                           const float* temperature, const float* bias, int64_t bias_ld,
+                           int32_t n_bias, int32_t anchor, uint64_t seed, uint32_t request,
+                           uint32_t* counts, int32_t* tokens, int32_t* status, float* margins)
+{
+    float* z = (float*)malloc(sizeof(float) * (size_t)V);
+    if (!z) return -1;
+    int32_t prev = anchor;
+    int refused = (anchor < 0 || anchor >= V) ? OR_BAD_DRAFT : OR_OK;
+    for (int32_t j = 0; j < depth; ++j) {
+        uint32_t* c = counts + (int64_t)j * V;
+        if (refused != OR_OK) {
+            memset(c, 0, sizeof(uint32_t) * (size_t)V);
+            tokens[j] = -1;
+            status[j] = refused;
+            if (margins) margins[j] = 0.0f;
+            continue;
+        }
+        const float* xr = x + (int64_t)j * ld;
+        const float* br = bias ? bias + (int64_t)(prev % n_bias) * bias_ld : NULL;
+        float t1 = -INFINITY, t2 = -INFINITY;
+        int32_t nfin = 0;
+        for (int32_t v = 0; v < V; ++v) {
+            z[v] = br ? xr[v] + br[v] : xr[v];
+            if (isfinite(z[v])) {
+                ++nfin;
+                if (z[v] > t1) { t2 = t1; t1 = z[v]; }
+                else if (z[v] > t2) t2 = z[v];
+            }
+        }
+        float T = temperature ? temperature[j] : 1.0f;
+        int32_t ids_unused = 0, nnz_unused = 0;
+        int st = oracle_q_build_row(z, V, T, 0, c, &ids_unused, &nnz_unused);
+        if (st == OR_OK) {
+            int32_t st2 = OR_OK;
+            tokens[j] = oracle_draft_sample_row(c, NULL, V, V, seed, request, (uint32_t)j, &st2);
+            st = st2;
+        }
+        if (st != OR_OK) {
+            tokens[j] = -1;
+            refused = st;
+        }
+        status[j] = st;
+        if (margins) {
+            float mg = 0.0f;
+            if (st == OR_OK) {
+                if (nfin < 2) mg = FLT_MAX;
+                else {
+                    mg = t1 - t2;
+                    if (!(mg <= FLT_MAX)) mg = FLT_MAX;
+                }
+            }
+            margins[j] = mg;
+        }
+        prev = tokens[j];
+    }
+    free(z);
+    return OR_OK;
 }

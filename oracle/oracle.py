@@ -74,6 +74,8 @@ def lib():
                                                            _I32, _U64, _U32, _P, _P, _P]),
                 "oracle_verify_match_req": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, _U64, _U32,
                                                            _P, _P, _P]),
+                "oracle_q_chain_request": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, _P, _I64, _I32,
+                                                          _I32, _U64, _U32, _P, _P, _P, _P]),
                 "oracle_fletcher64": (_U64, [_P, _I64]),
                 "oracle_q_pack_row": (_U64, [_P, _P, _I32, _I32, _I32, _P]),
                 "oracle_q_validate_row": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, ctypes.c_int,
@@ -351,3 +353,26 @@ def verify_match(z, drafts, seed, request_ids=None):
         com[b] = cm
         flags[b] = fl.value
     return acc, com, flags, status
+
+
+# ------------------------------------------------------ Markov draft chain
+def q_chain(x, temperature, bias, anchors, seed, request_ids=None):
+    """x: [B, depth, V] fp32 base logits; temperature [B*depth] or None; bias
+    [n_bias, V] fp32 or None; anchors [B].  Returns (counts [B*depth, V],
+    tokens [B, depth], status [B*depth], margins [B, depth])."""
+    x = _c(x, np.float32)
+    B, depth, V = x.shape
+    t = None if temperature is None else _c(temperature, np.float32).reshape(B, depth)
+    b = None if bias is None else _c(bias, np.float32)
+    nb = 1 if b is None else b.shape[0]
+    req = np.arange(B, dtype=np.uint32) if request_ids is None else _c(request_ids, np.uint32)
+    counts = np.zeros((B, depth, V), np.uint32)
+    tokens = np.zeros((B, depth), np.int32)
+    status = np.zeros((B, depth), np.int32)
+    margins = np.zeros((B, depth), np.float32)
+    for r in range(B):
+        tr = None if t is None else _c(t[r], np.float32)
+        lib().oracle_q_chain_request(_ptr(x[r]), V, V, depth, _ptr(tr), _ptr(b), V, nb,
+                                     int(anchors[r]), seed, int(req[r]), _ptr(counts[r]),
+                                     _ptr(tokens[r]), _ptr(status[r]), _ptr(margins[r]))
+    return counts.reshape(B * depth, V), tokens, status.reshape(-1), margins
