@@ -63,6 +63,8 @@ def parse():
                     help="skip the stochastic (match) verification measurement")
     ap.add_argument("--no-chain", action="store_true",
                     help="skip the Markov-conditioned draft chain measurement")
+    ap.add_argument("--no-sharded", action="store_true",
+                    help="skip the vocabulary-sharded (TP2 emulation) q build measurement")
     ap.add_argument("--schedule", default="auto", choices=["auto", "one", "separate"],
                     help="dense q: one persistent launch, or q build then one verify pass")
     return ap.parse_args()
@@ -460,6 +462,34 @@ def run_ours(args, rank, world, local_rank):
         chain = {"ms": ce0.elapsed_time(ce1) / args.steps,
                  "bytes": rows_d * V * (wl.draft.itemsize + 4 + 4)}
 
+    # ---- the vocabulary-sharded q build and draw (two emulated ranks) on
+    #      this step's draft rows (dense q), timed apart from the step
+    sharded = None
+    if not args.no_sharded and top_k == 0:
+        sws = torch.empty((ds.dspark_q_sharded_workspace_bytes(rows_d),), dtype=torch.uint8,
+                          device=dev)
+        stok = torch.empty((B, depth), dtype=torch.int32, device=dev)
+        sst2 = torch.empty((rows_d,), dtype=torch.int32, device=dev)
+
+        def sharded_step():
+            ds.dspark_q_build_sample_sharded(xd, B, depth, 2, temps, wl.seed, req, counts, stok,
+                                             sst2, sws, stream)
+
+        for _ in range(max(3, args.warmup)):
+            sharded_step()
+        torch.cuda.synchronize()
+        se0 = torch.cuda.Event(enable_timing=True)
+        se1 = torch.cuda.Event(enable_timing=True)
+        se0.record(stream)
+        for _ in range(args.steps):
+            sharded_step()
+        se1.record(stream)
+        torch.cuda.synchronize()
+        sharded = {"ms": se0.elapsed_time(se1) / args.steps,
+                   "bytes": abytes.get("q_build_sample", 0) if not one_launch
+                   else rows_d * V * 8 + rows_d * 4,
+                   "internal": int((sst2 == ds.ST_INTERNAL).sum())}
+
     ms = elapsed_ms / args.steps
     if world > 1:
         t = max_over_ranks(torch.tensor([ms, e2e["ms_per_step"] if e2e else 0.0], device=dev))
@@ -469,7 +499,7 @@ def run_ours(args, rank, world, local_rank):
     l2 = ("inputs larger than L2 (%.2f GB per step)" % (in_bytes / 1e9) if n_copies == 1 else
           "inputs rotated over %d copies (%.2f GB in all, > 3 x L2)" % (
               n_copies, n_copies * in_bytes / 1e9))
-    return wl, ms, per_kernel, abytes, clock_info, e2e, l2, wire, match, chain
+    return wl, ms, per_kernel, abytes, clock_info, e2e, l2, wire, match, chain, sharded
 
 
 # ------------------------------------------------------------ CPU oracle
@@ -550,7 +580,7 @@ def main():
     import torch
     if world > 1:
         torch.distributed.init_process_group("nccl")
-    wl, ms, per_kernel, abytes, clocks, e2e, l2, wire, match, chain = run_ours(
+    wl, ms, per_kernel, abytes, clocks, e2e, l2, wire, match, chain, sharded = run_ours(
         args, rank, world, local_rank)
     if rank == 0:
         peaks = load_peaks()
@@ -620,6 +650,16 @@ def main():
                 "algorithmic_bytes": chain["bytes"],
                 "roofline": {"bound": "hbm", "unit": "GB/s", "peak": peak, "achieved": gbs_c,
                              "frac": gbs_c / peak},
+            }
+        if sharded:
+            gbs_s = sharded["bytes"] / (sharded["ms"] * 1e-3) / 1e9
+            line["sharded_q"] = {
+                "what": "dspark_q_build_sample_sharded with 2 emulated ranks on this step's draft "
+                        "rows, timed apart from the step",
+                "ms": round(sharded["ms"], 4), "rows_refused_internal": sharded["internal"],
+                "algorithmic_bytes": sharded["bytes"],
+                "roofline": {"bound": "hbm", "unit": "GB/s", "peak": peak, "achieved": gbs_s,
+                             "frac": gbs_s / peak},
             }
         if not args.no_cpu:
             line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)

@@ -30,7 +30,8 @@ __all__ = ["dspark_q_build", "dspark_q_build_sample", "dspark_draft_sample", "ds
            "dspark_verify_ratio", "dspark_verify", "dspark_target_probs", "dspark_spec_step",
            "dspark_spec_step_schedule", "dspark_spec_step_noalloc", "dspark_q_pack",
            "dspark_q_validate", "dspark_verify_match", "verify_match", "dspark_q_chain_sample",
-           "q_chain_sample", "q_build",
+           "q_chain_sample", "dspark_q_build_sample_sharded", "dspark_q_sharded_workspace_bytes",
+           "q_build_sample_sharded", "q_build",
            "draft_sample", "verify_greedy", "verify_ratio", "target_probs", "q_build_sample",
            "spec_step", "version"]
 
@@ -210,6 +211,22 @@ def dspark_q_chain_sample(draft_logits, B, depth, temperature, bias, anchors, se
           _i32(draft_tokens), _i32(row_status), _ptr(margins), _stream(stream))
 
 
+def dspark_q_sharded_workspace_bytes(n_rows):
+    return int(_lib.load().dspark_q_sharded_workspace_bytes(int(n_rows)))
+
+
+def dspark_q_build_sample_sharded(draft_logits, B, depth, n_shards, temperature, seed,
+                                  request_ids, counts, draft_tokens, row_status, workspace,
+                                  stream=None):
+    rows, V, ld = _rows(draft_logits)
+    if rows != B * depth:
+        raise ValueError("draft_logits must hold B*depth rows")
+    _call("dspark_q_build_sample_sharded", _ptr(draft_logits), _dtype_code(draft_logits), ld,
+          int(B), int(depth), V, int(n_shards), _ptr(temperature), int(seed) & (2 ** 64 - 1),
+          _i32(request_ids), _i32(counts), _i32(draft_tokens), _i32(row_status), _ptr(workspace),
+          _stream(stream))
+
+
 def dspark_q_pack(counts, sparse_ids, nnz, top_k, V, q_out, checksum_out, stream=None):
     """counts [n_rows, V] (dense) or [n_rows, top_k] with sparse_ids / nnz;
     q_out float32 of the same shape; checksum_out int64 [n_rows] (holding the
@@ -347,6 +364,20 @@ def q_chain_sample(draft_logits, B, depth, seed, anchors, bias=None, temperature
                           ws, counts, tokens, status, margins, stream)
     q = {"counts": counts, "ids": None, "nnz": None, "status": status, "top_k": 0}
     return q, tokens, margins
+
+
+def q_build_sample_sharded(draft_logits, B, depth, n_shards, seed, temperature=None,
+                           request_ids=None, stream=None):
+    """The vocabulary-sharded emulation of q_build_sample (dense q)."""
+    rows, V, _ = _rows(draft_logits)
+    dev = draft_logits.device
+    ws = _empty((dspark_q_sharded_workspace_bytes(rows),), torch.uint8, dev)
+    counts = _empty((rows, V), torch.int32, dev)
+    status = _empty((rows,), torch.int32, dev)
+    tokens = _empty((B, depth), torch.int32, dev)
+    dspark_q_build_sample_sharded(draft_logits, B, depth, n_shards, temperature, seed,
+                                  request_ids, counts, tokens, status, ws, stream)
+    return {"counts": counts, "ids": None, "nnz": None, "status": status, "top_k": 0}, tokens
 
 
 def q_pack(q, V, stream=None):

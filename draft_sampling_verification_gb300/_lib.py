@@ -31,6 +31,8 @@ SIGNATURES = {
                       _P, _P, _P, _P, _P, _P],
     "dspark_spec_step_schedule": [_I32, _I32],
     "dspark_q_pack": [_P, _P, _P, _I32, _I32, _I32, _P, _P, _P],
+    "dspark_q_build_sample_sharded": [_P, _I32, _I64, _I32, _I32, _I32, _I32, _P, _U64, _P, _P,
+                                      _P, _P, _P, _P],
     "dspark_q_chain_sample": [_P, _I32, _I64, _I32, _I32, _I32, _P, _P, _I64, _I32, _P, _U64, _P,
                               _P, _P, _P, _P, _P, _P],
     "dspark_verify_match": [_P, _I32, _I64, _I32, _I32, _I32, _P, _U64, _P, _P, _P, _P, _P, _P],
@@ -53,7 +55,7 @@ def header_symbols(paths=None):
     names = set()
     for path in paths or HEADERS:
         text = open(path).read()
-        names.update(re.findall(r"^\s*(?:int|const char\*)\s+(dspark_\w+)\s*\(", text, re.M))
+        names.update(re.findall(r"^\s*(?:int|int64_t|const char\*)\s+(dspark_\w+)\s*\(", text, re.M))
     return sorted(names)
 
 
@@ -70,6 +72,8 @@ def load(path: str = LIB_PATH):
                 fn = getattr(lib, name)
                 fn.argtypes = args
                 fn.restype = ctypes.c_int
+            lib.dspark_q_sharded_workspace_bytes.argtypes = [_I32]
+            lib.dspark_q_sharded_workspace_bytes.restype = ctypes.c_int64
             lib.dspark_version.argtypes = []
             lib.dspark_version.restype = ctypes.c_char_p
             _lib = lib

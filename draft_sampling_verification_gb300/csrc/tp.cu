@@ -1,0 +1,481 @@
+// tp.cu -- the vocabulary-sharded q build and draft draw, emulated on one GPU
+// ("PP1 q transport and scheduling design", Sparse support and
+// vocabulary-sharded TP2 follow-up: each rank computes its logit max and
+// shifted sum and an all-reduce gives the global normalisation; the remaining
+// tickets are coordinated globally; the leader's one integer draw picks the
+// shard by its count mass, then the token inside it).
+//
+// The vocabulary is split into n_sh contiguous shards of ceil(V / n_sh) ids.
+// Each kernel below runs one CTA per (row, shard) -- the work of one rank --
+// and every exchange between ranks goes through a per-row record in the
+// caller's workspace between launches: a rank only reads the other ranks'
+// partials, never their rows.
+//   1  local max of y and the validity flags
+//   2  all-reduce max (each rank combines the partials); E and its uint64 sum
+//   3  all-reduce the sum; exact floors f, the fraction histogram (2048 bins
+//      of floor(2048 r)), the floor sum and the count of r > 0
+//   4  all-reduce F, the histograms and the counts; the bin holding the
+//      grant threshold; counts f + [bin above it]; each rank's table of the
+//      distinct exact fractions in that bin, with their counts
+//   5  the leader merges the tables: the threshold fraction T and each
+//      rank's quota of members at T (ranks in id order, so the lowest ids
+//      come first); a refused row is zeroed here
+//   6  each rank grants its members above T, and its quota of members at T
+//      to its lowest ids (an id-ordered block scan); its count total.  The
+//      threshold-bin members are marked in the counts by step 4, so only
+//      they are split again here
+//   7  the leader's draw: the shard by the count totals, the token inside
+// Floors and fractions are exact integer splits of E * RN64(2^24 / RN64(S)),
+// so the counts equal those of the unsharded build bit for bit.
+#include "common.cuh"
+
+namespace dspark {
+namespace {
+
+constexpr int kTpThr = 256;
+constexpr int kTpMaxShards = 8;
+constexpr int kTpBins = 2048;
+constexpr int kTpTab = 1024;  // distinct threshold-bin fractions per shard
+constexpr uint64_t kTpEmpty = ~0ull;  // an empty table slot (no fraction key is all ones)
+constexpr uint32_t kTpMark = 0x80000000u;  // a count marked as a threshold-bin member (f < 2^31)
+
+// One draft row's exchange record.
+struct TpRow {
+  float mx[kTpMaxShards];
+  uint32_t fl[kTpMaxShards];  // bit0 NaN / +inf / overflow, bit1 a finite y
+  uint64_t S[kTpMaxShards];
+  uint64_t F[kTpMaxShards];
+  uint32_t npos[kTpMaxShards];
+  uint64_t C[kTpMaxShards];
+  uint32_t over[kTpMaxShards];   // the shard's table overflowed
+  uint32_t quota[kTpMaxShards];  // members at T granted in the shard
+  uint64_t T;                    // the threshold fraction's key
+  int32_t st;                    // the row's status after the grant step
+  uint32_t hist[kTpMaxShards][kTpBins];
+  uint64_t tab_key[kTpMaxShards][kTpTab];
+  uint32_t tab_cnt[kTpMaxShards][kTpTab];
+};
+
+struct TpParams {
+  const void* x;
+  int dtype;
+  int64_t ld;
+  int V;
+  int n_sh;
+  int depth;
+  const float* temperature;
+  uint64_t seed;
+  const uint32_t* request_ids;
+  uint32_t* counts;
+  int32_t* tokens;
+  int32_t* status;
+  TpRow* ws;
+};
+
+struct TpShared {
+  uint64_t r64[32];
+  uint32_t r32[32];
+  float rf[32];
+  uint32_t hist[kTpBins];
+  int found;
+};
+
+struct OpMaxNaNTp {
+  __device__ float operator()(float a, float b) const {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+  }
+};
+
+struct Shard {
+  int row, s, lo, hi;
+};
+
+__device__ __forceinline__ Shard shard_of(const TpParams& p) {
+  Shard sh;
+  sh.row = blockIdx.x / p.n_sh;
+  sh.s = blockIdx.x % p.n_sh;
+  const int vs = (p.V + p.n_sh - 1) / p.n_sh;
+  sh.lo = min(p.V, sh.s * vs);
+  sh.hi = min(p.V, sh.lo + vs);
+  return sh;
+}
+
+__device__ __forceinline__ float inv_temp(const TpParams& p, int row, bool* bad) {
+  const float T = p.temperature ? p.temperature[row] : 1.0f;
+  const float iT = __frcp_rn(T);
+  *bad = !(isfinite(T) && T > 0.0f) || !(isfinite(iT) && iT >= 0x1p-126f);
+  return iT;
+}
+
+__device__ __forceinline__ float y_of(const TpParams& p, int row, int v, float invT) {
+  const char* xrow = reinterpret_cast<const char*>(p.x) +
+                     (int64_t)row * p.ld * (p.dtype == DSPARK_F32 ? 4 : 2);
+  const float x = load_logit(xrow, p.dtype, v);
+  return invT == 1.0f ? x : __fmul_rn(x, invT);
+}
+
+// The row's status from every rank's flags, and the global max (all-reduce).
+__device__ __forceinline__ int row_state(const TpParams& p, const TpRow& w, bool badT, float* m) {
+  float mm = -INFINITY;
+  uint32_t fl = 0;
+  for (int s = 0; s < p.n_sh; ++s) {
+    mm = fmaxf(mm, w.mx[s]);
+    fl |= w.fl[s];
+  }
+  *m = mm;
+  if (badT) return DSPARK_ST_BAD_TEMPERATURE;
+  if (fl & 1u) return DSPARK_ST_NONFINITE;
+  if (!(fl & 2u)) return DSPARK_ST_ZERO_MASS;
+  return DSPARK_ST_OK;
+}
+
+// floor(2048 r) of an exact split (r = rnum / 2^t)
+__device__ __forceinline__ uint32_t bin_of(const AllocSplit& a) {
+  if (a.rnum == 0ull) return 0u;
+  return (uint32_t)(a.t >= 11 ? (a.rnum >> (a.t - 11)) : (a.rnum << (11 - a.t)));
+}
+
+__device__ __forceinline__ AllocSplit split_of(float y, float m, uint64_t mk, int ek) {
+  uint32_t Ei;
+  int se;
+  weight_split_ef(weight40(__fsub_rn(y, m)), &Ei, &se);
+  return alloc_split(Ei, se, mk, ek);
+}
+
+__global__ void __launch_bounds__(kTpThr) tp_max_kernel(TpParams p) {
+  __shared__ TpShared sh;
+  const Shard d = shard_of(p);
+  bool badT;
+  const float invT = inv_temp(p, d.row, &badT);
+  float mx = -INFINITY;
+  uint32_t fl = 0;
+  if (!badT)
+    for (int v = d.lo + threadIdx.x; v < d.hi; v += kTpThr) {
+      const char* xrow = reinterpret_cast<const char*>(p.x) +
+                         (int64_t)d.row * p.ld * (p.dtype == DSPARK_F32 ? 4 : 2);
+      const float x = load_logit(xrow, p.dtype, v);
+      if (!(x < INFINITY)) fl |= 1u;  // NaN or +inf
+      const float y = invT == 1.0f ? x : __fmul_rn(x, invT);
+      if (fabsf(y) == INFINITY && fabsf(x) < INFINITY) fl |= 1u;  // overflow
+      if (y > -INFINITY && y < INFINITY) {
+        fl |= 2u;
+        mx = fmaxf(mx, y);
+      }
+    }
+  mx = block_reduce(mx, OpMaxNaNTp(), sh.rf);
+  fl = block_reduce(fl, OpOrU32(), sh.r32);
+  if (threadIdx.x == 0) {
+    p.ws[d.row].mx[d.s] = mx;
+    p.ws[d.row].fl[d.s] = fl;
+  }
+}
+
+__global__ void __launch_bounds__(kTpThr) tp_weights_kernel(TpParams p) {
+  __shared__ TpShared sh;
+  const Shard d = shard_of(p);
+  const TpRow& w = p.ws[d.row];
+  bool badT;
+  const float invT = inv_temp(p, d.row, &badT);
+  float m;
+  const int st = row_state(p, w, badT, &m);
+  uint64_t S = 0;
+  if (st == DSPARK_ST_OK)
+    for (int v = d.lo + threadIdx.x; v < d.hi; v += kTpThr)
+      S += __float2ull_rz(weight40(__fsub_rn(y_of(p, d.row, v, invT), m)));
+  S = block_reduce(S, OpAddU64(), sh.r64);
+  if (threadIdx.x == 0) p.ws[d.row].S[d.s] = S;
+}
+
+__global__ void __launch_bounds__(kTpThr) tp_floors_kernel(TpParams p) {
+  __shared__ TpShared sh;
+  const Shard d = shard_of(p);
+  TpRow& w = p.ws[d.row];
+  bool badT;
+  const float invT = inv_temp(p, d.row, &badT);
+  float m;
+  const int st = row_state(p, w, badT, &m);
+  for (int i = threadIdx.x; i < kTpBins; i += kTpThr) sh.hist[i] = 0u;
+  __syncthreads();
+  uint64_t F = 0;
+  uint32_t npos = 0;
+  if (st == DSPARK_ST_OK) {
+    uint64_t S = 0;
+    for (int s = 0; s < p.n_sh; ++s) S += w.S[s];
+    const AllocScale k = alloc_scale(S);
+    for (int v = d.lo + threadIdx.x; v < d.hi; v += kTpThr) {
+      const AllocSplit a = split_of(y_of(p, d.row, v, invT), m, k.mk, k.ek);
+      p.counts[(int64_t)d.row * p.V + v] = a.f;
+      F += a.f;
+      if (a.rnum != 0ull) {
+        ++npos;
+        atomicAdd(&sh.hist[bin_of(a)], 1u);
+      }
+    }
+  }
+  F = block_reduce(F, OpAddU64(), sh.r64);
+  npos = block_reduce(npos, OpAddU32(), sh.r32);
+  for (int i = threadIdx.x; i < kTpBins; i += kTpThr) w.hist[d.s][i] = sh.hist[i];
+  for (int i = threadIdx.x; i < kTpTab; i += kTpThr) {
+    w.tab_key[d.s][i] = kTpEmpty;
+    w.tab_cnt[d.s][i] = 0u;
+  }
+  if (threadIdx.x == 0) {
+    w.F[d.s] = F;
+    w.npos[d.s] = npos;
+    w.over[d.s] = 0u;
+  }
+}
+
+// The threshold bin and the tickets granted inside it, from every rank's
+// partials (each rank computes the same values).
+__device__ __forceinline__ int grant_state(const TpParams& p, const TpRow& w, int st,
+                                           uint32_t* R, int* bstar, uint32_t* Rin) {
+  *R = 0;
+  *bstar = -1;
+  *Rin = 0;
+  if (st != DSPARK_ST_OK) return st;
+  uint64_t F = 0, npos = 0;
+  for (int s = 0; s < p.n_sh; ++s) {
+    F += w.F[s];
+    npos += w.npos[s];
+  }
+  if (F == 0 || F > (uint64_t)kM || (uint64_t)kM - F > npos) return DSPARK_ST_ALLOC_INCONSISTENT;
+  *R = (uint32_t)((uint64_t)kM - F);
+  if (*R == 0) return st;
+  uint32_t above = 0;
+  for (int b = kTpBins - 1; b >= 0; --b) {
+    uint32_t c = 0;
+    for (int s = 0; s < p.n_sh; ++s) c += w.hist[s][b];
+    if (above + c >= *R) {
+      *bstar = b;
+      *Rin = *R - above;
+      break;
+    }
+    above += c;
+  }
+  return st;
+}
+
+__global__ void __launch_bounds__(kTpThr) tp_grant_kernel(TpParams p) {
+  const Shard d = shard_of(p);
+  TpRow& w = p.ws[d.row];
+  bool badT;
+  const float invT = inv_temp(p, d.row, &badT);
+  float m;
+  int st = row_state(p, w, badT, &m);
+  uint32_t R, Rin;
+  int bstar;
+  st = grant_state(p, w, st, &R, &bstar, &Rin);
+  if (st != DSPARK_ST_OK || R == 0) return;
+  uint64_t S = 0;
+  for (int s = 0; s < p.n_sh; ++s) S += w.S[s];
+  const AllocScale k = alloc_scale(S);
+  for (int v = d.lo + threadIdx.x; v < d.hi; v += kTpThr) {
+    const AllocSplit a = split_of(y_of(p, d.row, v, invT), m, k.mk, k.ek);
+    if (a.rnum == 0ull) continue;
+    const int b = (int)bin_of(a);
+    if (b > bstar) {
+      p.counts[(int64_t)d.row * p.V + v] = a.f + 1u;
+    } else if (b == bstar) {
+      p.counts[(int64_t)d.row * p.V + v] = a.f | kTpMark;
+      // count the fraction in the shard's table (open addressing)
+      const uint64_t key = frac_key(a);
+      uint32_t h = (uint32_t)((key * 0x9E3779B97F4A7C15ull) >> 54) & (kTpTab - 1);
+      bool done = false;
+      for (int probe = 0; probe < kTpTab && !done; ++probe) {
+        unsigned long long* slot =
+            reinterpret_cast<unsigned long long*>(&w.tab_key[d.s][(h + probe) & (kTpTab - 1)]);
+        const unsigned long long prev = atomicCAS(slot, (unsigned long long)kTpEmpty, key);
+        if (prev == kTpEmpty || prev == key) {
+          atomicAdd(&w.tab_cnt[d.s][(h + probe) & (kTpTab - 1)], 1u);
+          done = true;
+        }
+      }
+      if (!done) w.over[d.s] = 1u;
+    }
+  }
+}
+
+// The leader of each row: merges the ranks' tables into the threshold
+// fraction T and each rank's quota of members at T, writes the status (and
+// zeroes a refused row).
+__global__ void __launch_bounds__(kTpThr) tp_threshold_kernel(TpParams p) {
+  __shared__ TpShared sh;
+  const int row = blockIdx.x;
+  TpRow& w = p.ws[row];
+  bool badT;
+  inv_temp(p, row, &badT);
+  float m;
+  int st = row_state(p, w, badT, &m);
+  uint32_t R, Rin;
+  int bstar;
+  st = grant_state(p, w, st, &R, &bstar, &Rin);
+  bool over = false;
+  for (int s = 0; s < p.n_sh; ++s) over |= w.over[s] != 0u;
+  if (st == DSPARK_ST_OK && R > 0 && over) st = DSPARK_ST_INTERNAL;
+  __shared__ uint64_t keys[kTpTab];
+  __shared__ uint32_t cnts[kTpTab];
+  __shared__ uint32_t nk;
+  __shared__ uint64_t Tsh;
+  if (threadIdx.x == 0) {
+    nk = 0u;
+    Tsh = kTpEmpty;
+    sh.found = -1;
+  }
+  __syncthreads();
+  if (st == DSPARK_ST_OK && R > 0) {
+    // the ranks' non-empty slots, gathered (a fraction held by several
+    // ranks keeps one slot per rank; the counts still add up)
+    const int n = p.n_sh * kTpTab;
+    for (int i = threadIdx.x; i < n; i += kTpThr) {
+      const uint64_t ki = w.tab_key[i / kTpTab][i % kTpTab];
+      if (ki == kTpEmpty) continue;
+      const uint32_t j = atomicAdd(&nk, 1u);
+      if (j < (uint32_t)kTpTab) {
+        keys[j] = ki;
+        cnts[j] = w.tab_cnt[i / kTpTab][i % kTpTab];
+      }
+    }
+    __syncthreads();
+    if (nk > (uint32_t)kTpTab) {
+      st = DSPARK_ST_INTERNAL;  // more distinct fractions than the gather holds
+    } else {
+      // T: the fraction with (members above it) < Rin <= (members at or above it)
+      for (uint32_t i = threadIdx.x; i < nk; i += kTpThr) {
+        const uint64_t ki = keys[i];
+        uint64_t above = 0, at = 0;
+        for (uint32_t j = 0; j < nk; ++j) {
+          if (keys[j] > ki) above += cnts[j];
+          else if (keys[j] == ki) at += cnts[j];
+        }
+        if (above < Rin && Rin <= above + at) {
+          Tsh = ki;  // every slot holding T writes the same values
+          sh.found = (int)(Rin - above);
+        }
+      }
+      __syncthreads();
+      if (sh.found < 0) st = DSPARK_ST_INTERNAL;  // the tables miss members of the bin
+    }
+  }
+  if (threadIdx.x == 0) {
+    // each rank's quota of members at T, ranks in id order
+    uint32_t need = st == DSPARK_ST_OK && R > 0 ? (uint32_t)sh.found : 0u;
+    for (int s = 0; s < p.n_sh; ++s) {
+      uint32_t at_s = 0;
+      if (need > 0u)
+        for (int j = 0; j < kTpTab; ++j)
+          if (w.tab_key[s][j] == Tsh) at_s += w.tab_cnt[s][j];
+      const uint32_t q = min(need, at_s);
+      w.quota[s] = q;
+      need -= q;
+    }
+    w.T = st == DSPARK_ST_OK ? Tsh : kTpEmpty;
+  }
+  if (st != DSPARK_ST_OK)
+    for (int v = threadIdx.x; v < p.V; v += kTpThr) p.counts[(int64_t)row * p.V + v] = 0u;
+  if (threadIdx.x == 0) {
+    w.st = st;
+    p.status[row] = st;
+    if (p.tokens && st != DSPARK_ST_OK) p.tokens[row] = -1;
+  }
+}
+
+// Each rank grants its marked members above T, and its quota of members at
+// T to its lowest ids (an id-ordered block scan), and sums its counts.
+__global__ void __launch_bounds__(kTpThr) tp_ties_kernel(TpParams p) {
+  __shared__ TpShared sh;
+  const Shard d = shard_of(p);
+  TpRow& w = p.ws[d.row];
+  uint64_t C = 0;
+  if (w.st == DSPARK_ST_OK) {
+    bool badT;
+    const float invT = inv_temp(p, d.row, &badT);
+    float m;
+    row_state(p, w, badT, &m);
+    uint64_t S = 0;
+    for (int s = 0; s < p.n_sh; ++s) S += w.S[s];
+    const AllocScale k = alloc_scale(S);
+    const uint64_t T = w.T;
+    const uint32_t quota = w.quota[d.s];
+    uint32_t* crow = p.counts + (int64_t)d.row * p.V;
+    uint32_t base = 0;  // members at T in this shard with a lower id
+    for (int v0 = d.lo; v0 < d.hi; v0 += kTpThr) {
+      const int v = v0 + threadIdx.x;
+      uint32_t c = v < d.hi ? crow[v] : 0u;
+      const bool marked = (c & kTpMark) != 0u;
+      uint32_t at = 0;
+      if (marked) {
+        c &= ~kTpMark;
+        const uint64_t key = frac_key(split_of(y_of(p, d.row, v, invT), m, k.mk, k.ek));
+        if (key > T) c += 1u;
+        else if (key == T) at = 1u;
+      }
+      if (quota > 0u) {  // uniform over the block
+        uint32_t tot;
+        const uint32_t incl = block_inclusive_scan(at, sh.r32, &tot);
+        if (at && base + incl - 1u < quota) c += 1u;
+        base += tot;
+        __syncthreads();
+      }
+      if (marked) crow[v] = c;
+      C += c;
+    }
+  }
+  C = block_reduce(C, OpAddU64(), sh.r64);
+  if (threadIdx.x == 0) w.C[d.s] = C;
+}
+
+// The leader's draw picks the shard by the count totals; that rank finds the
+// token (the first id whose cumulative count exceeds the draw).
+__global__ void __launch_bounds__(kTpThr) tp_draw_kernel(TpParams p) {
+  __shared__ TpShared sh;
+  const Shard d = shard_of(p);
+  if (p.status[d.row] != DSPARK_ST_OK) return;
+  const TpRow& w = p.ws[d.row];
+  uint64_t before = 0;
+  for (int s = 0; s < d.s; ++s) before += w.C[s];
+  const int b = d.row / p.depth, j = d.row % p.depth;
+  const uint32_t req = p.request_ids ? p.request_ids[b] : (uint32_t)b;
+  const uint64_t D = draw_u32(p.seed, req, (uint32_t)j, DSPARK_PURPOSE_PROPOSAL) >> 8;
+  if (!(D >= before && D - before < w.C[d.s])) return;
+  const uint64_t t = D - before;
+  // block scan over the shard, 256 ids at a time
+  uint64_t base = 0;
+  for (int v0 = d.lo; v0 < d.hi; v0 += kTpThr) {
+    const int v = v0 + threadIdx.x;
+    const uint32_t c = v < d.hi ? p.counts[(int64_t)d.row * p.V + v] : 0u;
+    uint32_t tot;
+    const uint32_t incl = block_inclusive_scan(c, sh.r32, &tot);
+    if (c > 0u && base + incl > t && base + incl - c <= t) p.tokens[d.row] = v;
+    base += tot;
+    __syncthreads();
+    if (base > t) break;
+  }
+}
+
+}  // namespace
+
+int64_t q_sharded_workspace_bytes(int n_rows) { return (int64_t)n_rows * sizeof(TpRow); }
+
+cudaError_t launch_q_sharded(const void* x, int dtype, int64_t ld, int B, int depth, int V,
+                             int n_sh, const float* temperature, uint64_t seed,
+                             const uint32_t* request_ids, uint32_t* counts, int32_t* tokens,
+                             int32_t* status, void* workspace, cudaStream_t stream) {
+  TpParams p{x,     dtype,       ld,     V,      n_sh,   depth,
+             temperature, seed, request_ids, counts, tokens, status,
+             static_cast<TpRow*>(workspace)};
+  const int rows = B * depth;
+  const int units = rows * n_sh;
+  tp_max_kernel<<<units, kTpThr, 0, stream>>>(p);
+  tp_weights_kernel<<<units, kTpThr, 0, stream>>>(p);
+  tp_floors_kernel<<<units, kTpThr, 0, stream>>>(p);
+  tp_grant_kernel<<<units, kTpThr, 0, stream>>>(p);
+  tp_threshold_kernel<<<rows, kTpThr, 0, stream>>>(p);
+  tp_ties_kernel<<<units, kTpThr, 0, stream>>>(p);
+  if (tokens) tp_draw_kernel<<<units, kTpThr, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace dspark

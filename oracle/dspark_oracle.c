@@ -893,3 +893,300 @@ int oracle_q_chain_request(const float* x, int64_t ld, int32_t V, int32_t depth,
     free(z);
     return OR_OK;
 }
+
+/* =========================================================================
+ * Vocabulary-sharded emulator ("PP1 q transport and scheduling design",
+ * Sparse support and vocabulary-sharded TP2 follow-up): the vocabulary is
+ * split into n_sh contiguous shards [s*Vs, min(V, (s+1)*Vs)), Vs =
+ * ceil(V / n_sh), and every step that needs the whole row is an explicit
+ * exchange of per-shard partials:
+ *   - dense q: all-reduce max, all-reduce the uint64 weight sums and the
+ *     floor sums, then the remaining tickets granted globally: each shard
+ *     offers its own R best remainders (remainder desc, id asc), the leader
+ *     merges them and the R best win;
+ *   - top-k q: each shard's local top-k (y desc, id asc), the leader merges
+ *     the at most n_sh * k candidates into the global top-k and allocates on
+ *     that support;
+ *   - draw: the leader's one 24-bit draw selects the shard by the shards'
+ *     count totals, and the shard picks the token inside;
+ *   - ratio verification: all-reduce of (max, shifted sum) for p, p(x) from
+ *     the shard owning x, the test at the leader; the residual draw selects
+ *     the shard by the shards' residual masses, then the token inside.
+ * Its integer outputs equal those of the unsharded functions (the tests pin
+ * that); only p's rounding order differs.
+ * ========================================================================= */
+typedef struct { double r; int32_t id; } or_rem;
+
+static int or_rem_before(const or_rem* a, const or_rem* b)
+{
+    return a->r > b->r || (a->r == b->r && a->id < b->id);
+}
+
+static int or_cmp_rem_sh(const void* a, const void* b)
+{
+    const or_rem* u = (const or_rem*)a;
+    const or_rem* v = (const or_rem*)b;
+    return or_rem_before(u, v) ? -1 : (or_rem_before(v, u) ? 1 : 0);
+}
+
+/* One draft row, dense (top_k == 0) or top-k, counts into dense[V]. */
+int oracle_q_build_row_sharded(const float* x, int32_t V, float T, int32_t top_k,
+                               int32_t n_sh, uint32_t* dense)
+{
+    memset(dense, 0, sizeof(uint32_t) * (size_t)V);
+    if (!(isfinite(T) && T > 0.0f)) return OR_BAD_TEMPERATURE;
+    float invT = 1.0f / T;
+    if (!(isfinite(invT) && invT >= 0x1p-126f)) return OR_BAD_TEMPERATURE;
+    const int32_t Vs = (V + n_sh - 1) / n_sh;
+    float* y = (float*)malloc(sizeof(float) * (size_t)V);
+    uint8_t* sup = (uint8_t*)calloc((size_t)V, 1);
+    if (!y || !sup) { free(y); free(sup); return -1; }
+    int st = OR_OK;
+    /* per shard: validate and scale; then the all-reduce of "any finite" */
+    int32_t n_finite = 0;
+    for (int32_t s = 0; s < n_sh && st == OR_OK; ++s) {
+        for (int32_t v = s * Vs; v < V && v < (s + 1) * Vs; ++v) {
+            float xv = x[v];
+            if (isnan(xv) || xv == INFINITY) { st = OR_NONFINITE; break; }
+            y[v] = xv * invT;
+            if (isfinite(xv) && !isfinite(y[v])) { st = OR_NONFINITE; break; }
+            if (y[v] > -INFINITY) ++n_finite;
+        }
+    }
+    if (st == OR_OK && n_finite == 0) st = OR_ZERO_MASS;
+    if (st != OR_OK) { free(y); free(sup); return st; }
+
+    /* support: all finite (dense), or the merge of the shards' local top-k */
+    if (top_k > 0 && top_k < n_finite) {
+        or_yid* cand = (or_yid*)malloc(sizeof(or_yid) * (size_t)(n_sh * top_k + 1));
+        or_yid* loc = (or_yid*)malloc(sizeof(or_yid) * (size_t)(Vs + 1));
+        int32_t nc = 0;
+        for (int32_t s = 0; s < n_sh; ++s) {
+            int32_t nl = 0;
+            for (int32_t v = s * Vs; v < V && v < (s + 1) * Vs; ++v)
+                if (y[v] > -INFINITY) { loc[nl].y = y[v]; loc[nl].id = v; ++nl; }
+            qsort(loc, (size_t)nl, sizeof(or_yid), or_cmp_topk);
+            for (int32_t i = 0; i < nl && i < top_k; ++i) cand[nc++] = loc[i];
+        }
+        qsort(cand, (size_t)nc, sizeof(or_yid), or_cmp_topk);       /* leader merge */
+        for (int32_t i = 0; i < top_k; ++i) sup[cand[i].id] = 1;
+        free(cand);
+        free(loc);
+    } else {
+        for (int32_t v = 0; v < V; ++v) sup[v] = (y[v] > -INFINITY);
+    }
+    /* all-reduce max over the support */
+    float m = -INFINITY;
+    for (int32_t s = 0; s < n_sh; ++s) {
+        float ms = -INFINITY;
+        for (int32_t v = s * Vs; v < V && v < (s + 1) * Vs; ++v) if (sup[v] && y[v] > ms) ms = y[v];
+        if (ms > m) m = ms;
+    }
+    /* per shard E and uint64 sums; all-reduce */
+    uint64_t* E = (uint64_t*)calloc((size_t)V, sizeof(uint64_t));
+    uint64_t S = 0;
+    for (int32_t s = 0; s < n_sh; ++s) {
+        uint64_t Ss = 0;
+        for (int32_t v = s * Vs; v < V && v < (s + 1) * Vs; ++v) {
+            if (!sup[v]) continue;
+            float e = oracle_exp_ds(y[v] - m);
+            E[v] = (uint64_t)floor((double)e * 1099511627776.0);
+            Ss += E[v];
+        }
+        S += Ss;
+    }
+    /* floors per shard, all-reduce F; then the global remaining-ticket grant */
+    double k = 16777216.0 / (double)S;
+    uint64_t F = 0;
+    int32_t npos = 0;
+    double* r = (double*)calloc((size_t)V, sizeof(double));
+    for (int32_t v = 0; v < V; ++v) {
+        if (!sup[v]) continue;
+        double a = (double)E[v] * k;
+        double f = floor(a);
+        dense[v] = (uint32_t)f;
+        r[v] = a - f;
+        F += (uint64_t)f;
+        if (r[v] > 0.0) ++npos;
+    }
+    if (F > (uint64_t)OR_M || (uint64_t)OR_M - F >= (uint64_t)OR_M ||
+        (uint64_t)OR_M - F > (uint64_t)npos) {
+        st = OR_ALLOC_INCONSISTENT;
+    } else {
+        const int64_t R = (int64_t)OR_M - (int64_t)F;
+        or_rem* offers = (or_rem*)malloc(sizeof(or_rem) * (size_t)(n_sh * (R + 1) + 1));
+        or_rem* loc = (or_rem*)malloc(sizeof(or_rem) * (size_t)(Vs + 1));
+        int64_t no = 0;
+        for (int32_t s = 0; s < n_sh; ++s) {
+            int32_t nl = 0;
+            for (int32_t v = s * Vs; v < V && v < (s + 1) * Vs; ++v)
+                if (sup[v]) { loc[nl].r = r[v]; loc[nl].id = v; ++nl; }
+            qsort(loc, (size_t)nl, sizeof(or_rem), or_cmp_rem_sh);
+            for (int64_t i = 0; i < nl && i < R; ++i) offers[no++] = loc[i];
+        }
+        qsort(offers, (size_t)no, sizeof(or_rem), or_cmp_rem_sh);
+        for (int64_t i = 0; i < R; ++i) dense[offers[i].id] += 1u;
+        free(offers);
+        free(loc);
+        uint64_t total = 0;
+        for (int32_t v = 0; v < V; ++v) total += dense[v];
+        if (total != (uint64_t)OR_M) st = OR_ALLOC_INCONSISTENT;
+    }
+    if (st != OR_OK) memset(dense, 0, sizeof(uint32_t) * (size_t)V);
+    free(y); free(sup); free(E); free(r);
+    return st;
+}
+
+/* The draw over dense counts: the shard by the shards' count totals, then the
+ * token inside it. */
+int32_t oracle_draw_sharded(const uint32_t* counts, int32_t V, int32_t n_sh, uint32_t D)
+{
+    const int32_t Vs = (V + n_sh - 1) / n_sh;
+    uint64_t before = 0;
+    for (int32_t s = 0; s < n_sh; ++s) {
+        uint64_t Cs = 0;
+        for (int32_t v = s * Vs; v < V && v < (s + 1) * Vs; ++v) Cs += counts[v];
+        if ((uint64_t)D < before + Cs) {
+            uint64_t cum = before;
+            for (int32_t v = s * Vs; v < V && v < (s + 1) * Vs; ++v) {
+                cum += counts[v];
+                if (cum > (uint64_t)D) return v;
+            }
+        }
+        before += Cs;
+    }
+    return -1;
+}
+
+/* Target p of one row from the shards' (max, shifted sum) partials. */
+static int or_target_row_sharded(const float* z, int32_t V, int32_t n_sh, double* p)
+{
+    const int32_t Vs = (V + n_sh - 1) / n_sh;
+    double M = -INFINITY;
+    double* ms = (double*)malloc(sizeof(double) * (size_t)n_sh * 2);
+    double* ss = ms + n_sh;
+    for (int32_t s = 0; s < n_sh; ++s) {
+        float m = -INFINITY;
+        for (int32_t v = s * Vs; v < V && v < (s + 1) * Vs; ++v) {
+            if (isnan(z[v]) || z[v] == INFINITY) { free(ms); return OR_NONFINITE; }
+            if (z[v] > m) m = z[v];
+        }
+        double sum = 0.0;
+        for (int32_t v = s * Vs; v < V && v < (s + 1) * Vs; ++v)
+            if (z[v] > -INFINITY) sum += exp((double)z[v] - (double)m);
+        ms[s] = m;
+        ss[s] = sum;
+        if (m > M) M = m;
+    }
+    if (M == -INFINITY) { free(ms); return OR_ZERO_MASS; }
+    double Z = 0.0;
+    for (int32_t s = 0; s < n_sh; ++s)
+        if (ms[s] > -INFINITY) Z += ss[s] * exp(ms[s] - M);
+    for (int32_t v = 0; v < V; ++v)
+        p[v] = (z[v] == -INFINITY) ? 0.0 : exp((double)z[v] - M) / Z;
+    free(ms);
+    return OR_OK;
+}
+
+/* Residual (or bonus) draw: the shard by the shards' residual masses, then the
+ * token inside; flags as in oracle_residual_pick. */
+static int32_t or_residual_pick_sharded(const double* p, const uint32_t* c, int32_t V,
+                                        int32_t n_sh, uint32_t w, uint32_t* flags)
+{
+    const int32_t Vs = (V + n_sh - 1) / n_sh;
+    double* r = (double*)malloc(sizeof(double) * (size_t)V);
+    double* Zs = (double*)calloc((size_t)n_sh, sizeof(double));
+    double Z = 0.0;
+    int degenerate = 0;
+    for (int pass = 0; pass < 2; ++pass) {
+        Z = 0.0;
+        for (int32_t s = 0; s < n_sh; ++s) {
+            Zs[s] = 0.0;
+            for (int32_t v = s * Vs; v < V && v < (s + 1) * Vs; ++v) {
+                double q = (c && !degenerate) ? (double)c[v] / 16777216.0 : 0.0;
+                double rv = p[v] - q;
+                r[v] = rv > 0.0 ? rv : 0.0;
+                Zs[s] += r[v];
+            }
+            Z += Zs[s];
+        }
+        if (Z > 0.0 || !c || degenerate) break;
+        degenerate = 1;
+        if (flags) *flags |= OR_FLAG_DEGENERATE;
+    }
+    double t = ((double)w * 0x1p-32) * Z;
+    int32_t pick = -1, last_pos = -1;
+    double before = 0.0, cum = 0.0, prev = 0.0;
+    for (int32_t s = 0; s < n_sh && pick < 0; ++s) {
+        if (t < before + Zs[s] || s == n_sh - 1) {
+            cum = before;
+            for (int32_t v = s * Vs; v < V && v < (s + 1) * Vs; ++v) {
+                if (r[v] > 0.0) last_pos = v;
+                prev = cum;
+                cum += r[v];
+                if (cum > t) { pick = v; break; }
+            }
+        }
+        before += Zs[s];
+    }
+    if (pick < 0) {
+        for (int32_t v = V - 1; v >= 0; --v) if (r[v] > 0.0) { last_pos = v; break; }
+        pick = last_pos;
+        prev = cum - (last_pos >= 0 ? r[last_pos] : 0.0);
+    }
+    if (flags && (fabs(t - prev) <= 1e-6 || fabs(cum - t) <= 1e-6))
+        *flags |= OR_FLAG_NEAR_BOUNDARY;
+    free(r);
+    free(Zs);
+    return pick;
+}
+
+/* Ratio verification of one request with dense q, sharded. */
+int oracle_verify_ratio_req_sharded(const float* z, int64_t ld, int32_t V, int32_t depth,
+                                    const int32_t* drafts, const uint32_t* counts,
+                                    int32_t n_sh, uint64_t seed, uint32_t request,
+                                    int32_t* accept_len, int32_t* committed, uint32_t* flags)
+{
+    uint32_t fl = 0;
+    or_discard(depth, accept_len, committed);
+    if (flags) *flags = 0;
+    for (int32_t j = 0; j < depth; ++j)
+        if (drafts[j] < 0 || drafts[j] >= V) return OR_BAD_DRAFT;
+    double* p = (double*)malloc(sizeof(double) * (size_t)V);
+    int st = OR_OK;
+    int32_t L = depth, pick = -1;
+    for (int32_t j = 0; j < depth; ++j) {
+        st = or_target_row_sharded(z + (int64_t)j * ld, V, n_sh, p);
+        if (st != OR_OK) goto done;
+        const uint32_t* q = counts + (int64_t)j * V;
+        uint32_t c = q[drafts[j]];
+        if (c == 0) { st = OR_BAD_DRAFT; goto done; }
+        uint32_t U = oracle_draw_u32(seed, request, (uint32_t)j, OR_PURPOSE_ACCEPT) >> 8;
+        double pj = p[drafts[j]];
+        double uq = (double)((uint64_t)U * (uint64_t)c) * 0x1p-48;
+        if (fabs(uq - pj) <= 1e-6 * ((double)c * 0x1p-24)) fl |= OR_FLAG_AMBIG_ACCEPT;
+        if (!oracle_ratio_accept(U, c, pj)) {
+            L = j;
+            uint64_t total = 0;
+            for (int32_t v = 0; v < V; ++v) total += q[v];
+            if (total != (uint64_t)OR_M) { st = OR_BAD_Q; goto done; }
+            uint32_t w = oracle_draw_u32(seed, request, (uint32_t)j, OR_PURPOSE_RESIDUAL);
+            pick = or_residual_pick_sharded(p, q, V, n_sh, w, &fl);
+            break;
+        }
+    }
+    if (L == depth) {
+        st = or_target_row_sharded(z + (int64_t)depth * ld, V, n_sh, p);
+        if (st != OR_OK) goto done;
+        uint32_t w = oracle_draw_u32(seed, request, (uint32_t)depth, OR_PURPOSE_BONUS);
+        pick = or_residual_pick_sharded(p, NULL, V, n_sh, w, &fl);
+    }
+    *accept_len = L;
+    for (int32_t i = 0; i < L; ++i) committed[i] = drafts[i];
+    committed[L] = pick;
+done:
+    if (st != OR_OK) { or_discard(depth, accept_len, committed); fl = 0; }
+    if (flags) *flags = fl;
+    free(p);
+    return st;
+}

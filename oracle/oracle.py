@@ -76,6 +76,10 @@ def lib():
                                                            _P, _P, _P]),
                 "oracle_q_chain_request": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, _P, _I64, _I32,
                                                           _I32, _U64, _U32, _P, _P, _P, _P]),
+                "oracle_q_build_row_sharded": (ctypes.c_int, [_P, _I32, _F32, _I32, _I32, _P]),
+                "oracle_draw_sharded": (_I32, [_P, _I32, _I32, _U32]),
+                "oracle_verify_ratio_req_sharded": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, _P,
+                                                                   _I32, _U64, _U32, _P, _P, _P]),
                 "oracle_fletcher64": (_U64, [_P, _I64]),
                 "oracle_q_pack_row": (_U64, [_P, _P, _I32, _I32, _I32, _P]),
                 "oracle_q_validate_row": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, ctypes.c_int,
@@ -376,3 +380,51 @@ def q_chain(x, temperature, bias, anchors, seed, request_ids=None):
                                      int(anchors[r]), seed, int(req[r]), _ptr(counts[r]),
                                      _ptr(tokens[r]), _ptr(status[r]), _ptr(margins[r]))
     return counts.reshape(B * depth, V), tokens, status.reshape(-1), margins
+
+
+# ------------------------------------------------- vocabulary-sharded emulator
+def q_build_sharded(x, n_shards, temperature=None, top_k=0):
+    """Dense counts [n_rows, V] and status from the sharded emulator."""
+    x = _c(x, np.float32)
+    n_rows, V = x.shape
+    t = np.ones(n_rows, np.float32) if temperature is None else _c(
+        np.broadcast_to(temperature, (n_rows,)), np.float32)
+    counts = np.zeros((n_rows, V), np.uint32)
+    st = np.zeros(n_rows, np.int32)
+    for r in range(n_rows):
+        cr = np.zeros(V, np.uint32)
+        st[r] = lib().oracle_q_build_row_sharded(_ptr(x[r]), V, float(t[r]), top_k, n_shards,
+                                                 _ptr(cr))
+        counts[r] = cr
+    return counts, st
+
+
+def draw_sharded(counts_row, n_shards, D):
+    c = _c(counts_row, np.uint32)
+    return int(lib().oracle_draw_sharded(_ptr(c), c.size, n_shards, int(D)))
+
+
+def verify_ratio_sharded(z, drafts, counts, n_shards, seed, request_ids=None):
+    z = _c(z, np.float32)
+    drafts = _c(drafts, np.int32)
+    counts = _c(counts, np.uint32)
+    B, rows, V = z.shape
+    depth = rows - 1
+    req = np.arange(B, dtype=np.uint32) if request_ids is None else _c(request_ids, np.uint32)
+    acc = np.zeros(B, np.int32)
+    com = np.full((B, depth + 1), -1, np.int32)
+    flags = np.zeros(B, np.uint32)
+    status = np.zeros(B, np.int32)
+    a = ctypes.c_int32(0)
+    fl = ctypes.c_uint32(0)
+    for b in range(B):
+        cm = np.zeros(depth + 1, np.int32)
+        cb = counts.reshape(B, depth, V)[b]
+        status[b] = lib().oracle_verify_ratio_req_sharded(_ptr(z[b]), V, V, depth, _ptr(drafts[b]),
+                                                          _ptr(cb), n_shards, seed, int(req[b]),
+                                                          ctypes.byref(a), _ptr(cm),
+                                                          ctypes.byref(fl))
+        acc[b] = a.value
+        com[b] = cm
+        flags[b] = fl.value
+    return acc, com, flags, status
