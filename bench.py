@@ -463,17 +463,17 @@ def run_ours(args, rank, world, local_rank):
                  "bytes": rows_d * V * (wl.draft.itemsize + 4 + 4)}
 
     # ---- the vocabulary-sharded q build and draw (two emulated ranks) on
-    #      this step's draft rows (dense q), timed apart from the step
+    #      this step's draft rows, timed apart from the step
     sharded = None
-    if not args.no_sharded and top_k == 0:
+    if not args.no_sharded:
         sws = torch.empty((ds.dspark_q_sharded_workspace_bytes(rows_d),), dtype=torch.uint8,
                           device=dev)
         stok = torch.empty((B, depth), dtype=torch.int32, device=dev)
         sst2 = torch.empty((rows_d,), dtype=torch.int32, device=dev)
 
         def sharded_step():
-            ds.dspark_q_build_sample_sharded(xd, B, depth, 2, temps, wl.seed, req, counts, stok,
-                                             sst2, sws, stream)
+            ds.dspark_q_build_sample_sharded(xd, B, depth, 2, temps, top_k, wl.seed, req, counts,
+                                             ids, nnz, stok, sst2, sws, stream)
 
         for _ in range(max(3, args.warmup)):
             sharded_step()

@@ -215,16 +215,16 @@ def dspark_q_sharded_workspace_bytes(n_rows):
     return int(_lib.load().dspark_q_sharded_workspace_bytes(int(n_rows)))
 
 
-def dspark_q_build_sample_sharded(draft_logits, B, depth, n_shards, temperature, seed,
-                                  request_ids, counts, draft_tokens, row_status, workspace,
-                                  stream=None):
+def dspark_q_build_sample_sharded(draft_logits, B, depth, n_shards, temperature, top_k, seed,
+                                  request_ids, counts, sparse_ids, nnz, draft_tokens, row_status,
+                                  workspace, stream=None):
     rows, V, ld = _rows(draft_logits)
     if rows != B * depth:
         raise ValueError("draft_logits must hold B*depth rows")
     _call("dspark_q_build_sample_sharded", _ptr(draft_logits), _dtype_code(draft_logits), ld,
-          int(B), int(depth), V, int(n_shards), _ptr(temperature), int(seed) & (2 ** 64 - 1),
-          _i32(request_ids), _i32(counts), _i32(draft_tokens), _i32(row_status), _ptr(workspace),
-          _stream(stream))
+          int(B), int(depth), V, int(n_shards), _ptr(temperature), int(top_k),
+          int(seed) & (2 ** 64 - 1), _i32(request_ids), _i32(counts), _i32(sparse_ids), _i32(nnz),
+          _i32(draft_tokens), _i32(row_status), _ptr(workspace), _stream(stream))
 
 
 def dspark_q_pack(counts, sparse_ids, nnz, top_k, V, q_out, checksum_out, stream=None):
@@ -366,18 +366,24 @@ def q_chain_sample(draft_logits, B, depth, seed, anchors, bias=None, temperature
     return q, tokens, margins
 
 
-def q_build_sample_sharded(draft_logits, B, depth, n_shards, seed, temperature=None,
+def q_build_sample_sharded(draft_logits, B, depth, n_shards, seed, temperature=None, top_k=0,
                            request_ids=None, stream=None):
-    """The vocabulary-sharded emulation of q_build_sample (dense q)."""
+    """The vocabulary-sharded emulation of q_build_sample."""
     rows, V, _ = _rows(draft_logits)
     dev = draft_logits.device
     ws = _empty((dspark_q_sharded_workspace_bytes(rows),), torch.uint8, dev)
-    counts = _empty((rows, V), torch.int32, dev)
+    if top_k > 0:
+        counts = _empty((rows, top_k), torch.int32, dev)
+        ids = _empty((rows, top_k), torch.int32, dev)
+        nnz = _empty((rows,), torch.int32, dev)
+    else:
+        counts = _empty((rows, V), torch.int32, dev)
+        ids = nnz = None
     status = _empty((rows,), torch.int32, dev)
     tokens = _empty((B, depth), torch.int32, dev)
-    dspark_q_build_sample_sharded(draft_logits, B, depth, n_shards, temperature, seed,
-                                  request_ids, counts, tokens, status, ws, stream)
-    return {"counts": counts, "ids": None, "nnz": None, "status": status, "top_k": 0}, tokens
+    dspark_q_build_sample_sharded(draft_logits, B, depth, n_shards, temperature, top_k, seed,
+                                  request_ids, counts, ids, nnz, tokens, status, ws, stream)
+    return {"counts": counts, "ids": ids, "nnz": nnz, "status": status, "top_k": top_k}, tokens
 
 
 def q_pack(q, V, stream=None):

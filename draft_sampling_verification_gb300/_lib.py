@@ -31,8 +31,8 @@ SIGNATURES = {
                       _P, _P, _P, _P, _P, _P],
     "dspark_spec_step_schedule": [_I32, _I32],
     "dspark_q_pack": [_P, _P, _P, _I32, _I32, _I32, _P, _P, _P],
-    "dspark_q_build_sample_sharded": [_P, _I32, _I64, _I32, _I32, _I32, _I32, _P, _U64, _P, _P,
-                                      _P, _P, _P, _P],
+    "dspark_q_build_sample_sharded": [_P, _I32, _I64, _I32, _I32, _I32, _I32, _P, _I32, _U64,
+                                      _P, _P, _P, _P, _P, _P, _P, _P],
     "dspark_q_chain_sample": [_P, _I32, _I64, _I32, _I32, _I32, _P, _P, _I64, _I32, _P, _U64, _P,
                               _P, _P, _P, _P, _P, _P],
     "dspark_verify_match": [_P, _I32, _I64, _I32, _I32, _I32, _P, _U64, _P, _P, _P, _P, _P, _P],

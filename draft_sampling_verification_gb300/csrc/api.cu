@@ -33,9 +33,10 @@ cudaError_t launch_verify_modes(const void* z, int dtype, int64_t ld, int B, int
 int spec_step_schedule(int B, int depth);
 int64_t q_sharded_workspace_bytes(int n_rows);
 cudaError_t launch_q_sharded(const void* x, int dtype, int64_t ld, int B, int depth, int V,
-                             int n_sh, const float* temperature, uint64_t seed,
-                             const uint32_t* request_ids, uint32_t* counts, int32_t* tokens,
-                             int32_t* status, void* workspace, cudaStream_t stream);
+                             int n_sh, const float* temperature, int top_k, uint64_t seed,
+                             const uint32_t* request_ids, uint32_t* counts, int32_t* ids,
+                             int32_t* nnz, int32_t* tokens, int32_t* status, void* workspace,
+                             cudaStream_t stream);
 cudaError_t launch_q_chain(const void* x, int dtype, int64_t ld, int B, int depth, int V,
                            const float* temperature, const float* bias, int64_t bias_ld,
                            int n_bias, const int32_t* anchors, uint64_t seed,
@@ -375,24 +376,27 @@ int64_t dspark_q_sharded_workspace_bytes(int32_t n_rows) {
 
 int dspark_q_build_sample_sharded(const void* draft_logits, int32_t dtype, int64_t ld, int32_t B,
                                   int32_t depth, int32_t V, int32_t n_shards,
-                                  const float* temperature, uint64_t seed,
+                                  const float* temperature, int32_t top_k, uint64_t seed,
                                   const uint32_t* request_ids, uint32_t* counts,
-                                  int32_t* draft_tokens, int32_t* row_status, void* workspace,
-                                  void* stream) {
+                                  int32_t* sparse_ids, int32_t* nnz, int32_t* draft_tokens,
+                                  int32_t* row_status, void* workspace, void* stream) {
   if (int e = check_common(dtype, V, ld)) return e;
+  if (int e = check_topk(top_k, V)) return e;
   if (depth < 1 || depth > DSPARK_MAX_DEPTH) return DSPARK_ERR_SIZE;
   if (B < 0 || (int64_t)B * depth * 8 > kMaxGridRows) return DSPARK_ERR_SIZE;
   if (n_shards < 1 || n_shards > 8) return DSPARK_ERR_ARG;
   if (B == 0) return 0;
   if (!draft_logits || !counts || !row_status || !workspace) return DSPARK_ERR_NULL;
+  if (top_k > 0 && (!sparse_ids || !nnz)) return DSPARK_ERR_NULL;
   if (!aligned(draft_logits, esize(dtype)) || !aligned(counts, 4) || !aligned(row_status, 4) ||
       !aligned(workspace, 16) || (draft_tokens && !aligned(draft_tokens, 4)) ||
-      (temperature && !aligned(temperature, 4)) || (request_ids && !aligned(request_ids, 4)))
+      (temperature && !aligned(temperature, 4)) || (request_ids && !aligned(request_ids, 4)) ||
+      (sparse_ids && !aligned(sparse_ids, 4)) || (nnz && !aligned(nnz, 4)))
     return DSPARK_ERR_ALIGN;
-  return launch_result(dspark::launch_q_sharded(draft_logits, dtype, ld, B, depth, V, n_shards,
-                                                temperature, seed, request_ids, counts,
-                                                draft_tokens, row_status, workspace,
-                                                static_cast<cudaStream_t>(stream)));
+  return launch_result(dspark::launch_q_sharded(
+      draft_logits, dtype, ld, B, depth, V, n_shards, temperature, top_k, seed, request_ids,
+      counts, sparse_ids, nnz, draft_tokens, row_status, workspace,
+      static_cast<cudaStream_t>(stream)));
 }
 
 int dspark_q_pack(const uint32_t* counts, const int32_t* sparse_ids, const int32_t* nnz,

@@ -30,13 +30,10 @@
 // same radix select cuts it back to the top k of the prefix.  Rows in
 // ascending order of y make every element a candidate there: correct, slow.
 //
-// The allocation then runs on the at most k survivors in FP64, as the method
-// states it: E = floor(exp_ds(y - m) * 2^40), S = sum E,
-// a = RN64(E * RN64(2^24 / RN64(S))), f = floor a, r = a - f, and the
-// R = M - sum f largest r (lowest id first) get one more ticket.  The nonzero
-// counts are written in ascending id order; the draft draw takes the first
-// id whose inclusive cumulative count exceeds the 24-bit draw.
-#include "common.cuh"
+// The allocation then runs on the at most k survivors (support_alloc.cuh):
+// FP64 as the method states it, the nonzero counts in ascending id order,
+// and the draft draw on them.
+#include "support_alloc.cuh"
 
 namespace dspark {
 namespace {
@@ -62,6 +59,8 @@ static_assert(kKWStage % 256 == 0, "whole 256-element steps");
 static_assert(kKWarps * kKWSlots * kKWStageBytes <= kKStages * kKStageBytes,
               "the warps' rings fit in the ring");
 static_assert(kKSample == 8 * kKThr && kKSample <= kKCap, "8 sample keys per thread");
+static_assert(kSupScratch <= kKStages * kKStageBytes && kKThr == kSupThr,
+              "the allocation's scratch fits in the ring");
 
 struct KParams {
   const void* x;
@@ -81,7 +80,7 @@ struct KParams {
 };
 
 struct KShared {
-  double kd;                             // RN64(2^24 / RN64(S))
+  SupShared sup;                         // the allocation on the support
   uint64_t mbar[kKStages];               // the exact streaming pass
   uint64_t wbar[kKWarps * kKWSlots];     // the warps' rings
   uint64_t red64[32];
@@ -96,7 +95,6 @@ struct KShared {
   float invT;
   int bad_T;
   int timeout;
-  int found;
 };
 
 __device__ __forceinline__ float fmax_nan(float a, float b) {
@@ -107,9 +105,6 @@ __device__ __forceinline__ float fmax_nan(float a, float b) {
 
 struct OpMaxNaN {
   __device__ float operator()(float a, float b) const { return fmax_nan(a, b); }
-};
-struct OpMaxU32 {
-  __device__ uint32_t operator()(uint32_t a, uint32_t b) const { return a > b ? a : b; }
 };
 
 // Inverse of float_key.
@@ -425,7 +420,6 @@ __global__ void __launch_bounds__(kKThr, 3) q_topk_kernel(KParams p) {
     sh.n_fin = 0u;
     sh.thr = -INFINITY;
     sh.timeout = 0;
-    sh.found = -1;
     for (int c = 0; c < kKStages; ++c) mbar_init(&sh.mbar[c], 1);
     for (int c = 0; c < kKWarps * kKWSlots; ++c) mbar_init(&sh.wbar[c], 1);
     mbar_init_fence();
@@ -587,126 +581,16 @@ __global__ void __launch_bounds__(kKThr, 3) q_topk_kernel(KParams p) {
   if (st == DSPARK_ST_OK && cnt > k) keep_top_k(cnt, k, keys, ids, tkeys, tids, sh);
   const int ns = min(cnt, k);
 
-  // ---- allocation on the support (the ring is free now).  Each support
-  //      entry is one 16-byte record {r low, r high, id, count}: the
-  //      remainder r in [0, 1) as its bit pattern (the same order as the
-  //      values, compared in integer arithmetic: FP64 compares are slow
-  //      here), read back with one 128-bit load in the quadratic loops.
-  uint4* ent = reinterpret_cast<uint4*>(ring);
-  float* e_arr = reinterpret_cast<float*>(ring + 16 * kKSupCap);
-  if (st == DSPARK_ST_OK) {
-    uint32_t mk = 0u;
-    for (int i = tid; i < ns; i += kKThr) mk = max(mk, keys[i]);
-    mk = block_reduce(mk, OpMaxU32(), sh.red32);
-    const float m = key_float(mk);
-    uint64_t S = 0;
-    for (int i = tid; i < ns; i += kKThr) {
-      const float e = weight40(__fsub_rn(key_float(keys[i]), m));
-      e_arr[i] = e;
-      S += (uint64_t)__float2ull_rz(e);
-    }
-    S = block_reduce(S, OpAddU64(), sh.red64);
-    // one FP64 division for the block (FP64 is slow here)
-    if (tid == 0) sh.kd = __ddiv_rn(16777216.0, __ull2double_rn(S));
-    __syncthreads();
-    const double kd = sh.kd;
-    uint64_t F = 0;
-    uint32_t npos = 0;
-    for (int i = tid; i < ns; i += kKThr) {
-      const double a = __dmul_rn((double)e_arr[i], kd);
-      const double f = floor(a);
-      const uint64_t rb = (uint64_t)__double_as_longlong(__dsub_rn(a, f));
-      ent[i] = make_uint4((uint32_t)rb, (uint32_t)(rb >> 32), (uint32_t)ids[i], (uint32_t)f);
-      F += (uint64_t)f;
-      npos += (rb != 0u) ? 1u : 0u;
-    }
-    F = block_reduce(F, OpAddU64(), sh.red64);
-    npos = block_reduce(npos, OpAddU32(), sh.red32);
-    if (F > (uint64_t)DSPARK_M) {
-      st = DSPARK_ST_ALLOC_INCONSISTENT;
-    } else {
-      const uint64_t R = (uint64_t)DSPARK_M - F;
-      if (R >= (uint64_t)DSPARK_M || R > (uint64_t)npos) {
-        st = DSPARK_ST_ALLOC_INCONSISTENT;
-      } else {
-        // the R largest remainders (lowest id first among equal ones):
-        // rank = the entries that come before this one
-        uint32_t grant[kKSupCap / kKThr];
-#pragma unroll
-        for (int q = 0; q < kKSupCap / kKThr; ++q) {
-          const int i = tid + q * kKThr;
-          grant[q] = 0u;
-          if (i < ns) {
-            const uint4 ei = ent[i];
-            const uint64_t ri = ((uint64_t)ei.y << 32) | ei.x;
-            uint32_t rank = 0;
-#pragma unroll 8
-            for (int j = 0; j < ns; ++j) {
-              const uint4 ej = ent[j];
-              const uint64_t rj = ((uint64_t)ej.y << 32) | ej.x;
-              rank += (uint32_t)(rj > ri) | ((uint32_t)(rj == ri) & (uint32_t)(ej.z < ei.z));
-            }
-            grant[q] = ((uint64_t)rank < R) ? 1u : 0u;
-          }
-        }
-        __syncthreads();  // every rank is taken before the counts change
-        uint64_t csum = 0;
-#pragma unroll
-        for (int q = 0; q < kKSupCap / kKThr; ++q) {
-          const int i = tid + q * kKThr;
-          if (i < ns) {
-            const uint32_t c = ent[i].w + grant[q];
-            ent[i].w = c;
-            csum += c;
-          }
-        }
-        csum = block_reduce(csum, OpAddU64(), sh.red64);
-        if (csum != (uint64_t)DSPARK_M) st = DSPARK_ST_ALLOC_INCONSISTENT;
-      }
-    }
+  // ---- allocation on the support (the ring is free now), outputs, draw
+  uint32_t D = 0;
+  if (p.tokens) {
+    const int b = row / p.depth, j = row % p.depth;
+    const uint32_t req = p.request_ids ? p.request_ids[b] : (uint32_t)b;
+    D = draw_u32(p.seed, req, (uint32_t)j, DSPARK_PURPOSE_PROPOSAL) >> 8;
   }
-
-  // ---- outputs: nonzero counts in ascending id order, the draw
-  int32_t* ids_out = p.ids + (int64_t)row * k;
-  uint32_t* cnt_out = p.counts + (int64_t)row * k;
-  uint32_t nnz = 0;
-  if (st == DSPARK_ST_OK) {
-    uint32_t D = 0;
-    if (p.tokens) {
-      const int b = row / p.depth, j = row % p.depth;
-      const uint32_t req = p.request_ids ? p.request_ids[b] : (uint32_t)b;
-      D = draw_u32(p.seed, req, (uint32_t)j, DSPARK_PURPOSE_PROPOSAL) >> 8;
-    }
-    const uint2* ic = reinterpret_cast<const uint2*>(ent);  // {id, count} at odd halves
-    for (int i = tid; i < ns; i += kKThr) {
-      const uint2 mine = ic[2 * i + 1];
-      const uint32_t c = mine.y, idi = mine.x;
-      if (c == 0u) continue;
-      nnz += 1u;
-      uint32_t pos = 0, before = 0;
-#pragma unroll 8
-      for (int j = 0; j < ns; ++j) {
-        const uint2 o = ic[2 * j + 1];
-        const uint32_t pre = (uint32_t)(o.y > 0u) & (uint32_t)(o.x < idi);
-        pos += pre;
-        before += pre ? o.y : 0u;
-      }
-      ids_out[pos] = (int32_t)idi;
-      cnt_out[pos] = c;
-      if (before <= D && D - before < c) sh.found = (int32_t)idi;
-    }
-    nnz = block_reduce(nnz, OpAddU32(), sh.red32);
-  }
-  for (int i = (int)nnz + tid; i < k; i += kKThr) {
-    ids_out[i] = -1;
-    cnt_out[i] = 0u;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    p.nnz[row] = (int32_t)nnz;
-    p.status[row] = st;
-    if (p.tokens) p.tokens[row] = (st == DSPARK_ST_OK) ? sh.found : -1;
-  }
+  support_alloc_emit(st, ns, k, keys, ids, ring, sh.sup, p.counts + (int64_t)row * k,
+                     p.ids + (int64_t)row * k, p.nnz + row, p.status + row,
+                     p.tokens ? p.tokens + row : nullptr, D);
 }
 
 }  // namespace

@@ -27,7 +27,15 @@
 //   7  the leader's draw: the shard by the count totals, the token inside
 // Floors and fractions are exact integer splits of E * RN64(2^24 / RN64(S)),
 // so the counts equal those of the unsharded build bit for bit.
-#include "common.cuh"
+//
+// Top-k rows (same follow-up: a global top-k merge of the ranks' local
+// top-k): each rank selects its local top k by (y desc, id asc) with a radix
+// select over its shard and sends those candidates; the leader merges the at
+// most n_sh * k candidates into the global top k by the same order (the
+// global top k is a subset of the union of the local ones) and allocates the
+// tickets on that support.  The leader's draw over the support in id order is
+// the draw that picks the shard by its count total, then the token inside.
+#include "support_alloc.cuh"
 
 namespace dspark {
 namespace {
@@ -48,11 +56,12 @@ struct TpRow {
   uint32_t npos[kTpMaxShards];
   uint64_t C[kTpMaxShards];
   uint32_t over[kTpMaxShards];   // the shard's table overflowed
+  uint32_t nc[kTpMaxShards];     // top-k rows: the shard's candidates
   uint32_t quota[kTpMaxShards];  // members at T granted in the shard
   uint64_t T;                    // the threshold fraction's key
   int32_t st;                    // the row's status after the grant step
   uint32_t hist[kTpMaxShards][kTpBins];
-  uint64_t tab_key[kTpMaxShards][kTpTab];
+  uint64_t tab_key[kTpMaxShards][kTpTab];  // top-k rows: candidates (key << 32 | id)
   uint32_t tab_cnt[kTpMaxShards][kTpTab];
 };
 
@@ -70,6 +79,9 @@ struct TpParams {
   int32_t* tokens;
   int32_t* status;
   TpRow* ws;
+  int top_k;     // 0: dense rows
+  int32_t* ids;  // top-k rows: [rows][top_k]
+  int32_t* nnz;  // top-k rows: [rows]
 };
 
 struct TpShared {
@@ -455,19 +467,253 @@ __global__ void __launch_bounds__(kTpThr) tp_draw_kernel(TpParams p) {
   }
 }
 
+// ------------------------------------------------------------ top-k rows
+static_assert(DSPARK_MAX_TOPK <= kTpTab, "a shard's candidates fit in its table");
+constexpr int kTkCand = kTpMaxShards * DSPARK_MAX_TOPK;  // the leader's merge buffer
+
+struct TkShared {
+  uint32_t hist[256];
+  uint32_t r32[32];
+  float rf[32];
+  uint32_t sel_digit, sel_above, sel_equal;
+  uint32_t n;
+};
+
+// Block-wide radix select (8-bit digits, most significant first): the r-th
+// largest value of val(i) over i < n with take(i) (1 <= r <= the count);
+// *above: the entries with a larger value, *equal: those equal to it.  The
+// lanes of a warp that fall in one bin add to it with one atomic.  Called by
+// every thread of the block; the result is uniform.
+template <int kBits, typename T, typename Val, typename Take>
+__device__ T radix_select_desc(int n, uint32_t r, Val val, Take take, TkShared& sh,
+                               uint32_t* above, uint32_t* equal) {
+  const int lane = threadIdx.x & 31;
+  T prefix = 0, mask = 0;
+  uint32_t above_acc = 0, eq = 0;
+  for (int shift = kBits - 8; shift >= 0; shift -= 8) {
+    __syncthreads();
+    sh.hist[threadIdx.x] = 0u;  // kTpThr == 256 bins
+    __syncthreads();
+    for (int i0 = 0; i0 < n; i0 += kTpThr) {
+      const int i = i0 + (int)threadIdx.x;
+      uint32_t bin = 0xFFFFFFFFu;
+      if (i < n && take(i)) {
+        const T v = val(i);
+        if ((v & mask) == prefix) bin = (uint32_t)(v >> shift) & 255u;
+      }
+      const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+      if (bin != 0xFFFFFFFFu && lane == __ffs(peers) - 1)
+        atomicAdd(&sh.hist[bin], (uint32_t)__popc(peers));
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      // lane l holds bins 255 - 8l down to 248 - 8l
+      uint32_t c[8], t = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        c[j] = sh.hist[255 - 8 * lane - j];
+        t += c[j];
+      }
+      uint32_t incl = t;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+      }
+      const uint32_t excl = incl - t;
+      if (excl < r && r <= incl) {
+        uint32_t acc = excl;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (acc < r && r <= acc + c[j]) {
+            sh.sel_digit = (uint32_t)(255 - 8 * lane - j);
+            sh.sel_above = acc;
+            sh.sel_equal = c[j];
+          }
+          acc += c[j];
+        }
+      }
+    }
+    __syncthreads();
+    const uint32_t ab = sh.sel_above;
+    eq = sh.sel_equal;
+    r -= ab;
+    above_acc += ab;
+    prefix |= (T)sh.sel_digit << shift;
+    mask |= (T)255u << shift;
+  }
+  *above = above_acc;
+  *equal = eq;
+  return prefix;
+}
+
+// Order key of y for the support: larger y, larger key; -0 taken as +0.
+__device__ __forceinline__ uint32_t tk_key(float y) { return float_key(__fadd_rn(y, 0.0f)); }
+
+// Each rank: validity flags and max of its shard (as the dense rows), then its
+// local top k by (y desc, id asc) -- every finite element when it holds at
+// most k -- sent as (key << 32 | id) records.
+__global__ void __launch_bounds__(kTpThr) tp_topk_local_kernel(TpParams p) {
+  __shared__ TkShared sh;
+  const Shard d = shard_of(p);
+  TpRow& w = p.ws[d.row];
+  bool badT;
+  const float invT = inv_temp(p, d.row, &badT);
+  float mx = -INFINITY;
+  uint32_t fl = 0, nfin = 0;
+  if (!badT)
+    for (int v = d.lo + threadIdx.x; v < d.hi; v += kTpThr) {
+      const char* xrow = reinterpret_cast<const char*>(p.x) +
+                         (int64_t)d.row * p.ld * (p.dtype == DSPARK_F32 ? 4 : 2);
+      const float x = load_logit(xrow, p.dtype, v);
+      if (!(x < INFINITY)) fl |= 1u;  // NaN or +inf
+      const float y = invT == 1.0f ? x : __fmul_rn(x, invT);
+      if (fabsf(y) == INFINITY && fabsf(x) < INFINITY) fl |= 1u;  // overflow
+      if (y > -INFINITY && y < INFINITY) {
+        fl |= 2u;
+        ++nfin;
+        mx = fmaxf(mx, y);
+      }
+    }
+  mx = block_reduce(mx, OpMaxNaNTp(), sh.rf);
+  fl = block_reduce(fl, OpOrU32(), sh.r32);
+  nfin = block_reduce(nfin, OpAddU32(), sh.r32);
+  if (threadIdx.x == 0) {
+    w.mx[d.s] = mx;
+    w.fl[d.s] = fl;
+    sh.n = 0u;
+  }
+  __syncthreads();
+  const int k = p.top_k;
+  uint32_t nc = 0;
+  if (!badT && !(fl & 1u) && nfin > 0u) {
+    auto key_at = [&](int i, uint32_t* key) -> bool {  // i: position in the shard
+      const float y = y_of(p, d.row, d.lo + i, invT);
+      *key = tk_key(y);
+      return y > -INFINITY;
+    };
+    const int n = d.hi - d.lo;
+    uint32_t T = 0u, need = 0xFFFFFFFFu;  // take key > T, and `need` lowest ids at T
+    if (nfin > (uint32_t)k) {
+      uint32_t above, equal;
+      T = radix_select_desc<32, uint32_t>(
+          n, (uint32_t)k,
+          [&](int i) {
+            uint32_t key;
+            key_at(i, &key);
+            return key;
+          },
+          [&](int i) {
+            uint32_t key;
+            return key_at(i, &key);
+          },
+          sh, &above, &equal);
+      need = (uint32_t)k - above;
+    }
+    // the candidates, in id order (ties at T: the lowest ids)
+    uint32_t base = 0;
+    for (int i0 = 0; i0 < n; i0 += kTpThr) {
+      const int i = i0 + (int)threadIdx.x;
+      uint32_t key = 0u;
+      const bool fin = i < n && key_at(i, &key);
+      const bool at = fin && nfin > (uint32_t)k && key == T;
+      const bool hi = fin && (nfin <= (uint32_t)k || key > T);
+      uint32_t tot;
+      const uint32_t incl = block_inclusive_scan(at ? 1u : 0u, sh.r32, &tot);
+      if (hi || (at && base + incl <= need)) {
+        const uint32_t j = atomicAdd(&sh.n, 1u);
+        w.tab_key[d.s][j] = ((uint64_t)key << 32) | (uint32_t)(d.lo + i);
+      }
+      base += tot;
+      __syncthreads();
+    }
+    nc = sh.n;
+  }
+  if (threadIdx.x == 0) w.nc[d.s] = nc;
+}
+
+// The leader of each row: the global top k of the ranks' candidates, the
+// allocation on it, the outputs and the draw.
+__global__ void __launch_bounds__(kTpThr) tp_topk_merge_kernel(TpParams p) {
+  __shared__ TkShared sh;
+  __shared__ SupShared ssh;
+  extern __shared__ __align__(16) unsigned char dyn[];
+  uint64_t* cand = reinterpret_cast<uint64_t*>(dyn);                   // [kTkCand]
+  uint32_t* skeys = reinterpret_cast<uint32_t*>(cand + kTkCand);       // [top_k]
+  int32_t* sids = reinterpret_cast<int32_t*>(skeys + DSPARK_MAX_TOPK); // [top_k]
+  unsigned char* scratch = reinterpret_cast<unsigned char*>(sids + DSPARK_MAX_TOPK);
+  const int row = blockIdx.x;
+  const TpRow& w = p.ws[row];
+  const int k = p.top_k;
+  bool badT;
+  inv_temp(p, row, &badT);
+  float m;
+  const int st = row_state(p, w, badT, &m);
+  int n = 0;
+  if (st == DSPARK_ST_OK) {
+    for (int s = 0; s < p.n_sh; ++s) {
+      const int ns = (int)w.nc[s];
+      for (int i = threadIdx.x; i < ns; i += kTpThr) cand[n + i] = w.tab_key[s][i];
+      n += ns;
+    }
+  }
+  if (threadIdx.x == 0) sh.n = 0u;
+  __syncthreads();
+  int ns = min(n, k);
+  if (st == DSPARK_ST_OK) {
+    // the k largest (key, -id): a record's order value is key << 32 | ~id
+    auto ord = [&](int i) { return cand[i] ^ 0xFFFFFFFFull; };
+    uint64_t C = 0ull;
+    if (n > k) {
+      uint32_t above, equal;
+      C = radix_select_desc<64, uint64_t>(n, (uint32_t)k, ord, [](int) { return true; }, sh,
+                                          &above, &equal);
+    }
+    for (int i = threadIdx.x; i < n; i += kTpThr)
+      if (ord(i) >= C) {
+        const uint32_t j = atomicAdd(&sh.n, 1u);  // exactly min(n, k) qualify
+        skeys[j] = (uint32_t)(cand[i] >> 32);
+        sids[j] = (int32_t)(uint32_t)cand[i];
+      }
+    __syncthreads();
+  }
+  uint32_t D = 0;
+  if (p.tokens) {
+    const int b = row / p.depth, j = row % p.depth;
+    const uint32_t req = p.request_ids ? p.request_ids[b] : (uint32_t)b;
+    D = draw_u32(p.seed, req, (uint32_t)j, DSPARK_PURPOSE_PROPOSAL) >> 8;
+  }
+  support_alloc_emit(st, ns, k, skeys, sids, scratch, ssh, p.counts + (int64_t)row * k,
+                     p.ids + (int64_t)row * k, p.nnz + row, p.status + row,
+                     p.tokens ? p.tokens + row : nullptr, D);
+}
+
+constexpr int kTkMergeSmem =
+    kTkCand * 8 + DSPARK_MAX_TOPK * 8 + kSupScratch;  // candidates, support, scratch
+
 }  // namespace
 
 int64_t q_sharded_workspace_bytes(int n_rows) { return (int64_t)n_rows * sizeof(TpRow); }
 
 cudaError_t launch_q_sharded(const void* x, int dtype, int64_t ld, int B, int depth, int V,
-                             int n_sh, const float* temperature, uint64_t seed,
-                             const uint32_t* request_ids, uint32_t* counts, int32_t* tokens,
-                             int32_t* status, void* workspace, cudaStream_t stream) {
-  TpParams p{x,     dtype,       ld,     V,      n_sh,   depth,
-             temperature, seed, request_ids, counts, tokens, status,
-             static_cast<TpRow*>(workspace)};
+                             int n_sh, const float* temperature, int top_k, uint64_t seed,
+                             const uint32_t* request_ids, uint32_t* counts, int32_t* ids,
+                             int32_t* nnz, int32_t* tokens, int32_t* status, void* workspace,
+                             cudaStream_t stream) {
+  TpParams p{x,           dtype,  ld,     V,      n_sh,
+             depth,       temperature, seed, request_ids, counts,
+             tokens,      status, static_cast<TpRow*>(workspace), top_k, ids, nnz};
   const int rows = B * depth;
   const int units = rows * n_sh;
+  if (top_k > 0) {
+    cudaError_t e = cudaFuncSetAttribute(tp_topk_merge_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kTkMergeSmem);
+    if (e != cudaSuccess) return e;
+    tp_topk_local_kernel<<<units, kTpThr, 0, stream>>>(p);
+    tp_topk_merge_kernel<<<rows, kTpThr, kTkMergeSmem, stream>>>(p);
+    return cudaGetLastError();
+  }
   tp_max_kernel<<<units, kTpThr, 0, stream>>>(p);
   tp_weights_kernel<<<units, kTpThr, 0, stream>>>(p);
   tp_floors_kernel<<<units, kTpThr, 0, stream>>>(p);

@@ -393,21 +393,23 @@ int dspark_q_chain_sample(const void* draft_logits, int32_t dtype, int64_t ld, i
                           void* stream);
 
 /*
- * dspark_q_build_sample_sharded -- the dense q build and draft draw with the
- * vocabulary split over n_shards emulated ranks on one GPU ("PP1 q transport
- * and scheduling design", Sparse support and vocabulary-sharded TP2
- * follow-up: all-reduce of the max and the shifted sums, remaining tickets
- * coordinated globally, the leader's one draw choosing the shard by its count
- * mass and then the token inside).  Shard s holds ids [s*Vs, min(V,
- * (s+1)*Vs)), Vs = ceil(V / n_shards); each kernel runs one CTA per (row,
- * shard) and ranks exchange only partials, through the workspace.
+ * dspark_q_build_sample_sharded -- dspark_q_build_sample with the vocabulary
+ * split over n_shards emulated ranks on one GPU ("PP1 q transport and
+ * scheduling design", Sparse support and vocabulary-sharded TP2 follow-up:
+ * all-reduce of the max and the shifted sums, remaining tickets coordinated
+ * globally, a global top-k merge of the ranks' local top-k, the leader's one
+ * draw choosing the shard by its count mass and then the token inside).
+ * Shard s holds ids [s*Vs, min(V, (s+1)*Vs)), Vs = ceil(V / n_shards); each
+ * per-rank kernel runs one CTA per (row, shard) and ranks exchange only
+ * partials, through the workspace.
  *
- * Arguments and outputs as dspark_q_build_sample with top_k = 0 (draft_tokens
- * may be NULL: q only); the counts, tokens and statuses equal that call's bit
- * for bit.  The ranks exchange, for the fraction bin holding the grant
- * threshold, a table of its distinct exact fractions with their counts; a row
- * whose bin holds more than 1024 distinct fractions over all shards is
- * refused with DSPARK_ST_INTERNAL (exact ties of any multiplicity are fine).
+ * Arguments and outputs as dspark_q_build_sample (draft_tokens may be NULL:
+ * q only); the counts, sparse ids, nnz, tokens and statuses equal that call's
+ * bit for bit.  Dense rows: the ranks exchange, for the fraction bin holding
+ * the grant threshold, a table of its distinct exact fractions with their
+ * counts; a row whose bin holds more than 1024 distinct fractions over all
+ * shards is refused with DSPARK_ST_INTERNAL (exact ties of any multiplicity
+ * are fine).  Top-k rows: each rank sends at most top_k candidates.
  * n_shards in [1, 8] (DSPARK_ERR_ARG otherwise).
  * workspace: dspark_q_sharded_workspace_bytes(B*depth) bytes of device
  * memory, 16-byte aligned, owned by the caller.
@@ -415,10 +417,10 @@ int dspark_q_chain_sample(const void* draft_logits, int32_t dtype, int64_t ld, i
 int64_t dspark_q_sharded_workspace_bytes(int32_t n_rows);
 int dspark_q_build_sample_sharded(const void* draft_logits, int32_t dtype, int64_t ld, int32_t B,
                                   int32_t depth, int32_t V, int32_t n_shards,
-                                  const float* temperature, uint64_t seed,
+                                  const float* temperature, int32_t top_k, uint64_t seed,
                                   const uint32_t* request_ids, uint32_t* counts,
-                                  int32_t* draft_tokens, int32_t* row_status, void* workspace,
-                                  void* stream);
+                                  int32_t* sparse_ids, int32_t* nnz, int32_t* draft_tokens,
+                                  int32_t* row_status, void* workspace, void* stream);
 
 /*
  * dspark_q_pack -- the wire form of q rows ("PP1 q transport and scheduling

@@ -105,3 +105,27 @@ def test_spec_step_noalloc_host_checks(lib):
     empty = list(a)
     empty[6] = 0
     assert f(*empty) == 0
+
+
+def test_sharded_argument_errors(lib):
+    f = lib.dspark_q_build_sample_sharded
+    # (logits, dtype, ld, B, depth, V, n_shards, T, top_k, seed, req, counts, ids, nnz,
+    #  tokens, status, workspace, stream)
+    ok = (P, 0, 8, 1, 1, 8, 2, None, 0, 0, None, P, None, None, P, P, P, None)
+
+    def call(**kw):
+        a = list(ok)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return f(*a)
+
+    assert call(a6=0) == -7 and call(a6=9) == -7         # n_shards outside [1, 8]
+    assert call(a5=0) == -2                              # V = 0
+    assert call(a4=0) == -2                              # depth = 0
+    assert call(a8=9) == -4                              # top_k > V
+    assert call(a8=4) == -1                              # sparse without ids / nnz
+    assert call(a16=None) == -1                          # no workspace
+    assert call(a16=ctypes.c_void_p(24)) == -5           # workspace not 16-byte aligned
+    assert call(a3=0) == 0                               # empty batch
+    assert lib.dspark_q_sharded_workspace_bytes(-1) == 0
+    assert lib.dspark_q_sharded_workspace_bytes(3) == 3 * lib.dspark_q_sharded_workspace_bytes(1)
