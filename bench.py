@@ -16,9 +16,10 @@ which `--workload c3` covers).
 Prints ONE JSON line (rank 0):
   value   verify rows/s (B x 6 rows per step) with inputs resident in HBM,
           device time from CUDA events on the launching stream;
-  e2e     the same metric through the same C-ABI calls with pinned host
-          buffers: H2D of the step's logits and D2H of its results inside the
-          timed region;
+  e2e     the same metric through the host-buffer C-ABI call
+          (dspark_spec_step_host) on pinned host buffers: the H2D copies of
+          the step's logits and the D2H copies of its results are inside the
+          timed region; steps alternate over two streams;
   roofline  the dominant kernel's algorithmic bytes per launch / its mean
           CUDA-event duration, against the measured HBM copy bandwidth;
   cpu_baseline  the CPU oracle timed on a bounded sample of the workload.
@@ -318,46 +319,64 @@ def run_ours(args, rank, world, local_rank):
             per_kernel[k] += marks[s][i].elapsed_time(marks[s][i + 1])
     per_kernel = {k: v / args.steps for k, v in per_kernel.items()}
 
-    # ---- end to end: pinned host buffers, copies inside the timed region
+    # ---- end to end: the host-buffer entry (dspark_spec_step_host) on pinned
+    #      host buffers, its copies inside the timed region.  Steps alternate
+    #      between two streams, each with its own staging buffer, so the copy
+    #      engine loads one step's inputs while the SMs run the previous step.
     e2e = None
     if not args.no_e2e:
-        h_d = torch.from_numpy(wl.draft).pin_memory()
-        h_t = (torch.from_numpy(wl.target) if wl.target_dtype == "f32"
-               else torch.from_numpy(wl.target.view(np.int16))).pin_memory()
-        d_d = torch.empty_like(xd)
-        d_t = torch.empty(xt.shape, dtype=xt.dtype, device=dev)
-        d_t_raw = d_t if wl.target_dtype == "f32" else d_t.view(torch.int16)
-        res_shapes = [(B,), (B, depth + 1), (B,)]
-        h_res = {m: [torch.empty(s, dtype=torch.int32).pin_memory() for s in res_shapes]
-                 for m in wl.modes}
-        h_tok = torch.empty((B, depth), dtype=torch.int32).pin_memory()
+        h_d = torch.from_numpy(np.ascontiguousarray(wl.draft)).pin_memory()
+        h_t = (torch.from_numpy(np.ascontiguousarray(wl.target)) if wl.target_dtype == "f32"
+               else torch.from_numpy(np.ascontiguousarray(wl.target).view(np.int16)).view(
+                   torch.bfloat16)).pin_memory()
+        h_temp = torch.from_numpy(np.ascontiguousarray(wl.temperature)).pin_memory()
+        h_req = torch.from_numpy(np.ascontiguousarray(req_np).view(np.int32)).pin_memory()
+        n_st = 2
+        streams = [torch.cuda.Stream(dev) for _ in range(n_st)]
+        sbytes = ds.dspark_spec_step_host_staging_bytes(B, depth, V, ds._dtype_code(h_d),
+                                                        ds._dtype_code(h_t))
+        staging = [torch.empty((sbytes,), dtype=torch.uint8, device=dev) for _ in range(n_st)]
 
-        def e2e_step():
-            d_d.copy_(h_d, non_blocking=True)
-            d_t_raw.copy_(h_t, non_blocking=True)
-            step(d_d, d_t)
-            h_tok.copy_(tok, non_blocking=True)
-            for m in wl.modes:
-                a, c, f, s = outs[m]
-                h_res[m][0].copy_(a, non_blocking=True)
-                h_res[m][1].copy_(c, non_blocking=True)
-                h_res[m][2].copy_(s, non_blocking=True)
+        def pinned(shape):
+            return torch.empty(shape, dtype=torch.int32).pin_memory()
 
-        for _ in range(max(1, args.warmup // 2)):
-            e2e_step()
+        h_out = []
+        for _ in range(n_st):
+            o = {"tok": pinned((B, depth)), "rst": pinned((rows_d,))}
+            if "greedy" in wl.modes:
+                o["greedy"] = (pinned((B,)), pinned((B, depth + 1)), pinned((B,)))
+            if "ratio" in wl.modes:
+                o["ratio"] = (pinned((B,)), pinned((B, depth + 1)), pinned((B,)), pinned((B,)))
+            h_out.append(o)
+
+        def e2e_step(i):
+            o = h_out[i % n_st]
+            ds.dspark_spec_step_host(h_d, h_t, B, depth, h_temp, wl.seed, h_req, o["tok"],
+                                     o["rst"], staging[i % n_st], greedy_out=o.get("greedy"),
+                                     ratio_out=o.get("ratio"), stream=streams[i % n_st])
+
+        for i in range(max(2, args.warmup // 2)):
+            e2e_step(i)
         torch.cuda.synchronize()
         barrier()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        e1.record(stream)
+        e0.record(streams[0])
+        for st_ in streams[1:]:
+            st_.wait_event(e0)
+        for i in range(args.steps):
+            e2e_step(i)
+        for st_ in streams[1:]:
+            streams[0].wait_stream(st_)
+        e1.record(streams[0])
         torch.cuda.synchronize()
         e2e_ms = e0.elapsed_time(e1) / args.steps
-        h2d = h_d.numel() * h_d.element_size() + h_t.numel() * h_t.element_size()
-        d2h = h_tok.numel() * 4 + sum(t.numel() * 4 for m in wl.modes for t in h_res[m])
-        e2e = {"ms_per_step": e2e_ms, "h2d": h2d, "d2h": d2h}
+        h2d = (h_d.numel() * h_d.element_size() + h_t.numel() * h_t.element_size()
+               + h_temp.numel() * 4 + h_req.numel() * 4)
+        o = h_out[0]
+        d2h = (o["tok"].numel() + o["rst"].numel()
+               + sum(t.numel() for m in ("greedy", "ratio") for t in o.get(m, ()))) * 4
+        e2e = {"ms_per_step": e2e_ms, "h2d": h2d, "d2h": d2h, "streams": n_st}
 
     # ---- the received-q path on this step's q rows: the sender's pack
     #      (wire values + checksums), the receiver's validation (values,
@@ -617,7 +636,12 @@ def main():
         if e2e:
             line["e2e"] = {"value": rows / (e2e["ms_per_step"] * 1e-3), "unit": "verify rows/s",
                            "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
-                           "ms_per_step": e2e["ms_per_step"]}
+                           "ms_per_step": e2e["ms_per_step"],
+                           "how": "dspark_spec_step_host per step (host rows copied to a staging "
+                                  "buffer, the step, the outputs copied back), steps alternating "
+                                  "over %d streams and staging buffers" % e2e["streams"],
+                           "h2d_link_gbs": round(e2e["h2d"] / (e2e["ms_per_step"] * 1e-3) / 1e9,
+                                                 1)}
         if wire:
             gbs_p = wire["pack_bytes"] / (wire["pack_ms"] * 1e-3) / 1e9
             gbs_v = wire["validate_bytes"] / (wire["validate_ms"] * 1e-3) / 1e9

@@ -31,7 +31,8 @@ __all__ = ["dspark_q_build", "dspark_q_build_sample", "dspark_draft_sample", "ds
            "dspark_spec_step_schedule", "dspark_spec_step_noalloc", "dspark_q_pack",
            "dspark_q_validate", "dspark_verify_match", "verify_match", "dspark_q_chain_sample",
            "q_chain_sample", "dspark_q_build_sample_sharded", "dspark_q_sharded_workspace_bytes",
-           "q_build_sample_sharded", "q_build",
+           "q_build_sample_sharded", "dspark_spec_step_host",
+           "dspark_spec_step_host_staging_bytes", "q_build",
            "draft_sample", "verify_greedy", "verify_ratio", "target_probs", "q_build_sample",
            "spec_step", "version"]
 
@@ -176,6 +177,40 @@ def dspark_spec_step_noalloc(draft_logits, target_logits, B, depth, temperature,
           _ptr(temperature), int(seed) & (2 ** 64 - 1), _i32(request_ids), _i32(counts),
           _i32(draft_tokens), _i32(row_status), _i32(g[0]), _i32(g[1]), _i32(g[2]), _i32(r[0]),
           _i32(r[1]), _i32(r[2]), _i32(r[3]), int(schedule), _stream(stream))
+
+
+def _host(t):
+    if t is None:
+        return None
+    if t.is_cuda or not t.is_contiguous():
+        raise ValueError("expected a contiguous host tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def dspark_spec_step_host_staging_bytes(B, depth, V, draft_dtype, target_dtype):
+    return int(_lib.load().dspark_spec_step_host_staging_bytes(int(B), int(depth), int(V),
+                                                               int(draft_dtype), int(target_dtype)))
+
+
+def dspark_spec_step_host(draft_logits, target_logits, B, depth, temperature, seed, request_ids,
+                          draft_tokens, row_status, staging, greedy_out=None, ratio_out=None,
+                          stream=None, schedule=0):
+    """dspark_spec_step on host tensors (page-locked for asynchronous copies):
+    draft_logits [B*depth, V] and target_logits [B*(depth+1), V] (float32 or
+    bfloat16), temperature / request_ids (or None), host outputs; staging is
+    a device uint8 tensor of dspark_spec_step_host_staging_bytes bytes."""
+    V = draft_logits.shape[-1]
+    if (draft_logits.numel() != B * depth * V or target_logits.numel() != B * (depth + 1) * V
+            or target_logits.shape[-1] != V):
+        raise ValueError("draft_logits must hold B*depth rows and target_logits B*(depth+1) rows "
+                         "of the same V")
+    g = greedy_out or (None, None, None)
+    r = ratio_out or (None, None, None, None)
+    _call("dspark_spec_step_host", _host(draft_logits), _dtype_code(draft_logits),
+          _host(target_logits), _dtype_code(target_logits), int(B), int(depth), int(V),
+          _host(temperature), int(seed) & (2 ** 64 - 1), _host(request_ids), _host(draft_tokens),
+          _host(row_status), _host(g[0]), _host(g[1]), _host(g[2]), _host(r[0]), _host(r[1]),
+          _host(r[2]), _host(r[3]), _ptr(staging), int(schedule), _stream(stream))
 
 
 def dspark_spec_step_schedule(B, depth):

@@ -41,6 +41,8 @@ SIGNATURES = {
                                  _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I32, _P],
     "dspark_spec_step": [_P, _I32, _I64, _P, _I32, _I64, _I32, _I32, _I32, _P, _U64, _P, _P, _P,
                          _P, _P, _P, _P, _P, _P, _P, _P, _P, _I32, _P],
+    "dspark_spec_step_host": [_P, _I32, _P, _I32, _I32, _I32, _I32, _P, _U64, _P, _P, _P, _P, _P,
+                              _P, _P, _P, _P, _P, _P, _I32, _P],
     "dspark_debug_exp_weights": [_P, _I64, _P, _P, _P],
     "dspark_debug_philox": [_P, _U64, _I64, _P, _P],
     "dspark_debug_alloc_scale": [_P, _I64, _P, _P, _P, _P, _P],
@@ -74,6 +76,8 @@ def load(path: str = LIB_PATH):
                 fn.restype = ctypes.c_int
             lib.dspark_q_sharded_workspace_bytes.argtypes = [_I32]
             lib.dspark_q_sharded_workspace_bytes.restype = ctypes.c_int64
+            lib.dspark_spec_step_host_staging_bytes.argtypes = [_I32, _I32, _I32, _I32, _I32]
+            lib.dspark_spec_step_host_staging_bytes.restype = ctypes.c_int64
             lib.dspark_version.argtypes = []
             lib.dspark_version.restype = ctypes.c_char_p
             _lib = lib

@@ -346,6 +346,116 @@ int dspark_spec_step_noalloc(const void* draft_logits, int32_t draft_dtype, int6
                         ratio_status, nullptr, true, schedule, stream);
 }
 
+namespace {
+
+// The staging buffer of dspark_spec_step_host: 256-byte aligned segments.
+struct HostStaging {
+  int64_t counts, draft, target, temperature, request_ids, tokens, row_status, g_acc, g_com,
+      g_st, r_acc, r_com, r_flags, r_st, workspace, total;
+};
+
+int64_t seg(int64_t* at, int64_t bytes) {
+  const int64_t o = *at;
+  *at += (bytes + 255) / 256 * 256;
+  return o;
+}
+
+HostStaging host_staging(int32_t B, int32_t depth, int32_t V, int32_t dd, int32_t td) {
+  HostStaging h;
+  int64_t at = 0;
+  const int64_t rows = (int64_t)B * depth, trows = (int64_t)B * (depth + 1);
+  h.counts = seg(&at, rows * V * 4);
+  h.draft = seg(&at, rows * V * esize(dd));
+  h.target = seg(&at, trows * V * esize(td));
+  h.temperature = seg(&at, rows * 4);
+  h.request_ids = seg(&at, (int64_t)B * 4);
+  h.tokens = seg(&at, rows * 4);
+  h.row_status = seg(&at, rows * 4);
+  h.g_acc = seg(&at, (int64_t)B * 4);
+  h.g_com = seg(&at, trows * 4);
+  h.g_st = seg(&at, (int64_t)B * 4);
+  h.r_acc = seg(&at, (int64_t)B * 4);
+  h.r_com = seg(&at, trows * 4);
+  h.r_flags = seg(&at, (int64_t)B * 4);
+  h.r_st = seg(&at, (int64_t)B * 4);
+  h.workspace = seg(&at, ((int64_t)B + 1) * 4);
+  h.total = at;
+  return h;
+}
+
+}  // namespace
+
+int64_t dspark_spec_step_host_staging_bytes(int32_t B, int32_t depth, int32_t V,
+                                            int32_t draft_dtype, int32_t target_dtype) {
+  if (B < 0 || depth < 1 || depth > DSPARK_MAX_DEPTH || V < 1 || V > DSPARK_MAX_V) return 0;
+  if (check_common(draft_dtype, V, V) || check_common(target_dtype, V, V)) return 0;
+  return host_staging(B, depth, V, draft_dtype, target_dtype).total;
+}
+
+int dspark_spec_step_host(const void* h_draft_logits, int32_t draft_dtype,
+                          const void* h_target_logits, int32_t target_dtype, int32_t B,
+                          int32_t depth, int32_t V, const float* h_temperature, uint64_t seed,
+                          const uint32_t* h_request_ids, int32_t* h_draft_tokens,
+                          int32_t* h_row_status, int32_t* h_greedy_accept_len,
+                          int32_t* h_greedy_committed, int32_t* h_greedy_status,
+                          int32_t* h_ratio_accept_len, int32_t* h_ratio_committed,
+                          uint32_t* h_ratio_flags, int32_t* h_ratio_status, void* staging,
+                          int32_t schedule, void* stream) {
+  if (int e = check_common(draft_dtype, V, V)) return e;
+  if (int e = check_common(target_dtype, V, V)) return e;
+  if (depth < 1 || depth > DSPARK_MAX_DEPTH) return DSPARK_ERR_SIZE;
+  if (B < 0 || (int64_t)B * depth > kMaxGridRows) return DSPARK_ERR_SIZE;
+  if (schedule < DSPARK_SCHEDULE_AUTO || schedule > DSPARK_SCHEDULE_SEPARATE)
+    return DSPARK_ERR_ARG;
+  if (B == 0) return 0;
+  const bool g = h_greedy_accept_len || h_greedy_committed || h_greedy_status;
+  const bool r = h_ratio_accept_len || h_ratio_committed || h_ratio_status;
+  if (!h_draft_logits || !h_target_logits || !h_draft_tokens || !h_row_status || !staging)
+    return DSPARK_ERR_NULL;
+  if (!g && !r) return DSPARK_ERR_NULL;
+  if (g && (!h_greedy_accept_len || !h_greedy_committed || !h_greedy_status))
+    return DSPARK_ERR_NULL;
+  if (r && (!h_ratio_accept_len || !h_ratio_committed || !h_ratio_status)) return DSPARK_ERR_NULL;
+  if (!aligned(staging, 256)) return DSPARK_ERR_ALIGN;
+  const HostStaging h = host_staging(B, depth, V, draft_dtype, target_dtype);
+  char* base = static_cast<char*>(staging);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t rows = (int64_t)B * depth, trows = (int64_t)B * (depth + 1);
+  auto h2d = [&](int64_t off, const void* src, int64_t bytes) {
+    return cudaMemcpyAsync(base + off, src, (size_t)bytes, cudaMemcpyHostToDevice, st);
+  };
+  auto d2h = [&](void* dst, int64_t off, int64_t bytes) {
+    return cudaMemcpyAsync(dst, base + off, (size_t)bytes, cudaMemcpyDeviceToHost, st);
+  };
+  cudaError_t e = h2d(h.draft, h_draft_logits, rows * V * esize(draft_dtype));
+  if (e == cudaSuccess) e = h2d(h.target, h_target_logits, trows * V * esize(target_dtype));
+  if (e == cudaSuccess && h_temperature) e = h2d(h.temperature, h_temperature, rows * 4);
+  if (e == cudaSuccess && h_request_ids) e = h2d(h.request_ids, h_request_ids, (int64_t)B * 4);
+  if (e != cudaSuccess) return launch_result(e);
+  auto dp = [&](int64_t off) { return reinterpret_cast<int32_t*>(base + off); };
+  const int rc = spec_step_impl(
+      base + h.draft, draft_dtype, V, base + h.target, target_dtype, V, B, depth, V,
+      h_temperature ? reinterpret_cast<const float*>(base + h.temperature) : nullptr, seed,
+      h_request_ids ? reinterpret_cast<const uint32_t*>(base + h.request_ids) : nullptr,
+      reinterpret_cast<uint32_t*>(base + h.counts), dp(h.tokens), dp(h.row_status),
+      g ? dp(h.g_acc) : nullptr, g ? dp(h.g_com) : nullptr, g ? dp(h.g_st) : nullptr,
+      r ? dp(h.r_acc) : nullptr, r ? dp(h.r_com) : nullptr,
+      (r && h_ratio_flags) ? reinterpret_cast<uint32_t*>(base + h.r_flags) : nullptr,
+      r ? dp(h.r_st) : nullptr, reinterpret_cast<uint32_t*>(base + h.workspace), false, schedule,
+      stream);
+  if (rc != 0) return rc;
+  e = d2h(h_draft_tokens, h.tokens, rows * 4);
+  if (e == cudaSuccess) e = d2h(h_row_status, h.row_status, rows * 4);
+  if (e == cudaSuccess && g) e = d2h(h_greedy_accept_len, h.g_acc, (int64_t)B * 4);
+  if (e == cudaSuccess && g) e = d2h(h_greedy_committed, h.g_com, trows * 4);
+  if (e == cudaSuccess && g) e = d2h(h_greedy_status, h.g_st, (int64_t)B * 4);
+  if (e == cudaSuccess && r) e = d2h(h_ratio_accept_len, h.r_acc, (int64_t)B * 4);
+  if (e == cudaSuccess && r) e = d2h(h_ratio_committed, h.r_com, trows * 4);
+  if (e == cudaSuccess && r && h_ratio_flags) e = d2h(h_ratio_flags, h.r_flags, (int64_t)B * 4);
+  if (e == cudaSuccess && r) e = d2h(h_ratio_status, h.r_st, (int64_t)B * 4);
+  return launch_result(e);
+}
+
 int dspark_q_chain_sample(const void* draft_logits, int32_t dtype, int64_t ld, int32_t B,
                           int32_t depth, int32_t V, const float* temperature, const float* bias,
                           int64_t bias_ld, int32_t n_bias, const int32_t* anchors, uint64_t seed,

@@ -430,6 +430,12 @@ __device__ __forceinline__ void tma_load_bulk(void* dst, const void* src, uint32
       : "memory");
 }
 
+// Bulk prefetch of [src, src + bytes) into L2 (src 16-byte aligned, bytes a
+// multiple of 16); nothing waits for it.
+__device__ __forceinline__ void l2_prefetch_bulk(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // One try_wait with a suspend-time hint: the thread may sleep in hardware
 // (up to the hint) until the phase completes instead of spinning.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t phase) {

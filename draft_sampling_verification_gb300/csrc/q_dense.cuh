@@ -111,6 +111,7 @@ struct DShared {
   uint32_t wcnt[kWarps];
   int sel_bin;
   uint32_t sel_above, sel_count, scan_base;
+  uint32_t draw;  // the row's 24-bit draft draw (fused draw only)
 };
 constexpr int kAllCap = kBins * 4 / (int)sizeof(Cand);
 
@@ -331,9 +332,12 @@ __device__ void ordered_ranks(cg::cluster_group& cluster, DShared& sh, int ngrou
 // the same row).  `mbar` holds kTma initialised mbarriers whose current phase
 // parity is `phase` (updated here).  When `ready` is given (a fused launch),
 // ready[row / depth] is incremented once the row's counts, status and token
-// are visible device-wide.
+// are visible device-wide.  When next_row >= 0, this CTA's part of that row
+// is prefetched into L2 while this row is built (the same cluster takes it
+// next, so its bulk copies then read L2).
 __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& sh, float* sl,
-                                            uint64_t* mbar, uint32_t& phase, uint32_t* ready) {
+                                            uint64_t* mbar, uint32_t& phase, uint32_t* ready,
+                                            int next_row = -1) {
   cg::cluster_group cluster = cg::this_cluster();
   uint32_t* slu = reinterpret_cast<uint32_t*>(sl);
 
@@ -384,6 +388,12 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
       mbar_arrive_expect_tx(&mbar[c], bytes);
       if (bytes) tma_load_bulk(sl + 4 * g0, xbase + 4 * g0, bytes, &mbar[c]);
     }
+  }
+  if (tid == 32 && p.tokens) {
+    // the draft draw, while the slice lands
+    const int b = row / p.depth, j = row % p.depth;
+    const uint32_t req = p.request_ids ? p.request_ids[b] : (uint32_t)b;
+    sh.draw = draw_u32(p.seed, req, (uint32_t)j, DSPARK_PURPOSE_PROPOSAL) >> 8;
   }
   if (use_tma_dtype) {
     // partial edge groups by plain loads, -inf padding
@@ -470,6 +480,13 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
     return;
   }
   const float m = sh.m;
+  if (next_row >= 0 && use_tma_dtype && tid == 0) {
+    // this CTA's aligned part of the next row, into L2
+    const char* nrow = reinterpret_cast<const char*>(p.x) + (int64_t)next_row * p.ld * 4;
+    const uintptr_t a0 = (reinterpret_cast<uintptr_t>(nrow + (int64_t)lo * 4) + 15u) & ~(uintptr_t)15u;
+    const uintptr_t a1 = reinterpret_cast<uintptr_t>(nrow + (int64_t)hi * 4) & ~(uintptr_t)15u;
+    if (a1 > a0) l2_prefetch_bulk(reinterpret_cast<const void*>(a0), (uint32_t)(a1 - a0));
+  }
 
   // ---- pass B: E = floor(exp_ds(y - m) * 2^40) in place, S = sum E
   uint64_t S = 0;
@@ -1147,9 +1164,7 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
   // ---- fused draft draw: the CTA whose range holds D finds the block of 32
   // groups holding it from the block sums, then the token inside it (warp 0)
   if (p.tokens && status == DSPARK_ST_OK) {
-    const int b = row / p.depth, j = row % p.depth;
-    const uint32_t req = p.request_ids ? p.request_ids[b] : (uint32_t)b;
-    const uint32_t D = draw_u32(p.seed, req, (uint32_t)j, DSPARK_PURPOSE_PROPOSAL) >> 8;
+    const uint32_t D = sh.draw;
     if (warp == 0 && D >= cbefore && D - cbefore < my_total) {
       const uint32_t t = D - cbefore;
       const int nblk = (ngroups + 31) / 32;

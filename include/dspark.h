@@ -352,6 +352,41 @@ int dspark_spec_step_noalloc(const void* draft_logits, int32_t draft_dtype, int6
                              int32_t* ratio_status, int32_t schedule, void* stream);
 
 /*
+ * dspark_spec_step_host -- dspark_spec_step on host buffers: the inputs are
+ * copied from host memory into the caller's device staging buffer, the step
+ * runs there, and the drafts and verification outputs are copied back to
+ * host memory.  Copies, kernels and copies are enqueued on `stream` in that
+ * order, as cudaMemcpyAsync calls (page-locked host memory keeps them
+ * asynchronous; pageable memory works but the host waits for each copy).
+ * The pages have no counterpart: this is the path of a caller whose logits
+ * are in host memory.
+ *
+ * Host inputs: h_draft_logits [B*depth][V] and h_target_logits
+ * [B*(depth+1)][V], rows contiguous (ld = V), dtypes as dspark_spec_step;
+ * h_temperature [B*depth] and h_request_ids [B] may be NULL (T = 1, ids
+ * 0..B-1).  Host outputs as dspark_spec_step: h_draft_tokens and
+ * h_row_status [B*depth] required, the greedy triple and the ratio triple
+ * each all or none (at least one mode), h_ratio_flags [B] may be NULL.
+ * staging: dspark_spec_step_host_staging_bytes(B, depth, V, draft_dtype,
+ * target_dtype) bytes of device memory, 256-byte aligned, owned by the
+ * caller; the step's q counts [B*depth][V] stay at its start (uint32).
+ * Overlapping calls need separate staging buffers.  Host argument errors as
+ * dspark_spec_step (DSPARK_ERR_ALIGN also for staging); a failed copy or
+ * launch returns its CUDA error code (> 0).
+ */
+int64_t dspark_spec_step_host_staging_bytes(int32_t B, int32_t depth, int32_t V,
+                                            int32_t draft_dtype, int32_t target_dtype);
+int dspark_spec_step_host(const void* h_draft_logits, int32_t draft_dtype,
+                          const void* h_target_logits, int32_t target_dtype, int32_t B,
+                          int32_t depth, int32_t V, const float* h_temperature, uint64_t seed,
+                          const uint32_t* h_request_ids, int32_t* h_draft_tokens,
+                          int32_t* h_row_status, int32_t* h_greedy_accept_len,
+                          int32_t* h_greedy_committed, int32_t* h_greedy_status,
+                          int32_t* h_ratio_accept_len, int32_t* h_ratio_committed,
+                          uint32_t* h_ratio_flags, int32_t* h_ratio_status, void* staging,
+                          int32_t schedule, void* stream);
+
+/*
  * dspark_target_probs -- the target distribution p of n_rows logit rows at
  * T = 1 ("PP1 q transport and scheduling design": the full target p after
  * the unchanged target processors, T = 1, top_p = 1), with the argmax

@@ -129,3 +129,30 @@ def test_sharded_argument_errors(lib):
     assert call(a3=0) == 0                               # empty batch
     assert lib.dspark_q_sharded_workspace_bytes(-1) == 0
     assert lib.dspark_q_sharded_workspace_bytes(3) == 3 * lib.dspark_q_sharded_workspace_bytes(1)
+
+
+def test_spec_step_host_argument_errors(lib):
+    f = lib.dspark_spec_step_host
+    # (draft, dd, target, td, B, depth, V, T, seed, req, tok, rst, g_acc, g_com, g_st, r_acc,
+    #  r_com, r_flags, r_st, staging, schedule, stream)
+    ok = [P, 0, P, 1, 2, 5, 8, None, 0, None, P, P, P, P, P, None, None, None, None,
+          ctypes.c_void_p(256), 0, None]
+
+    def call(**kw):
+        a = list(ok)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return f(*a)
+
+    assert call(a5=0) == -2                        # depth
+    assert call(a6=0) == -2                        # V
+    assert call(a1=9) == -3                        # dtype
+    assert call(a20=7) == -7                       # schedule
+    assert call(a19=None) == -1                    # no staging
+    assert call(a19=ctypes.c_void_p(272)) == -5    # staging not 256-byte aligned
+    assert call(a12=None, a13=None, a14=None) == -1  # no mode
+    assert call(a13=None) == -1                    # a partial greedy triple
+    assert call(a4=0) == 0                         # empty batch
+    sb = lib.dspark_spec_step_host_staging_bytes
+    assert sb(2, 5, 8, 0, 1) % 256 == 0 and sb(2, 5, 8, 0, 1) >= 2 * 5 * 8 * 8 + 2 * 6 * 8 * 2
+    assert sb(2, 0, 8, 0, 1) == 0 and sb(-1, 5, 8, 0, 1) == 0

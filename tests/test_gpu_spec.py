@@ -147,3 +147,45 @@ def test_verify_one_pass_equals_separate_calls(case):
     for m in ref:
         for x, y in zip(got[m], ref[m]):
             assert torch.equal(x, y), (case, m)
+
+
+@pytest.mark.parametrize("name,schedule", [("c2", ds.SCHEDULE_AUTO), ("c4", ds.SCHEDULE_SEPARATE),
+                                           ("c4", ds.SCHEDULE_ONE_LAUNCH)])
+def test_spec_step_host_equals_device_step(oracle, name, schedule):
+    """dspark_spec_step_host (host buffers, its own staging and copies) gives
+    the device step's outputs bit for bit, on two streams at once."""
+    wl = W.config2() if name == "c2" else W.config4(B=8)
+    d, t, temps, req = dev_inputs(wl)
+    ref_q, ref_tok, ref = fused(d, t, wl, temps, req, wl.modes, schedule)
+    B, depth, V = wl.B, wl.depth, wl.V
+    h_d = d.cpu().pin_memory()
+    h_t = t.cpu().pin_memory()
+    h_temp = temps.cpu().pin_memory()
+    h_req = req.cpu().pin_memory()
+    sb = ds.dspark_spec_step_host_staging_bytes(B, depth, V, ds._dtype_code(h_d),
+                                                ds._dtype_code(h_t))
+    outs = []
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    stagings = []
+    for s in streams:
+        pin = lambda shape: torch.full(shape, -9, dtype=torch.int32).pin_memory()
+        o = {"tok": pin((B, depth)), "rst": pin((B * depth,))}
+        if "greedy" in wl.modes:
+            o["greedy"] = (pin((B,)), pin((B, depth + 1)), pin((B,)))
+        if "ratio" in wl.modes:
+            o["ratio"] = (pin((B,)), pin((B, depth + 1)), pin((B,)), pin((B,)))
+        stg = torch.empty((sb,), dtype=torch.uint8, device="cuda")
+        stagings.append(stg)
+        ds.dspark_spec_step_host(h_d, h_t, B, depth, h_temp, wl.seed, h_req, o["tok"], o["rst"],
+                                 stg, greedy_out=o.get("greedy"), ratio_out=o.get("ratio"),
+                                 stream=s, schedule=schedule)
+        outs.append(o)
+    torch.cuda.synchronize()
+    for o, stg in zip(outs, stagings):
+        assert torch.equal(o["tok"], ref_tok.cpu())
+        assert torch.equal(o["rst"], ref_q["status"].cpu())
+        # the q counts stay at the start of the staging buffer
+        counts = stg[: B * depth * V * 4].view(torch.int32).view(B * depth, V)
+        assert torch.equal(counts, ref_q["counts"])
+        for m in wl.modes:
+            assert all(torch.equal(x, y.cpu()) for x, y in zip(o[m], ref[m])), m
