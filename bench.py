@@ -153,7 +153,8 @@ def max_over_ranks(values):
 PROFILES = {
     ("q_build_sample", "dense"): ("q_dense_c4_b64.md", ("q_dense.cu", "q_dense.cuh", "common.cuh"),
                                   "traffic_bytes_per_row"),
-    ("q_build_sample", "topk"): ("q_topk_c3_b64.md", ("q_topk.cu", "common.cuh"),
+    ("q_build_sample", "topk"): ("q_topk_c3_b64.md", ("q_topk.cu", "common.cuh",
+                                                       "support_alloc.cuh"),
                                  "traffic_bytes_per_row"),
 }
 
