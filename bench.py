@@ -68,6 +68,10 @@ def parse():
                     help="skip the vocabulary-sharded (TP2 emulation) q build measurement")
     ap.add_argument("--schedule", default="auto", choices=["auto", "one", "separate"],
                     help="dense q: one persistent launch, or q build then one verify pass")
+    ap.add_argument("--sweep", action="store_true",
+                    help="the batch sweep (B in 1..1024, top-256 q, all-accept and all-reject "
+                         "targets, greedy and ratio timed apart): one JSON line per (B, "
+                         "variant) instead of the single bench line")
     return ap.parse_args()
 
 
@@ -559,6 +563,97 @@ def cpu_baseline(wl, budget_s):
                                                                 secs)}
 
 
+def run_sweep(args):
+    """The batch sweep of the benchmark definition: B in {1, 8, 32, 128, 512,
+    1024} x depth 5 x V = 129,280 with the Zipf generators and a top-256 q,
+    the all-accept (target = draft) and all-reject (target mass off the draft
+    support) extremes; the q build with its draw and each verification mode
+    are timed apart with CUDA events, and each line gives rows/s and
+    algorithmic GB/s per mode."""
+    import torch
+
+    import draft_sampling_verification_gb300 as ds
+    from draft_sampling_verification_gb300 import build as dsbuild
+    from draft_sampling_verification_gb300 import workloads as W
+
+    dsbuild.build()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    peak = (load_peaks() or {}).get("hbm_gbs")
+    for B in (1, 8, 32, 128, 512, 1024):
+        for variant in ("accept", "reject"):
+            wl = W.config5(B, variant=variant)
+            depth, V, k = wl.depth, wl.V, wl.top_k
+            xd = torch.from_numpy(wl.draft).to(dev)
+            xt = torch.from_numpy(wl.target).to(dev)
+            in_bytes = wl.draft.nbytes + wl.target.nbytes
+            n_copies = max(1, -(-3 * L2_BYTES // in_bytes)) if in_bytes < 3 * L2_BYTES else 1
+            copies = [(xd, xt)] + [(xd.clone(), xt.clone()) for _ in range(n_copies - 1)]
+            temps = torch.from_numpy(wl.temperature).to(dev)
+            req = torch.from_numpy(wl.request_ids.view(np.int32)).to(dev)
+            rows_d = B * depth
+            counts = torch.empty((rows_d, k), dtype=torch.int32, device=dev)
+            ids = torch.empty((rows_d, k), dtype=torch.int32, device=dev)
+            nnz = torch.empty((rows_d,), dtype=torch.int32, device=dev)
+            qst = torch.empty((rows_d,), dtype=torch.int32, device=dev)
+            tok = torch.empty((B, depth), dtype=torch.int32, device=dev)
+            i32 = lambda *shape: torch.empty(shape, dtype=torch.int32, device=dev)
+            g = (i32(B), i32(B, depth + 1), i32(B))
+            r = (i32(B), i32(B, depth + 1), i32(B), i32(B))
+
+            def q_build(i):
+                ds.dspark_q_build_sample(copies[i % n_copies][0], B, depth, temps, k, wl.seed,
+                                         req, counts, ids, nnz, tok, qst, stream)
+
+            def verify(i, mode):
+                ds.dspark_verify(copies[i % n_copies][1], B, depth, tok,
+                                 g if mode == "greedy" else None,
+                                 r if mode == "ratio" else None, counts, ids, nnz, k, wl.seed,
+                                 req, stream)
+
+            def timed(fn):
+                for i in range(max(3, args.warmup)):
+                    fn(i)
+                torch.cuda.synchronize()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for i in range(args.steps):
+                    fn(i)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                return e0.elapsed_time(e1) / args.steps
+
+            q_ms = timed(q_build)
+            q_build(0)
+            per_mode = {}
+            for mode in ("greedy", "ratio"):
+                v_ms = timed(lambda i, m=mode: verify(i, m))
+                verify(0, mode)
+                torch.cuda.synchronize()
+                out = g if mode == "greedy" else r
+                assert int((out[-1] != 0).sum()) == 0, "refused requests in the sweep"
+                acc = out[0].cpu().numpy()
+                ab = algorithmic_bytes(wl, acc if mode == "greedy" else None,
+                                       acc if mode == "ratio" else None)
+                step_ms = q_ms + v_ms
+                per_mode[mode] = {
+                    "verify_ms": round(v_ms, 4), "step_ms": round(step_ms, 4),
+                    "verify_rows_per_s": B * (depth + 1) / (step_ms * 1e-3),
+                    "step_gbs": (ab["q_build_sample"] + ab["verify"]) / (step_ms * 1e-3) / 1e9,
+                    "verify_gbs": ab["verify"] / (v_ms * 1e-3) / 1e9,
+                    "mean_accept_len": float(acc.mean())}
+            qb = algorithmic_bytes(wl, np.zeros(B, np.int32), None)["q_build_sample"]
+            print(json.dumps({
+                "sweep": "batch sweep, top-%d q" % k, "B": B, "variant": variant,
+                "q_build_ms": round(q_ms, 4), "q_build_gbs": qb / (q_ms * 1e-3) / 1e9,
+                "hbm_peak_gbs": peak, "modes": per_mode,
+                "l2": "inputs larger than L2" if n_copies == 1 else
+                      "inputs rotated over %d copies" % n_copies}), flush=True)
+            del copies, xd, xt
+            torch.cuda.empty_cache()
+
+
 def run_reference(args, rank, world):
     from draft_sampling_verification_gb300 import workloads as W
     if rank != 0:
@@ -596,6 +691,9 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.sweep:
+        run_sweep(args)
         return
     import torch
     if world > 1:
