@@ -345,47 +345,64 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
       e.fl = sh.timeout ? 1u : 0u;
     }
     cluster.sync();
-    if (tid == 0) {
-      // peers' partials in rank order (identical in every CTA)
+    if (warp == 0) {
+      // peers' partials, fetched at once (lane r reads rank r), then merged in
+      // rank order by every lane (identical in every CTA)
+      float pm = -INFINITY, ps = 0.0f, pav = -INFINITY;
+      int pai = 0x7FFFFFFF;
+      uint32_t pfl = 0;
+      if (lane < NC) {
+        const VX* e = cluster.map_shared_rank(&sh.x[xi], lane);
+        pm = e->m;
+        ps = e->s;
+        pav = e->amv;
+        pai = e->ami;
+        pfl = e->fl;
+      }
       float m = -INFINITY, s = 0.0f, av = -INFINITY;
       int ai = 0x7FFFFFFF;
       uint32_t fl = 0;
       bool bad = false;
+#pragma unroll
       for (int r = 0; r < NC; ++r) {
-        const VX* e = cluster.map_shared_rank(&sh.x[xi], r);
-        const float m2 = e->m;
-        fl |= e->fl;
+        const float m2 = __shfl_sync(0xffffffffu, pm, r);
+        const float s2 = __shfl_sync(0xffffffffu, ps, r);
+        const float av2 = __shfl_sync(0xffffffffu, pav, r);
+        const int ai2 = __shfl_sync(0xffffffffu, pai, r);
+        fl |= __shfl_sync(0xffffffffu, pfl, r);
         if (!(m2 < INFINITY)) bad = true;  // NaN or +inf in that slice
-        if (kD && need_r) ms_merge(m, s, bad ? -INFINITY : m2, bad ? 0.0f : e->s);
+        if (kD && need_r) ms_merge(m, s, bad ? -INFINITY : m2, bad ? 0.0f : s2);
         else m = fmaxf(m, m2);
-        if (kG && need_g) am_merge(av, ai, e->amv, e->ami);
+        if (kG && need_g) am_merge(av, ai, av2, ai2);
       }
-      sh.M = bad ? NAN : m;
-      sh.S = s;
-      sh.AMV = av;
-      sh.AMI = ai;
-      sh.FL = fl;
-      if (kR && need_r && j < depth && !bad && m > -INFINITY && !(fl & 1u)) {
-        // the ratio test: accept iff U * c < p(x) * 2^48
-        int dec = 0, dst = DSPARK_ST_OK;
-        uint32_t dfl = 0;
-        if (p.top_k > 0 && !sh.q_ok) {
-          dec = -1;
-          dst = DSPARK_ST_BAD_Q;
-        } else if (cx == 0u) {
-          dec = -1;
-          dst = DSPARK_ST_BAD_DRAFT;
-        } else {
-          const float px = (zx == -INFINITY) ? 0.0f : __fdiv_rn(expf(zx - m), s);
-          const double uc = (double)((uint64_t)U * (uint64_t)cx);
-          const double p48 = (double)px * 281474976710656.0;
-          if (fabs(uc * 0x1p-48 - (double)px) <= 1e-6 * ((double)cx * 0x1p-24))
-            dfl = DSPARK_FLAG_AMBIG_ACCEPT;
-          dec = (uc < p48) ? 1 : 0;
+      if (lane == 0) {
+        sh.M = bad ? NAN : m;
+        sh.S = s;
+        sh.AMV = av;
+        sh.AMI = ai;
+        sh.FL = fl;
+        if (kR && need_r && j < depth && !bad && m > -INFINITY && !(fl & 1u)) {
+          // the ratio test: accept iff U * c < p(x) * 2^48
+          int dec = 0, dst = DSPARK_ST_OK;
+          uint32_t dfl = 0;
+          if (p.top_k > 0 && !sh.q_ok) {
+            dec = -1;
+            dst = DSPARK_ST_BAD_Q;
+          } else if (cx == 0u) {
+            dec = -1;
+            dst = DSPARK_ST_BAD_DRAFT;
+          } else {
+            const float px = (zx == -INFINITY) ? 0.0f : __fdiv_rn(expf(zx - m), s);
+            const double uc = (double)((uint64_t)U * (uint64_t)cx);
+            const double p48 = (double)px * 281474976710656.0;
+            if (fabs(uc * 0x1p-48 - (double)px) <= 1e-6 * ((double)cx * 0x1p-24))
+              dfl = DSPARK_FLAG_AMBIG_ACCEPT;
+            dec = (uc < p48) ? 1 : 0;
+          }
+          sh.dec = dec;
+          sh.dst = dst;
+          sh.dflags = dfl;
         }
-        sh.dec = dec;
-        sh.dst = dst;
-        sh.dflags = dfl;
       }
     }
     xi ^= 1;
@@ -539,18 +556,22 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
         sh.x[xi].cs = c2;
       }
       cluster.sync();
-      if (tid == 0) {
-        uint64_t before = 0, Z = 0, CS = 0;
-        for (int r = 0; r < NC; ++r) {
-          const VX* e = cluster.map_shared_rank(&sh.x[xi], r);
-          const uint64_t zr = e->z;
-          if (r < rank) before += zr;
-          Z += zr;
-          CS += e->cs;
+      if (warp == 0) {
+        // peers' masses, fetched at once (lane r reads rank r); exact sums
+        uint64_t zr = 0, cr = 0;
+        if (lane < NC) {
+          const VX* e = cluster.map_shared_rank(&sh.x[xi], lane);
+          zr = e->z;
+          cr = e->cs;
         }
-        sh.Z = Z;
-        sh.before = before;
-        sh.CS = CS;
+        const uint64_t before = warp_reduce(lane < rank ? zr : 0ull, OpAddU64());
+        const uint64_t Z = warp_reduce(zr, OpAddU64());
+        const uint64_t CS = warp_reduce(cr, OpAddU64());
+        if (lane == 0) {
+          sh.Z = Z;
+          sh.before = before;
+          sh.CS = CS;
+        }
       }
       xi ^= 1;
       __syncthreads();
