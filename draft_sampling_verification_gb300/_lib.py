@@ -16,7 +16,7 @@ INCLUDE = os.path.join(os.path.dirname(_HERE), "include")
 HEADERS = [os.path.join(INCLUDE, "dspark.h"), os.path.join(INCLUDE, "dspark_debug.h")]
 
 _P = ctypes.c_void_p
-_I32, _I64, _U64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64
+_I32, _I64, _U64, _U32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_uint32
 
 SIGNATURES = {
     "dspark_q_build": [_P, _I32, _I64, _I32, _I32, _P, _I32, _P, _P, _P, _P, _P],
@@ -46,6 +46,7 @@ SIGNATURES = {
     "dspark_debug_exp_weights": [_P, _I64, _P, _P, _P],
     "dspark_debug_philox": [_P, _U64, _I64, _P, _P],
     "dspark_debug_alloc_scale": [_P, _I64, _P, _P, _P, _P, _P],
+    "dspark_debug_wait": [_I32, _P, _U32, _P, _P],
 }
 
 _lock = threading.Lock()

@@ -471,6 +471,26 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t phase)
   return false;
 }
 
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Waits (at most kWaitLimitNs) until *flag >= target, another CTA's release
+// seen through an acquire load; false on timeout.
+static __device__ __noinline__ bool wait_count(const uint32_t* flag, uint32_t target) {
+  if (ld_acquire(flag) >= target) return true;
+  const uint64_t t0 = global_ns();
+  uint32_t nap = 64;
+  while (global_ns() - t0 < kWaitLimitNs) {
+    __nanosleep(nap);
+    if (ld_acquire(flag) >= target) return true;
+    nap = nap < 1024u ? 2u * nap : 1024u;
+  }
+  return false;
+}
+
 // Float holding an integer in [0, 2^23) to int, by the 2^23 offset trick.
 __device__ __forceinline__ int small_float_to_int(float v) {
   return __float_as_int(__fadd_rn(v, 8388608.0f)) - 0x4B000000;

@@ -34,6 +34,22 @@ __global__ void philox_kernel(const uint4* ctr, uint64_t seed, int64_t n, uint4*
     out[i] = dspark::philox4x32_10(ctr[i], (uint32_t)seed, (uint32_t)(seed >> 32));
 }
 
+__global__ void wait_kernel(int which, const uint32_t* count, uint32_t target, int32_t* status) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  bool ok;
+  if (which == 2) {
+    ok = dspark::wait_count(count, target);
+  } else {
+    dspark::mbar_init(&bar, 2);
+    dspark::mbar_init_fence();
+    dspark::mbar_arrive_expect_tx(&bar, 0);
+    if (which == 1) dspark::mbar_arrive_expect_tx(&bar, 0);
+    ok = dspark::mbar_wait_bounded(&bar, 0);
+  }
+  *status = ok ? DSPARK_ST_OK : DSPARK_ST_TIMEOUT;
+}
+
 int grid_for(int64_t n) {
   const int64_t g = (n + 255) / 256;
   return (int)(g < 152 * 16 ? (g < 1 ? 1 : g) : 152 * 16);
@@ -81,6 +97,17 @@ int dspark_debug_philox(const uint32_t* ctr, uint64_t seed, int64_t n, uint32_t*
     return DSPARK_ERR_ALIGN;
   philox_kernel<<<grid_for(n), 256, 0, static_cast<cudaStream_t>(stream)>>>(
       reinterpret_cast<const uint4*>(ctr), seed, n, reinterpret_cast<uint4*>(out));
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? 0 : (int)e;
+}
+
+int dspark_debug_wait(int32_t which, const uint32_t* count, uint32_t target, int32_t* status,
+                      void* stream) {
+  if (which < 0 || which > 2) return DSPARK_ERR_ARG;
+  if (!status || (which == 2 && !count)) return DSPARK_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(status) & 3) || (reinterpret_cast<uintptr_t>(count) & 3))
+    return DSPARK_ERR_ALIGN;
+  wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(which, count, target, status);
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? 0 : (int)e;
 }

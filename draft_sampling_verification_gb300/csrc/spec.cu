@@ -67,25 +67,6 @@ __device__ __forceinline__ void decode_item(int k, const WorkParams& w, bool* ve
   *idx = (w.B - l) + (k - n2);
 }
 
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// Waits (at most 2 s) until *flag >= target.
-__device__ bool wait_count(const uint32_t* flag, uint32_t target) {
-  if (ld_acquire(flag) >= target) return true;
-  const uint64_t t0 = global_ns();
-  uint32_t nap = 64;
-  while (global_ns() - t0 < kWaitLimitNs) {
-    __nanosleep(nap);
-    if (ld_acquire(flag) >= target) return true;
-    nap = nap < 1024u ? 2u * nap : 1024u;
-  }
-  return false;
-}
-
 // The two phases as calls, so that each is register-allocated on its own.
 __device__ __noinline__ void q_row(const qdense::Params& qp, int row, qdense::DShared& sh,
                                    float* sl, uint64_t* mbar, uint32_t& phase, uint32_t* ready) {

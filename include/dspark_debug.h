@@ -45,6 +45,22 @@ int dspark_debug_alloc_scale(const uint64_t* S, int64_t n, uint64_t* mk_out, int
 int dspark_debug_philox(const uint32_t* ctr, uint64_t seed, int64_t n, uint32_t* out,
                         void* stream);
 
+/*
+ * The library's two bounded waits, run once on one thread so that their
+ * time limit can be seen to work (2 s; the kernels that use them report
+ * DSPARK_ST_TIMEOUT when it runs out, and the context stays usable):
+ *   which = 0: an mbarrier expecting two arrivals gets one, then is waited on
+ *              (the wait of every bulk copy into shared memory) -- it never
+ *              completes;
+ *   which = 1: the same mbarrier gets both arrivals, then is waited on;
+ *   which = 2: waits until *count >= target with acquire loads (the fused
+ *              step's wait for a request's q rows); count is device memory.
+ * *status (device) = DSPARK_ST_OK if the wait ended by its condition,
+ * DSPARK_ST_TIMEOUT if it gave up.  Other `which`: DSPARK_ERR_ARG.
+ */
+int dspark_debug_wait(int32_t which, const uint32_t* count, uint32_t target, int32_t* status,
+                      void* stream);
+
 #ifdef __cplusplus
 }
 #endif

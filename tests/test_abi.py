@@ -156,3 +156,10 @@ def test_spec_step_host_argument_errors(lib):
     sb = lib.dspark_spec_step_host_staging_bytes
     assert sb(2, 5, 8, 0, 1) % 256 == 0 and sb(2, 5, 8, 0, 1) >= 2 * 5 * 8 * 8 + 2 * 6 * 8 * 2
     assert sb(2, 0, 8, 0, 1) == 0 and sb(-1, 5, 8, 0, 1) == 0
+
+
+def test_debug_wait_argument_errors(lib):
+    assert lib.dspark_debug_wait(3, None, 0, P, None) == -7      # which
+    assert lib.dspark_debug_wait(0, None, 0, None, None) == -1   # no status
+    assert lib.dspark_debug_wait(2, None, 1, P, None) == -1      # count wait without a counter
+    assert lib.dspark_debug_wait(0, None, 0, ctypes.c_void_p(18), None) == -5
