@@ -65,6 +65,9 @@ struct __align__(16) Push {
 
 // Many-member path: member positions compacted per window, then the table of
 // distinct exact fractions (read by peers), then every peer's table merged.
+// steps of 32 slice positions in one warp's segment of the slice, at most
+constexpr int kAtSteps = ((DSPARK_MAX_V / kCl + 8) / kWarps + 31) / 32 + 1;
+
 struct ManyShared {
   union {
     uint16_t list[kWin];
@@ -72,6 +75,7 @@ struct ManyShared {
       uint64_t key[kCl * kTab];
       uint32_t cnt[kCl * kTab];
     } merged;
+    uint32_t atm[kWarps * kAtSteps];  // members at the threshold fraction, per step
   };
   uint64_t tkey[kTab];
   uint32_t tcnt[kTab];
@@ -112,6 +116,7 @@ struct DShared {
   int sel_bin;
   uint32_t sel_above, sel_count, scan_base;
   uint32_t draw;  // the row's 24-bit draft draw (fused draw only)
+  uint32_t n_merged;  // many-member path: non-empty merged table slots
 };
 constexpr int kAllCap = kBins * 4 / (int)sizeof(Cand);
 
@@ -787,14 +792,15 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
     if (lane == 0) sh.wred32[0] = t;
   }
   // exact fractions of the listed members
-  auto exact_key = [&](int s) -> uint64_t {
-    const float x = load_logit(xrow, p.dtype, (int64_t)(lo - off + s));
+  auto key_of_x = [&](float x) -> uint64_t {
     const float y = scale ? __fmul_rn(x, invT) : x;
     uint32_t Ei;
     int se;
     weight_split_ef(weight40(__fsub_rn(y, m)), &Ei, &se);
     return frac_key(alloc_split(Ei, se, mk, ek));
   };
+  auto x_at = [&](int s) -> float { return load_logit(xrow, p.dtype, (int64_t)(lo - off + s)); };
+  auto exact_key = [&](int s) -> uint64_t { return key_of_x(x_at(s)); };
   const uint32_t my_cand = sh.n_cand;
   for (uint32_t j = tid; j < min(my_cand, (uint32_t)kCandCap); j += kThr)
     sh.cand[j].key = exact_key(sh.cand[j].s);
@@ -938,11 +944,22 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
       for (int i = 0; i < kPer; ++i)
         if ((bits >> i) & 1u) ms.list[o++] = (uint16_t)(p0 + i);
       __syncthreads();
-      for (uint32_t j0 = 0; j0 < tot; j0 += kThr) {
+      // four rounds of members at a time: their logits are reloaded together
+      for (uint32_t j4 = 0; j4 < tot; j4 += 4 * kThr) {
+        float xs[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t j = j4 + u * kThr + tid;
+          xs[u] = j < tot ? x_at((int)ms.list[j]) : 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+        const uint32_t j0 = j4 + u * kThr;
+        if (j0 >= tot) break;  // the same for every thread
         const uint32_t j = j0 + tid;
         const bool valid = j < tot;
         const int sp = valid ? (int)ms.list[j] : 0;
-        const uint64_t key = valid ? exact_key(sp) : ~0ull;
+        const uint64_t key = valid ? key_of_x(xs[u]) : ~0ull;
         if (valid) {
           kmn = min(kmn, key);
           kmx = max(kmx, key);
@@ -968,6 +985,7 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
           if (cls < (uint32_t)kTab) set_low(sp, kMark | cls);
           else tovf = 1u;
         }
+        }
       }
       __syncthreads();
     }
@@ -980,17 +998,23 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
       sh.pub.kmax = kmx;
     }
     cluster.sync();  // tables published
-    if (tid == 0) {
+    if (warp == 0) {
+      // every peer's flags and key range, fetched at once (lane r reads rank r)
       uint32_t fo = 0;
       uint64_t a = ~0ull, bb = 0ull;
-      for (int r = 0; r < kCl; ++r) {
-        fo |= *cluster.map_shared_rank(&sh.pub.flags4, r);
-        a = min(a, *cluster.map_shared_rank(&sh.pub.kmin, r));
-        bb = max(bb, *cluster.map_shared_rank(&sh.pub.kmax, r));
+      if (lane < kCl) {
+        fo = *cluster.map_shared_rank(&sh.pub.flags4, lane);
+        a = *cluster.map_shared_rank(&sh.pub.kmin, lane);
+        bb = *cluster.map_shared_rank(&sh.pub.kmax, lane);
       }
-      sh.fovf = fo;
-      sh.gmin = a;
-      sh.gmax = bb;
+      fo = warp_reduce(fo, OpOrU32());
+      a = warp_reduce(a, OpMinU64());
+      bb = warp_reduce(bb, OpMaxU64());
+      if (lane == 0) {
+        sh.fovf = fo;
+        sh.gmin = a;
+        sh.gmax = bb;
+      }
     }
     __syncthreads();
     uint32_t mine = 0;
@@ -999,23 +1023,30 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
       if (tid == 0) {
         sh.thrk = 0ull;
         sh.need = 0u;
-      }
-      for (int t = tid; t < kCl * kTab; t += kThr) {
-        const int r = t / kTab, slot = t % kTab;
-        ms.merged.key[t] = *cluster.map_shared_rank(&ms.tkey[slot], r);
-        ms.merged.cnt[t] = *cluster.map_shared_rank(&ms.tcnt[slot], r);
+        sh.n_merged = 0u;
       }
       __syncthreads();
-      // the threshold fraction holds the Rin-th ticket: above < Rin <= above + at
+      // the non-empty slots of every table of the row, gathered here (a
+      // fraction held by several CTAs keeps one slot per CTA)
       for (int t = tid; t < kCl * kTab; t += kThr) {
-        if (ms.merged.cnt[t] == 0u) continue;
+        const int r = t / kTab, slot = t % kTab;
+        const uint32_t c = *cluster.map_shared_rank(&ms.tcnt[slot], r);
+        if (c == 0u) continue;
+        const uint32_t q = atomicAdd(&sh.n_merged, 1u);
+        ms.merged.key[q] = *cluster.map_shared_rank(&ms.tkey[slot], r);
+        ms.merged.cnt[q] = c;
+      }
+      __syncthreads();
+      const int nmg = (int)sh.n_merged;
+      // the threshold fraction holds the Rin-th ticket: above < Rin <= above + at
+      for (int t = tid; t < nmg; t += kThr) {
         const uint64_t kt = ms.merged.key[t];
         uint32_t above = 0, at = 0;
-        for (int u = 0; u < kCl * kTab; ++u) {
+        for (int u = 0; u < nmg; ++u) {
           const uint32_t cu = ms.merged.cnt[u];
           const uint64_t ku = ms.merged.key[u];
-          above += (cu != 0u && ku > kt) ? cu : 0u;
-          at += (cu != 0u && ku == kt) ? cu : 0u;
+          above += (ku > kt) ? cu : 0u;
+          at += (ku == kt) ? cu : 0u;
         }
         if (above < Rin && Rin <= above + at) {
           sh.thrk = kt;
@@ -1033,6 +1064,7 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
       // none; those at it are counted per warp segment (id order)
       const int seg = (npos + kWarps - 1) / kWarps;
       const int a0 = warp * seg, a1 = min(npos, a0 + seg);
+      uint32_t* atm = ms.atm + warp * kAtSteps;  // the merged tables are no longer read
       uint32_t wat = 0;
       for (int s0 = a0; s0 < a1; s0 += 32) {
         const int sp = s0 + lane;
@@ -1044,7 +1076,9 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
         } else if (stt == 0) {
           set_low(sp, thr);
         }
-        wat += (uint32_t)__popc(__ballot_sync(0xffffffffu, stt == 2));
+        const unsigned at = __ballot_sync(0xffffffffu, stt == 2);
+        if (lane == 0) atm[(s0 - a0) >> 5] = at;
+        wat += (uint32_t)__popc(at);
       }
       if (lane == 0) sh.wcnt[warp] = wat;
       __syncthreads();
@@ -1054,19 +1088,21 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
         sh.pub.n_eq = t;
       }
       cluster.sync();
-      if (tid == 0) {
-        uint32_t base = 0;
-        for (int r = 0; r < rank; ++r) base += *cluster.map_shared_rank(&sh.pub.n_eq, r);
-        sh.scan_base = base;
+      if (warp == 0) {
+        // members at the threshold in the lower ranks, fetched at once
+        const uint32_t e = lane < rank ? *cluster.map_shared_rank(&sh.pub.n_eq, lane) : 0u;
+        const uint32_t base = warp_reduce(e, OpAddU32());
+        if (lane == 0) sh.scan_base = base;
       }
       __syncthreads();
       uint32_t base = sh.scan_base;
       for (int w = 0; w < warp; ++w) base += sh.wcnt[w];
       const uint32_t need = sh.need;
       for (int s0 = a0; s0 < a1; s0 += 32) {
+        const unsigned msk = atm[(s0 - a0) >> 5];
+        if (msk == 0u) continue;  // the same for the whole warp
         const int sp = s0 + lane;
-        const bool at = (sp < a1) && cls_state(low_of(sp)) == 2;
-        const unsigned msk = __ballot_sync(0xffffffffu, at);
+        const bool at = (msk >> lane) & 1u;
         if (at) {
           const uint32_t rk = base + (uint32_t)__popc(msk & ((1u << lane) - 1u));
           set_low(sp, thr);
