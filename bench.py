@@ -527,6 +527,12 @@ def run_ours(args, rank, world, local_rank):
 
 
 # ------------------------------------------------------------ CPU oracle
+def target_rows_f32(wl, b):
+    """Request b's target rows as fp32 [1, depth+1, V] (bf16 widened exactly)."""
+    t = wl.target[b:b + 1]
+    return t if wl.target_dtype == "f32" else (t.astype(np.uint32) << 16).view(np.float32)
+
+
 def oracle_sample_run(wl, n_req, budget_s):
     """Runs the oracle over up to n_req requests of the workload within about
     budget_s seconds; returns (requests done, seconds)."""
@@ -540,7 +546,7 @@ def oracle_sample_run(wl, n_req, budget_s):
         counts, ids, nnz, st = O.q_build(x, wl.temperature[b * depth:(b + 1) * depth], wl.top_k)
         tok, sst = O.draft_sample(counts, ids, nnz, wl.top_k, 1, depth, wl.seed,
                                   wl.request_ids[b:b + 1], V=V)
-        z = wl.target_f32()[b:b + 1]
+        z = target_rows_f32(wl, b)
         drafts = tok.reshape(1, depth)
         for m in wl.modes:
             if m == "greedy":
@@ -554,22 +560,103 @@ def oracle_sample_run(wl, n_req, budget_s):
     return done, time.perf_counter() - t0
 
 
+# ---- the oracle over a process pool: the workload's arrays sit in shared
+#      memory (written once, outside the timed region); a task is one request
+_POOL_WL = {}
+
+
+def oracle_pool_init(meta):
+    """Pool worker start: attach the workload's shared arrays, load the oracle."""
+    from multiprocessing import shared_memory
+
+    from oracle import oracle as O
+    O.build()
+    O.lib()
+    for key in ("draft", "target"):
+        name, shape, dtype = meta[key]
+        shm = shared_memory.SharedMemory(name=name)
+        _POOL_WL[key + "_shm"] = shm  # kept open for the worker's life
+        _POOL_WL[key] = np.ndarray(shape, dtype=np.dtype(dtype), buffer=shm.buf)
+    _POOL_WL.update({k: meta[k] for k in ("temperature", "request_ids", "top_k", "seed", "modes",
+                                          "target_dtype")})
+
+
+def oracle_pool_request(b):
+    """One request through the oracle (q build, draft sample, verification)."""
+    from oracle import oracle as O
+    w = _POOL_WL
+    x = w["draft"][b]
+    depth, V = x.shape
+    t = w["target"][b:b + 1]
+    z = t if w["target_dtype"] == "f32" else (t.astype(np.uint32) << 16).view(np.float32)
+    top_k, seed, req = w["top_k"], w["seed"], w["request_ids"][b:b + 1]
+    counts, ids, nnz, st = O.q_build(x, w["temperature"][b * depth:(b + 1) * depth], top_k)
+    tok, sst = O.draft_sample(counts, ids, nnz, top_k, 1, depth, seed, req, V=V)
+    drafts = tok.reshape(1, depth)
+    for m in w["modes"]:
+        if m == "greedy":
+            O.verify_greedy(z, drafts)
+        else:
+            O.verify_ratio(z, drafts, counts, ids, nnz, top_k, seed, req)
+    return b
+
+
 def cpu_baseline(wl, budget_s):
+    """The oracle on the host cores: one thread, then requests spread over a
+    process pool (spawn) of every core this process may run on."""
     n, secs = oracle_sample_run(wl, wl.B, budget_s)
     rows = n * (wl.depth + 1)
-    return {"value": rows / secs, "unit": "verify rows/s", "cores": 1, "kind": "oracle",
-            "sample": "%d of %d requests of the same workload (q build, draft sample, %s "
-                      "verification), single thread, %.1f s" % (n, wl.B, "+".join(wl.modes),
-                                                                secs)}
+    single = {"value": rows / secs, "unit": "verify rows/s", "cores": 1,
+              "sample": "%d of %d requests, one thread, %.1f s" % (n, wl.B, secs)}
+    out = {"value": single["value"], "unit": "verify rows/s", "cores": 1, "kind": "oracle",
+           "sample": "%d of %d requests of the same workload (q build, draft sample, %s "
+                     "verification), single thread, %.1f s" % (n, wl.B, "+".join(wl.modes), secs),
+           "single_thread": single}
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    if not cores or cores < 2 or n < 1:
+        return out
+    import multiprocessing as mp
+    from concurrent.futures import ProcessPoolExecutor
+    from multiprocessing import shared_memory
+    per_req = secs / n
+    n_par = int(min(wl.B, max(cores, cores * budget_s / per_req)))  # about budget_s of wall time
+    shms = []
+    try:
+        meta = {"temperature": np.ascontiguousarray(wl.temperature),
+                "request_ids": np.ascontiguousarray(wl.request_ids), "top_k": wl.top_k,
+                "seed": wl.seed, "modes": tuple(wl.modes), "target_dtype": wl.target_dtype}
+        for key, arr in (("draft", wl.draft), ("target", wl.target)):
+            arr = np.ascontiguousarray(arr)
+            shm = shared_memory.SharedMemory(create=True, size=max(1, arr.nbytes))
+            shms.append(shm)
+            np.ndarray(arr.shape, dtype=arr.dtype, buffer=shm.buf)[...] = arr
+            meta[key] = (shm.name, arr.shape, arr.dtype.str)
+        with ProcessPoolExecutor(max_workers=cores, mp_context=mp.get_context("spawn"),
+                                 initializer=oracle_pool_init, initargs=(meta,)) as ex:
+            list(ex.map(int, range(cores)))  # every worker started and attached
+            t0 = time.perf_counter()
+            list(ex.map(oracle_pool_request, range(n_par)))
+            psecs = time.perf_counter() - t0
+    finally:
+        for shm in shms:
+            shm.close()
+            shm.unlink()
+    out.update({"value": n_par * (wl.depth + 1) / psecs, "cores": cores,
+                "sample": "%d of %d requests of the same workload (q build, draft sample, %s "
+                          "verification) spread over a pool of %d processes, %.1f s; the "
+                          "single-thread figure is beside it" % (n_par, wl.B, "+".join(wl.modes),
+                                                                cores, psecs)})
+    return out
 
 
 def run_sweep(args):
     """The batch sweep of the benchmark definition: B in {1, 8, 32, 128, 512,
-    1024} x depth 5 x V = 129,280 with the Zipf generators and a top-256 q,
-    the all-accept (target = draft) and all-reject (target mass off the draft
-    support) extremes; the q build with its draw and each verification mode
-    are timed apart with CUDA events, and each line gives rows/s and
-    algorithmic GB/s per mode."""
+    1024} x depth 5 x V = 129,280 with the Zipf generators, a top-256 and a
+    dense q, the all-accept (target = draft) and all-reject (target mass off
+    the draft support) extremes; the q build with its draw and each
+    verification mode are timed apart with CUDA events, and each line gives
+    rows/s and algorithmic GB/s per mode."""
+    import dataclasses
     import torch
 
     import draft_sampling_verification_gb300 as ds
@@ -580,78 +667,88 @@ def run_sweep(args):
     dev = torch.device("cuda", 0)
     stream = torch.cuda.current_stream(dev)
     peak = (load_peaks() or {}).get("hbm_gbs")
-    for B in (1, 8, 32, 128, 512, 1024):
-        for variant in ("accept", "reject"):
-            wl = W.config5(B, variant=variant)
-            depth, V, k = wl.depth, wl.V, wl.top_k
-            xd = torch.from_numpy(wl.draft).to(dev)
-            xt = torch.from_numpy(wl.target).to(dev)
-            in_bytes = wl.draft.nbytes + wl.target.nbytes
-            n_copies = max(1, -(-3 * L2_BYTES // in_bytes)) if in_bytes < 3 * L2_BYTES else 1
-            copies = [(xd, xt)] + [(xd.clone(), xt.clone()) for _ in range(n_copies - 1)]
-            temps = torch.from_numpy(wl.temperature).to(dev)
-            req = torch.from_numpy(wl.request_ids.view(np.int32)).to(dev)
-            rows_d = B * depth
+    def run_one(wl, B, variant, q_kind):
+        depth, V, k = wl.depth, wl.V, wl.top_k
+        xd = torch.from_numpy(wl.draft).to(dev)
+        xt = torch.from_numpy(wl.target).to(dev)
+        in_bytes = wl.draft.nbytes + wl.target.nbytes
+        n_copies = max(1, -(-3 * L2_BYTES // in_bytes)) if in_bytes < 3 * L2_BYTES else 1
+        copies = [(xd, xt)] + [(xd.clone(), xt.clone()) for _ in range(n_copies - 1)]
+        temps = torch.from_numpy(wl.temperature).to(dev)
+        req = torch.from_numpy(wl.request_ids.view(np.int32)).to(dev)
+        rows_d = B * depth
+        if k > 0:
             counts = torch.empty((rows_d, k), dtype=torch.int32, device=dev)
             ids = torch.empty((rows_d, k), dtype=torch.int32, device=dev)
             nnz = torch.empty((rows_d,), dtype=torch.int32, device=dev)
-            qst = torch.empty((rows_d,), dtype=torch.int32, device=dev)
-            tok = torch.empty((B, depth), dtype=torch.int32, device=dev)
-            i32 = lambda *shape: torch.empty(shape, dtype=torch.int32, device=dev)
-            g = (i32(B), i32(B, depth + 1), i32(B))
-            r = (i32(B), i32(B, depth + 1), i32(B), i32(B))
+        else:
+            counts = torch.empty((rows_d, V), dtype=torch.int32, device=dev)
+            ids = nnz = None
+        qst = torch.empty((rows_d,), dtype=torch.int32, device=dev)
+        tok = torch.empty((B, depth), dtype=torch.int32, device=dev)
+        i32 = lambda *shape: torch.empty(shape, dtype=torch.int32, device=dev)
+        g = (i32(B), i32(B, depth + 1), i32(B))
+        r = (i32(B), i32(B, depth + 1), i32(B), i32(B))
 
-            def q_build(i):
-                ds.dspark_q_build_sample(copies[i % n_copies][0], B, depth, temps, k, wl.seed,
-                                         req, counts, ids, nnz, tok, qst, stream)
+        def q_build(i):
+            ds.dspark_q_build_sample(copies[i % n_copies][0], B, depth, temps, k, wl.seed,
+                                     req, counts, ids, nnz, tok, qst, stream)
 
-            def verify(i, mode):
-                ds.dspark_verify(copies[i % n_copies][1], B, depth, tok,
-                                 g if mode == "greedy" else None,
-                                 r if mode == "ratio" else None, counts, ids, nnz, k, wl.seed,
-                                 req, stream)
+        def verify(i, mode):
+            ds.dspark_verify(copies[i % n_copies][1], B, depth, tok,
+                             g if mode == "greedy" else None,
+                             r if mode == "ratio" else None, counts, ids, nnz, k, wl.seed,
+                             req, stream)
 
-            def timed(fn):
-                for i in range(max(3, args.warmup)):
-                    fn(i)
-                torch.cuda.synchronize()
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                for i in range(args.steps):
-                    fn(i)
-                e1.record(stream)
-                torch.cuda.synchronize()
-                return e0.elapsed_time(e1) / args.steps
+        def timed(fn):
+            for i in range(max(3, args.warmup)):
+                fn(i)
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(args.steps):
+                fn(i)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) / args.steps
 
-            q_ms = timed(q_build)
-            q_build(0)
-            per_mode = {}
-            for mode in ("greedy", "ratio"):
-                v_ms = timed(lambda i, m=mode: verify(i, m))
-                verify(0, mode)
-                torch.cuda.synchronize()
-                out = g if mode == "greedy" else r
-                assert int((out[-1] != 0).sum()) == 0, "refused requests in the sweep"
-                acc = out[0].cpu().numpy()
-                ab = algorithmic_bytes(wl, acc if mode == "greedy" else None,
-                                       acc if mode == "ratio" else None)
-                step_ms = q_ms + v_ms
-                per_mode[mode] = {
-                    "verify_ms": round(v_ms, 4), "step_ms": round(step_ms, 4),
-                    "verify_rows_per_s": B * (depth + 1) / (step_ms * 1e-3),
-                    "step_gbs": (ab["q_build_sample"] + ab["verify"]) / (step_ms * 1e-3) / 1e9,
-                    "verify_gbs": ab["verify"] / (v_ms * 1e-3) / 1e9,
-                    "mean_accept_len": float(acc.mean())}
-            qb = algorithmic_bytes(wl, np.zeros(B, np.int32), None)["q_build_sample"]
-            print(json.dumps({
-                "sweep": "batch sweep, top-%d q" % k, "B": B, "variant": variant,
-                "q_build_ms": round(q_ms, 4), "q_build_gbs": qb / (q_ms * 1e-3) / 1e9,
-                "hbm_peak_gbs": peak, "modes": per_mode,
-                "l2": "inputs larger than L2" if n_copies == 1 else
-                      "inputs rotated over %d copies" % n_copies}), flush=True)
-            del copies, xd, xt
-            torch.cuda.empty_cache()
+        q_ms = timed(q_build)
+        q_build(0)
+        per_mode = {}
+        for mode in ("greedy", "ratio"):
+            v_ms = timed(lambda i, m=mode: verify(i, m))
+            verify(0, mode)
+            torch.cuda.synchronize()
+            out = g if mode == "greedy" else r
+            assert int((out[-1] != 0).sum()) == 0, "refused requests in the sweep"
+            acc = out[0].cpu().numpy()
+            ab = algorithmic_bytes(wl, acc if mode == "greedy" else None,
+                                   acc if mode == "ratio" else None)
+            step_ms = q_ms + v_ms
+            per_mode[mode] = {
+                "verify_ms": round(v_ms, 4), "step_ms": round(step_ms, 4),
+                "verify_rows_per_s": B * (depth + 1) / (step_ms * 1e-3),
+                "step_gbs": (ab["q_build_sample"] + ab["verify"]) / (step_ms * 1e-3) / 1e9,
+                "verify_gbs": ab["verify"] / (v_ms * 1e-3) / 1e9,
+                "mean_accept_len": float(acc.mean())}
+        qb = algorithmic_bytes(wl, np.zeros(B, np.int32), None)["q_build_sample"]
+        print(json.dumps({
+            "sweep": "batch sweep, %s q" % ("top-%d" % k if k else "dense"), "B": B,
+            "variant": variant, "q": q_kind,
+            "q_build_ms": round(q_ms, 4), "q_build_gbs": qb / (q_ms * 1e-3) / 1e9,
+            "hbm_peak_gbs": peak, "modes": per_mode,
+            "l2": "inputs larger than L2" if n_copies == 1 else
+                  "inputs rotated over %d copies" % n_copies}), flush=True)
+        del copies, xd, xt
+        torch.cuda.empty_cache()
+
+    for B in (1, 8, 32, 128, 512, 1024):
+        for variant in ("accept", "reject"):
+            wl_gen = W.config5(B, variant=variant)
+            for q_kind in ("sparse", "dense"):
+                run_one(wl_gen if q_kind == "sparse" else dataclasses.replace(wl_gen, top_k=0),
+                        B, variant, q_kind)
 
 
 def run_reference(args, rank, world):
