@@ -1,6 +1,7 @@
 // api.cu -- the extern "C" entry points declared in include/dspark.h.  Host
 // code only: argument checks (nothing is launched on a bad argument), then
 // one kernel launch on the caller's stream.  No allocation, no host sync.
+#include <nvtx3/nvToolsExt.h>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -69,6 +70,15 @@ cudaError_t launch_target_probs(const void* z, int dtype, int64_t ld, int n_rows
 
 namespace {
 
+// One NVTX range per ABI call, named after the call (a no-op unless a tool
+// such as Nsight Systems is attached).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
 constexpr int kMaxGridRows = (1 << 30) / 8;  // rows per launch (8-CTA clusters)
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -98,6 +108,7 @@ const char* dspark_version(void) { return "dspark-gb300 0.1 (" DSPARK_QSEM ", sm
 int dspark_q_build(const void* draft_logits, int32_t dtype, int64_t ld, int32_t n_rows, int32_t V,
                    const float* temperature, int32_t top_k, uint32_t* counts, int32_t* sparse_ids,
                    int32_t* nnz, int32_t* row_status, void* stream) {
+  const NvtxRange nvtx_range("dspark_q_build");
   if (int e = check_common(dtype, V, ld)) return e;
   if (int e = check_topk(top_k, V)) return e;
   if (n_rows < 0 || n_rows > kMaxGridRows) return DSPARK_ERR_SIZE;
@@ -122,6 +133,7 @@ int dspark_q_build_sample(const void* draft_logits, int32_t dtype, int64_t ld, i
                           uint64_t seed, const uint32_t* request_ids, uint32_t* counts,
                           int32_t* sparse_ids, int32_t* nnz, int32_t* draft_tokens,
                           int32_t* row_status, void* stream) {
+  const NvtxRange nvtx_range("dspark_q_build_sample");
   if (int e = check_common(dtype, V, ld)) return e;
   if (int e = check_topk(top_k, V)) return e;
   if (depth < 1 || depth > DSPARK_MAX_DEPTH) return DSPARK_ERR_SIZE;
@@ -149,6 +161,7 @@ int dspark_draft_sample(const uint32_t* counts, const int32_t* sparse_ids, const
                         int32_t top_k, int32_t B, int32_t depth, int32_t V, uint64_t seed,
                         const uint32_t* request_ids, int32_t* draft_tokens, int32_t* row_status,
                         void* stream) {
+  const NvtxRange nvtx_range("dspark_draft_sample");
   if (V < 1 || V > DSPARK_MAX_V) return DSPARK_ERR_SIZE;
   if (depth < 1 || depth > DSPARK_MAX_DEPTH) return DSPARK_ERR_SIZE;
   if (B < 0 || (int64_t)B * depth > (int64_t)(1 << 30)) return DSPARK_ERR_SIZE;
@@ -185,6 +198,7 @@ int dspark_verify_greedy(const void* target_logits, int32_t dtype, int64_t ld, i
                          int32_t depth, int32_t V, const int32_t* draft_tokens,
                          int32_t* accept_len, int32_t* committed, int32_t* req_status,
                          void* stream) {
+  const NvtxRange nvtx_range("dspark_verify_greedy");
   const int e = check_verify(target_logits, dtype, ld, B, depth, V, draft_tokens, accept_len,
                              committed, req_status);
   if (e != 0) return e > 0 ? 0 : e;
@@ -200,6 +214,7 @@ int dspark_verify_ratio(const void* target_logits, int32_t dtype, int64_t ld, in
                         int32_t top_k, uint64_t seed, const uint32_t* request_ids,
                         int32_t* accept_len, int32_t* committed, uint32_t* flags,
                         int32_t* req_status, void* stream) {
+  const NvtxRange nvtx_range("dspark_verify_ratio");
   const int e = check_verify(target_logits, dtype, ld, B, depth, V, draft_tokens, accept_len,
                              committed, req_status);
   if (e != 0) return e > 0 ? 0 : e;
@@ -220,6 +235,7 @@ int dspark_verify_match(const void* target_logits, int32_t dtype, int64_t ld, in
                         int32_t depth, int32_t V, const int32_t* draft_tokens, uint64_t seed,
                         const uint32_t* request_ids, int32_t* accept_len, int32_t* committed,
                         uint32_t* flags, int32_t* req_status, void* stream) {
+  const NvtxRange nvtx_range("dspark_verify_match");
   const int e = check_verify(target_logits, dtype, ld, B, depth, V, draft_tokens, accept_len,
                              committed, req_status);
   if (e != 0) return e > 0 ? 0 : e;
@@ -238,6 +254,7 @@ int dspark_verify(const void* target_logits, int32_t dtype, int64_t ld, int32_t 
                   int32_t* greedy_committed, int32_t* greedy_status, int32_t* ratio_accept_len,
                   int32_t* ratio_committed, uint32_t* ratio_flags, int32_t* ratio_status,
                   void* stream) {
+  const NvtxRange nvtx_range("dspark_verify");
   const bool g = greedy_accept_len || greedy_committed || greedy_status;
   const bool r = ratio_accept_len || ratio_committed || ratio_status;
   if (!g && !r) return DSPARK_ERR_NULL;
@@ -323,6 +340,7 @@ int dspark_spec_step(const void* draft_logits, int32_t draft_dtype, int64_t ld_d
                      int32_t* greedy_status, int32_t* ratio_accept_len, int32_t* ratio_committed,
                      uint32_t* ratio_flags, int32_t* ratio_status, uint32_t* workspace,
                      int32_t schedule, void* stream) {
+  const NvtxRange nvtx_range("dspark_spec_step");
   return spec_step_impl(draft_logits, draft_dtype, ld_draft, target_logits, target_dtype,
                         ld_target, B, depth, V, temperature, seed, request_ids, counts,
                         draft_tokens, row_status, greedy_accept_len, greedy_committed,
@@ -339,6 +357,7 @@ int dspark_spec_step_noalloc(const void* draft_logits, int32_t draft_dtype, int6
                              int32_t* greedy_status, int32_t* ratio_accept_len,
                              int32_t* ratio_committed, uint32_t* ratio_flags,
                              int32_t* ratio_status, int32_t schedule, void* stream) {
+  const NvtxRange nvtx_range("dspark_spec_step_noalloc");
   return spec_step_impl(draft_logits, draft_dtype, ld_draft, target_logits, target_dtype,
                         ld_target, B, depth, V, temperature, seed, request_ids, counts,
                         draft_tokens, row_status, greedy_accept_len, greedy_committed,
@@ -401,6 +420,7 @@ int dspark_spec_step_host(const void* h_draft_logits, int32_t draft_dtype,
                           int32_t* h_ratio_accept_len, int32_t* h_ratio_committed,
                           uint32_t* h_ratio_flags, int32_t* h_ratio_status, void* staging,
                           int32_t schedule, void* stream) {
+  const NvtxRange nvtx_range("dspark_spec_step_host");
   if (int e = check_common(draft_dtype, V, V)) return e;
   if (int e = check_common(target_dtype, V, V)) return e;
   if (depth < 1 || depth > DSPARK_MAX_DEPTH) return DSPARK_ERR_SIZE;
@@ -462,6 +482,7 @@ int dspark_q_chain_sample(const void* draft_logits, int32_t dtype, int64_t ld, i
                           const uint32_t* request_ids, float* workspace, uint32_t* counts,
                           int32_t* draft_tokens, int32_t* row_status, float* margins,
                           void* stream) {
+  const NvtxRange nvtx_range("dspark_q_chain_sample");
   if (int e = check_common(dtype, V, ld)) return e;
   if (depth < 1 || depth > DSPARK_MAX_DEPTH) return DSPARK_ERR_SIZE;
   if (B < 0 || (int64_t)B * depth > kMaxGridRows) return DSPARK_ERR_SIZE;
@@ -490,6 +511,7 @@ int dspark_q_build_sample_sharded(const void* draft_logits, int32_t dtype, int64
                                   const uint32_t* request_ids, uint32_t* counts,
                                   int32_t* sparse_ids, int32_t* nnz, int32_t* draft_tokens,
                                   int32_t* row_status, void* workspace, void* stream) {
+  const NvtxRange nvtx_range("dspark_q_build_sample_sharded");
   if (int e = check_common(dtype, V, ld)) return e;
   if (int e = check_topk(top_k, V)) return e;
   if (depth < 1 || depth > DSPARK_MAX_DEPTH) return DSPARK_ERR_SIZE;
@@ -512,6 +534,7 @@ int dspark_q_build_sample_sharded(const void* draft_logits, int32_t dtype, int64
 int dspark_q_pack(const uint32_t* counts, const int32_t* sparse_ids, const int32_t* nnz,
                   int32_t top_k, int32_t n_rows, int32_t V, float* q_out,
                   uint64_t* checksum_out, void* stream) {
+  const NvtxRange nvtx_range("dspark_q_pack");
   if (V < 1 || V > DSPARK_MAX_V) return DSPARK_ERR_SIZE;
   if (int e = check_topk(top_k, V)) return e;
   if (n_rows < 0 || n_rows > kMaxGridRows) return DSPARK_ERR_SIZE;
@@ -530,6 +553,7 @@ int dspark_q_validate(const float* q, const int32_t* sparse_ids, const int32_t* 
                       int32_t top_k, int32_t n_rows, int32_t V, const int32_t* tokens,
                       const uint64_t* expect, uint32_t* counts_out, int32_t* row_status,
                       void* stream) {
+  const NvtxRange nvtx_range("dspark_q_validate");
   if (V < 1 || V > DSPARK_MAX_V) return DSPARK_ERR_SIZE;
   if (int e = check_topk(top_k, V)) return e;
   if (n_rows < 0 || n_rows > kMaxGridRows) return DSPARK_ERR_SIZE;
@@ -548,6 +572,7 @@ int dspark_q_validate(const float* q, const int32_t* sparse_ids, const int32_t* 
 int dspark_target_probs(const void* target_logits, int32_t dtype, int64_t ld, int32_t n_rows,
                         int32_t V, float* p_out, int32_t* argmax, int32_t* row_status,
                         void* stream) {
+  const NvtxRange nvtx_range("dspark_target_probs");
   if (int e = check_common(dtype, V, ld)) return e;
   if (n_rows < 0 || n_rows > kMaxGridRows) return DSPARK_ERR_SIZE;
   if (n_rows == 0) return 0;
