@@ -54,8 +54,13 @@ struct __align__(16) VX {
   uint32_t pad[3];
 };
 
+constexpr int kVMaxNC = 8;  // the largest verify cluster
+
 struct VSh2 {
   VX x[2];
+  // every CTA's partials, pushed here by each CTA before the cluster barrier
+  // ([buffer][writer's rank]), so that after it the merge reads local memory
+  VX px[2][kVMaxNC];
   uint64_t bsum[kVMaxBlocks];
   float wm[8], ws[8], wam[8];
   int wai[8];
@@ -95,20 +100,6 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
-// (m, s) pairs: s is a sum of exp(z - m); merged to the larger m.
-__device__ __forceinline__ void ms_merge(float& m, float& s, float m2, float s2) {
-  const float M = fmaxf(m, m2);
-  if (M == -INFINITY) {
-    m = M;
-    s = 0.0f;
-    return;
-  }
-  const float a = (m == -INFINITY) ? 0.0f : s * expf(m - M);
-  const float c = (m2 == -INFINITY) ? 0.0f : s2 * expf(m2 - M);
-  m = M;
-  s = a + c;
 }
 
 __device__ __forceinline__ void am_merge(float& v, int& i, float v2, int i2) {
@@ -344,36 +335,50 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
       e.ami = ai;
       e.fl = sh.timeout ? 1u : 0u;
     }
+    if (warp == 0) {
+      // this CTA's partials into every peer's slot for it (lane r writes rank r)
+      __syncwarp();
+      if (lane < NC) *cluster.map_shared_rank(&sh.px[xi][rank], lane) = sh.x[xi];
+    }
     cluster.sync();
     if (warp == 0) {
-      // peers' partials, fetched at once (lane r reads rank r), then merged in
-      // rank order by every lane (identical in every CTA)
+      // every CTA's partials, from local memory (lane r holds rank r), then
+      // merged in rank order by every lane (identical in every CTA)
       float pm = -INFINITY, ps = 0.0f, pav = -INFINITY;
       int pai = 0x7FFFFFFF;
       uint32_t pfl = 0;
       if (lane < NC) {
-        const VX* e = cluster.map_shared_rank(&sh.x[xi], lane);
-        pm = e->m;
-        ps = e->s;
-        pav = e->amv;
-        pai = e->ami;
-        pfl = e->fl;
+        const VX& e = sh.px[xi][lane];
+        pm = e.m;
+        ps = e.s;
+        pav = e.amv;
+        pai = e.ami;
+        pfl = e.fl;
       }
-      float m = -INFINITY, s = 0.0f, av = -INFINITY;
-      int ai = 0x7FFFFFFF;
-      uint32_t fl = 0;
-      bool bad = false;
+      // a tree over the NC lanes (lane 0 ends with the row's values, the same
+      // in every CTA): the flags, the max and the argmax (lowest id among the
+      // maxima) are exact; each slice's sum is rescaled to the row max in its
+      // own lane, and the rescaled sums are added pairwise
+      const bool bad = __any_sync(0xffffffffu, !(pm < INFINITY));  // NaN or +inf
+      float m = (pm < INFINITY) ? pm : -INFINITY;
+      uint32_t fl = pfl;
+      float av = pav;
+      int ai = pai;
 #pragma unroll
-      for (int r = 0; r < NC; ++r) {
-        const float m2 = __shfl_sync(0xffffffffu, pm, r);
-        const float s2 = __shfl_sync(0xffffffffu, ps, r);
-        const float av2 = __shfl_sync(0xffffffffu, pav, r);
-        const int ai2 = __shfl_sync(0xffffffffu, pai, r);
-        fl |= __shfl_sync(0xffffffffu, pfl, r);
-        if (!(m2 < INFINITY)) bad = true;  // NaN or +inf in that slice
-        if (kD && need_r) ms_merge(m, s, bad ? -INFINITY : m2, bad ? 0.0f : s2);
-        else m = fmaxf(m, m2);
-        if (kG && need_g) am_merge(av, ai, av2, ai2);
+      for (int o = NC / 2; o > 0; o >>= 1) {
+        fl |= __shfl_xor_sync(0xffffffffu, fl, o);
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (kG && need_g) {
+          const float av2 = __shfl_xor_sync(0xffffffffu, av, o);
+          const int ai2 = __shfl_xor_sync(0xffffffffu, ai, o);
+          am_merge(av, ai, av2, ai2);
+        }
+      }
+      float s = 0.0f;
+      if (kD && need_r) {
+        s = (pm > -INFINITY && pm < INFINITY && m > -INFINITY) ? ps * expf(pm - m) : 0.0f;
+#pragma unroll
+        for (int o = NC / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
       }
       if (lane == 0) {
         sh.M = bad ? NAN : m;
@@ -555,14 +560,22 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
         sh.x[xi].z = a;
         sh.x[xi].cs = c2;
       }
+      if (warp == 0) {
+        // this CTA's masses into every peer's slot for it
+        __syncwarp();
+        if (lane < NC) {
+          VX* dst = cluster.map_shared_rank(&sh.px[xi][rank], lane);
+          dst->z = sh.x[xi].z;
+          dst->cs = sh.x[xi].cs;
+        }
+      }
       cluster.sync();
       if (warp == 0) {
-        // peers' masses, fetched at once (lane r reads rank r); exact sums
+        // every CTA's masses, from local memory (lane r holds rank r); exact sums
         uint64_t zr = 0, cr = 0;
         if (lane < NC) {
-          const VX* e = cluster.map_shared_rank(&sh.x[xi], lane);
-          zr = e->z;
-          cr = e->cs;
+          zr = sh.px[xi][lane].z;
+          cr = sh.px[xi][lane].cs;
         }
         const uint64_t before = warp_reduce(lane < rank ? zr : 0ull, OpAddU64());
         const uint64_t Z = warp_reduce(zr, OpAddU64());
