@@ -524,8 +524,12 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
             gsum += wfix(r);
           }
         }
-        // one block = the 32 groups of one warp in one iteration
-        const uint64_t bs = warp_reduce(gsum, OpAddU64());
+        // one block = the 32 groups of one warp in one iteration; gsum is at
+        // most EPG * 2^46 < 2^50 (r <= p <= 1), summed as two 25-bit halves
+        // with the 32-bit warp reduction
+        const uint32_t blo = __reduce_add_sync(0xffffffffu, (uint32_t)(gsum & 0x1FFFFFFull));
+        const uint32_t bhi = __reduce_add_sync(0xffffffffu, (uint32_t)(gsum >> 25));
+        const uint64_t bs = ((uint64_t)bhi << 25) + blo;
         if (lane == 0 && gb / 32 + warp < nblk) sh.bsum[gb / 32 + warp] = bs;
         zs += gsum;
       }
