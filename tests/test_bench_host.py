@@ -1,0 +1,49 @@
+"""Host-side parts of bench.py, on CPU: the per-request bf16 widening the
+oracle baseline uses, the oracle baseline over a process pool (same
+outputs as one thread), and the algorithmic byte counts."""
+import numpy as np
+
+import bench
+from draft_sampling_verification_gb300 import workloads as W
+
+
+def test_target_rows_f32_widens_one_request_exactly():
+    wl = W.config4(B=3, V=257)
+    for b in range(wl.B):
+        got = bench.target_rows_f32(wl, b)
+        assert got.shape == (1, wl.depth + 1, wl.V) and got.dtype == np.float32
+        assert np.array_equal(got[0], wl.target_f32()[b])
+
+
+def test_pool_requests_match_one_thread(oracle):
+    wl = W.config4(B=4, V=1031)
+    # the pool worker's request function, run in this process, against the
+    # single-thread loop's oracle calls
+    meta = {"draft": wl.draft, "target": wl.target, "temperature": wl.temperature,
+            "request_ids": wl.request_ids, "top_k": wl.top_k, "seed": wl.seed,
+            "modes": tuple(wl.modes), "target_dtype": wl.target_dtype}
+    bench._POOL_WL.clear()
+    bench._POOL_WL.update(meta)
+    for b in range(wl.B):
+        assert bench.oracle_pool_request(b) == b
+    n, secs = bench.oracle_sample_run(wl, wl.B, 60.0)
+    assert n == wl.B and secs > 0
+
+
+def test_cpu_baseline_reports_pool_and_single_thread(oracle):
+    wl = W.config4(B=8, V=1031)
+    out = bench.cpu_baseline(wl, 0.5)
+    assert out["kind"] == "oracle" and out["unit"] == "verify rows/s" and out["value"] > 0
+    assert out["single_thread"]["cores"] == 1 and out["single_thread"]["value"] > 0
+    assert out["cores"] >= 1
+
+
+def test_algorithmic_bytes_dense_and_sparse():
+    wl = W.config4(B=2, V=1031)
+    acc = np.array([0, wl.depth], np.int32)
+    ab = bench.algorithmic_bytes(wl, acc, acc)
+    rows_d = wl.B * wl.depth
+    assert ab["q_build_sample"] == rows_d * wl.V * 8 + rows_d * 4
+    # request 0 reads 1 target row and its q row (a rejection); request 1 reads all 6
+    esz = 2 if wl.target_dtype == "bf16" else 4
+    assert ab["verify"] == (1 + wl.depth + 1) * wl.V * esz + wl.V * 4
