@@ -156,6 +156,37 @@ __device__ __forceinline__ AllocSplit split_of(float y, float m, uint64_t mk, in
   return alloc_split(Ei, se, mk, ek);
 }
 
+// The dense kernel's certified float split of a = RN64(E k): with k = khi +
+// klo + d (|d| <= 2^-48 k), p1 + e1 = E khi exactly (fma) and p2 = RN32(E klo),
+// fr = RN(RN(p1 - f0) + RN(e1 + p2)) is within 2^-13 + 2^-34.4 p1 of
+// 2048 (a - f0) / 2048.  When 2048 fr is at least 2^-12 + 2^-15 from every
+// integer and p1 < 2^19, floor(a) = f0 + floor(G / 2048) and the bin
+// floor(2048 r) = G mod 2048 (G = floor(2048 fr)) are exact and r > 0;
+// otherwise cert is false and the exact integer split decides (about 1
+// element in 2,000).  E = 0 is certified with f = 0 and no fraction.
+struct TpFast {
+  uint32_t f, bin;
+  bool cert, zero;
+};
+__device__ __forceinline__ TpFast tp_fast_split(float Ef, float khi, float klo) {
+  TpFast o;
+  const float p1 = __fmul_rn(Ef, khi);
+  const float e1 = __fmaf_rn(Ef, khi, -p1);
+  const float p2 = __fmul_rn(Ef, klo);
+  const float f0 = floorf(p1);
+  const float fr = __fadd_rn(__fsub_rn(p1, f0), __fadd_rn(e1, p2));
+  const float fb = __fmul_rn(fr, 2048.0f);
+  const float G = floorf(fb);
+  o.zero = (Ef == 0.0f);
+  o.cert = o.zero || (fabsf(__fsub_rn(__fsub_rn(fb, G), 0.5f)) < 0.5f - 0x1p-12f - 0x1p-15f &&
+                      f0 < 524285.0f);  // 2^19 - 3
+  const int f0i = __float_as_int(__fadd_rn(f0, 12582912.0f)) - 0x4B400000;
+  const int Gi = __float_as_int(__fadd_rn(G, 12582912.0f)) - 0x4B400000;
+  o.f = o.zero ? 0u : (uint32_t)(f0i + (Gi >> 11));
+  o.bin = (uint32_t)Gi & (kTpBins - 1u);
+  return o;
+}
+
 __global__ void __launch_bounds__(kTpThr) tp_max_kernel(TpParams p) {
   __shared__ TpShared sh;
   const Shard d = shard_of(p);
@@ -217,12 +248,24 @@ __global__ void __launch_bounds__(kTpThr) tp_floors_kernel(TpParams p) {
     for (int s = 0; s < p.n_sh; ++s) S += w.S[s];
     const AllocScale k = alloc_scale(S);
     for (int v = d.lo + threadIdx.x; v < d.hi; v += kTpThr) {
-      const AllocSplit a = split_of(y_of(p, d.row, v, invT), m, k.mk, k.ek);
-      p.counts[(int64_t)d.row * p.V + v] = a.f;
-      F += a.f;
-      if (a.rnum != 0ull) {
+      const float Ef = weight40(__fsub_rn(y_of(p, d.row, v, invT), m));
+      const TpFast q = tp_fast_split(Ef, k.khi, k.klo);
+      uint32_t f = q.f, bin = q.bin;
+      bool pos = !q.zero;
+      if (!q.cert) {
+        uint32_t Ei;
+        int se;
+        weight_split_ef(Ef, &Ei, &se);
+        const AllocSplit a = alloc_split(Ei, se, k.mk, k.ek);
+        f = a.f;
+        pos = a.rnum != 0ull;
+        bin = bin_of(a);
+      }
+      p.counts[(int64_t)d.row * p.V + v] = f;
+      F += f;
+      if (pos) {
         ++npos;
-        atomicAdd(&sh.hist[bin_of(a)], 1u);
+        atomicAdd(&sh.hist[bin], 1u);
       }
     }
   }
@@ -270,6 +313,35 @@ __device__ __forceinline__ int grant_state(const TpParams& p, const TpRow& w, in
   return st;
 }
 
+// One element of the grant pass: an element above the threshold bin gets
+// f + 1; a member of the bin is marked in its count and returns true with
+// its exact fraction's key.
+__device__ __forceinline__ bool grant_one(const TpParams& p, const Shard& d, int v, float invT,
+                                          float m, const AllocScale& k, int bstar,
+                                          uint64_t* key) {
+  const float Ef = weight40(__fsub_rn(y_of(p, d.row, v, invT), m));
+  const TpFast q = tp_fast_split(Ef, k.khi, k.klo);
+  if (q.zero) return false;
+  int b = (int)q.bin;
+  uint32_t f = q.f;
+  AllocSplit a;
+  if (!q.cert || b == bstar) {  // the exact split: open elements, and the key of a member
+    uint32_t Ei;
+    int se;
+    weight_split_ef(Ef, &Ei, &se);
+    a = alloc_split(Ei, se, k.mk, k.ek);
+    if (a.rnum == 0ull) return false;
+    b = (int)bin_of(a);
+    f = a.f;
+  }
+  uint32_t* c = p.counts + (int64_t)d.row * p.V + v;
+  if (b > bstar) *c = f + 1u;
+  if (b != bstar) return false;
+  *c = f | kTpMark;  // its exact split was taken above
+  *key = frac_key(a);
+  return true;
+}
+
 __global__ void __launch_bounds__(kTpThr) tp_grant_kernel(TpParams p) {
   const Shard d = shard_of(p);
   TpRow& w = p.ws[d.row];
@@ -284,16 +356,14 @@ __global__ void __launch_bounds__(kTpThr) tp_grant_kernel(TpParams p) {
   uint64_t S = 0;
   for (int s = 0; s < p.n_sh; ++s) S += w.S[s];
   const AllocScale k = alloc_scale(S);
-  for (int v = d.lo + threadIdx.x; v < d.hi; v += kTpThr) {
-    const AllocSplit a = split_of(y_of(p, d.row, v, invT), m, k.mk, k.ek);
-    if (a.rnum == 0ull) continue;
-    const int b = (int)bin_of(a);
-    if (b > bstar) {
-      p.counts[(int64_t)d.row * p.V + v] = a.f + 1u;
-    } else if (b == bstar) {
-      p.counts[(int64_t)d.row * p.V + v] = a.f | kTpMark;
-      // count the fraction in the shard's table (open addressing)
-      const uint64_t key = frac_key(a);
+  for (int v0 = d.lo; v0 < d.hi; v0 += kTpThr) {  // whole warps: the table insert below
+    const int v = v0 + (int)threadIdx.x;
+    uint64_t key = kTpEmpty;
+    const bool member = v < d.hi && grant_one(p, d, v, invT, m, k, bstar, &key);
+    // count the members' fractions in the shard's table (open addressing),
+    // one atomic per distinct fraction in the warp
+    const unsigned grp = __match_any_sync(0xffffffffu, member ? key : kTpEmpty);
+    if (member && (int)(threadIdx.x & 31u) == __ffs(grp) - 1) {
       uint32_t h = (uint32_t)((key * 0x9E3779B97F4A7C15ull) >> 54) & (kTpTab - 1);
       bool done = false;
       for (int probe = 0; probe < kTpTab && !done; ++probe) {
@@ -301,7 +371,7 @@ __global__ void __launch_bounds__(kTpThr) tp_grant_kernel(TpParams p) {
             reinterpret_cast<unsigned long long*>(&w.tab_key[d.s][(h + probe) & (kTpTab - 1)]);
         const unsigned long long prev = atomicCAS(slot, (unsigned long long)kTpEmpty, key);
         if (prev == kTpEmpty || prev == key) {
-          atomicAdd(&w.tab_cnt[d.s][(h + probe) & (kTpTab - 1)], 1u);
+          atomicAdd(&w.tab_cnt[d.s][(h + probe) & (kTpTab - 1)], (uint32_t)__popc(grp));
           done = true;
         }
       }
@@ -371,15 +441,21 @@ __global__ void __launch_bounds__(kTpThr) tp_threshold_kernel(TpParams p) {
       if (sh.found < 0) st = DSPARK_ST_INTERNAL;  // the tables miss members of the bin
     }
   }
+  // each rank's members at T (every thread scans part of every table), then
+  // each rank's quota of them, ranks in id order
+  const bool want = st == DSPARK_ST_OK && R > 0;
+  uint32_t at_s[kTpMaxShards];
+  for (int s = 0; s < p.n_sh; ++s) {
+    uint32_t c = 0;
+    if (want)
+      for (int j = threadIdx.x; j < kTpTab; j += kTpThr)
+        if (w.tab_key[s][j] == Tsh) c += w.tab_cnt[s][j];
+    at_s[s] = block_reduce(c, OpAddU32(), sh.r32);
+  }
   if (threadIdx.x == 0) {
-    // each rank's quota of members at T, ranks in id order
-    uint32_t need = st == DSPARK_ST_OK && R > 0 ? (uint32_t)sh.found : 0u;
+    uint32_t need = want ? (uint32_t)sh.found : 0u;
     for (int s = 0; s < p.n_sh; ++s) {
-      uint32_t at_s = 0;
-      if (need > 0u)
-        for (int j = 0; j < kTpTab; ++j)
-          if (w.tab_key[s][j] == Tsh) at_s += w.tab_cnt[s][j];
-      const uint32_t q = min(need, at_s);
+      const uint32_t q = min(need, at_s[s]);
       w.quota[s] = q;
       need -= q;
     }
@@ -424,7 +500,7 @@ __global__ void __launch_bounds__(kTpThr) tp_ties_kernel(TpParams p) {
         if (key > T) c += 1u;
         else if (key == T) at = 1u;
       }
-      if (quota > 0u) {  // uniform over the block
+      if (quota > 0u && __syncthreads_or(at)) {  // uniform over the block
         uint32_t tot;
         const uint32_t incl = block_inclusive_scan(at, sh.r32, &tot);
         if (at && base + incl - 1u < quota) c += 1u;
