@@ -601,6 +601,58 @@ def oracle_pool_request(b):
     return b
 
 
+class OraclePool:
+    """A spawn process pool of every core this process may run on, with the
+    workload's arrays in shared memory (written once, outside any timing);
+    run(indices) times the oracle over those requests, one task each."""
+
+    def __init__(self, wl):
+        self.wl = wl
+        self.cores = (len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity")
+                      else os.cpu_count()) or 1
+        self.shms = []
+        self.ex = None
+
+    def __enter__(self):
+        import multiprocessing as mp
+        from concurrent.futures import ProcessPoolExecutor
+        from multiprocessing import shared_memory
+        wl = self.wl
+        meta = {"temperature": np.ascontiguousarray(wl.temperature),
+                "request_ids": np.ascontiguousarray(wl.request_ids), "top_k": wl.top_k,
+                "seed": wl.seed, "modes": tuple(wl.modes), "target_dtype": wl.target_dtype}
+        try:
+            for key, arr in (("draft", wl.draft), ("target", wl.target)):
+                arr = np.ascontiguousarray(arr)
+                shm = shared_memory.SharedMemory(create=True, size=max(1, arr.nbytes))
+                self.shms.append(shm)
+                np.ndarray(arr.shape, dtype=arr.dtype, buffer=shm.buf)[...] = arr
+                meta[key] = (shm.name, arr.shape, arr.dtype.str)
+            self.ex = ProcessPoolExecutor(max_workers=self.cores,
+                                          mp_context=mp.get_context("spawn"),
+                                          initializer=oracle_pool_init, initargs=(meta,))
+            list(self.ex.map(int, range(self.cores)))  # every worker started and attached
+        except BaseException:
+            self.__exit__(None, None, None)
+            raise
+        return self
+
+    def run(self, indices):
+        t0 = time.perf_counter()
+        list(self.ex.map(oracle_pool_request, list(indices)))
+        return time.perf_counter() - t0
+
+    def __exit__(self, *exc):
+        if self.ex is not None:
+            self.ex.shutdown()
+            self.ex = None
+        for shm in self.shms:
+            shm.close()
+            shm.unlink()
+        self.shms = []
+        return False
+
+
 def cpu_baseline(wl, budget_s):
     """The oracle on the host cores: one thread, then requests spread over a
     process pool (spawn) of every core this process may run on."""
@@ -612,40 +664,19 @@ def cpu_baseline(wl, budget_s):
            "sample": "%d of %d requests of the same workload (q build, draft sample, %s "
                      "verification), single thread, %.1f s" % (n, wl.B, "+".join(wl.modes), secs),
            "single_thread": single}
-    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    if not cores or cores < 2 or n < 1:
+    if n < 1:
         return out
-    import multiprocessing as mp
-    from concurrent.futures import ProcessPoolExecutor
-    from multiprocessing import shared_memory
-    per_req = secs / n
-    n_par = int(min(wl.B, max(cores, cores * budget_s / per_req)))  # about budget_s of wall time
-    shms = []
-    try:
-        meta = {"temperature": np.ascontiguousarray(wl.temperature),
-                "request_ids": np.ascontiguousarray(wl.request_ids), "top_k": wl.top_k,
-                "seed": wl.seed, "modes": tuple(wl.modes), "target_dtype": wl.target_dtype}
-        for key, arr in (("draft", wl.draft), ("target", wl.target)):
-            arr = np.ascontiguousarray(arr)
-            shm = shared_memory.SharedMemory(create=True, size=max(1, arr.nbytes))
-            shms.append(shm)
-            np.ndarray(arr.shape, dtype=arr.dtype, buffer=shm.buf)[...] = arr
-            meta[key] = (shm.name, arr.shape, arr.dtype.str)
-        with ProcessPoolExecutor(max_workers=cores, mp_context=mp.get_context("spawn"),
-                                 initializer=oracle_pool_init, initargs=(meta,)) as ex:
-            list(ex.map(int, range(cores)))  # every worker started and attached
-            t0 = time.perf_counter()
-            list(ex.map(oracle_pool_request, range(n_par)))
-            psecs = time.perf_counter() - t0
-    finally:
-        for shm in shms:
-            shm.close()
-            shm.unlink()
-    out.update({"value": n_par * (wl.depth + 1) / psecs, "cores": cores,
+    with OraclePool(wl) as pool:
+        if pool.cores < 2:
+            return out
+        per_req = secs / n
+        n_par = int(min(wl.B, max(pool.cores, pool.cores * budget_s / per_req)))
+        psecs = pool.run(range(n_par))
+    out.update({"value": n_par * (wl.depth + 1) / psecs, "cores": pool.cores,
                 "sample": "%d of %d requests of the same workload (q build, draft sample, %s "
                           "verification) spread over a pool of %d processes, %.1f s; the "
                           "single-thread figure is beside it" % (n_par, wl.B, "+".join(wl.modes),
-                                                                cores, psecs)})
+                                                                pool.cores, psecs)})
     return out
 
 
@@ -756,15 +787,25 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     wl = W.by_name(args.workload)
-    per_step = max(1, min(wl.B, 2))
-    for _ in range(args.warmup):
-        oracle_sample_run(wl, per_step, 1e9)
-    t0 = time.perf_counter()
-    done = 0
-    for _ in range(args.steps):
-        n, _ = oracle_sample_run(wl, per_step, 1e9)
-        done += n
-    secs = time.perf_counter() - t0
+    from oracle import oracle as O
+    O.build()
+    # each step: two requests per core of the host (a bounded sample of the
+    # workload's batch, taken in turn), spread over a process pool
+    with OraclePool(wl) as pool:
+        cores = pool.cores
+        per_step = max(1, min(wl.B, 2 * cores))
+        nxt = 0
+
+        def step():
+            nonlocal nxt
+            idx = [(nxt + i) % wl.B for i in range(per_step)]
+            nxt = (nxt + per_step) % wl.B
+            return pool.run(idx)
+
+        for _ in range(args.warmup):
+            step()
+        secs = sum(step() for _ in range(args.steps))
+    done = per_step * args.steps
     value = done * (wl.depth + 1) / secs
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "verify rows/s",
@@ -773,8 +814,9 @@ def run_reference(args, rank, world):
         "vs_baseline": None, "dtype": "f64+u64", "data": "synthetic (seeded generators)",
         "config": {"workload": wl.name, "B_per_gpu": wl.B, "depth": wl.depth, "V": wl.V,
                    "sample_per_step": "%d of %d requests" % (per_step, wl.B)},
-        "cpu_baseline": {"value": value, "unit": "verify rows/s", "cores": 1, "kind": "oracle",
-                         "sample": "%d requests per step of %s" % (per_step, wl.name)},
+        "cpu_baseline": {"value": value, "unit": "verify rows/s", "cores": cores, "kind": "oracle",
+                         "sample": "%d requests per step of %s over a pool of %d processes" % (
+                             per_step, wl.name, cores)},
         "e2e": {"value": value, "unit": "verify rows/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
