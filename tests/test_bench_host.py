@@ -47,3 +47,25 @@ def test_algorithmic_bytes_dense_and_sparse():
     # request 0 reads 1 target row and its q row (a rejection); request 1 reads all 6
     esz = 2 if wl.target_dtype == "bf16" else 4
     assert ab["verify"] == (1 + wl.depth + 1) * wl.V * esz + wl.V * 4
+
+
+def _args(**kw):
+    import types
+    a = dict(workload="c1", steps=1, warmup=0, gpus=1)
+    a.update(kw)
+    return types.SimpleNamespace(**a)
+
+
+def test_reference_arm_line(oracle, capsys):
+    import json
+    bench.run_reference(_args(), 0, 1)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC
+    assert line["value"] > 0 and line["unit"] == "verify rows/s" and line["higher_is_better"]
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+
+
+def test_reference_arm_other_ranks_print_nothing(capsys):
+    bench.run_reference(_args(), 1, 2)
+    assert capsys.readouterr().out == ""
