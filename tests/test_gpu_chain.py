@@ -16,10 +16,11 @@ pytestmark = pytest.mark.gpu
 
 def run(x, bias, anchors, seed, temps=None, bf16=False):
     B, depth, V = x.shape
-    xd = torch.from_numpy(x.reshape(B * depth, V)).cuda()
-    if bf16:
-        xd = xd.to(torch.bfloat16)
-        x = xd.float().cpu().numpy().reshape(B, depth, V)
+    xh = torch.from_numpy(x.reshape(B * depth, V))
+    if bf16:  # rounded on the host; the oracle reads the widened bf16 rows
+        xh = xh.to(torch.bfloat16)
+        x = xh.float().numpy().reshape(B, depth, V)
+    xd = xh.cuda()
     bt = None if bias is None else torch.from_numpy(bias).cuda()
     tt = None if temps is None else torch.from_numpy(temps).cuda()
     at = torch.from_numpy(np.asarray(anchors, np.int32)).cuda()

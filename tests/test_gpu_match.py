@@ -13,20 +13,19 @@ import torch
 import draft_sampling_verification_gb300 as ds
 from draft_sampling_verification_gb300 import workloads as W
 from oracle import oracle as O
-from parity import compare_verify, dev_inputs, np_
+from parity import compare_verify, dev_inputs, np_, oracle_q, oracle_sample
 
 pytestmark = pytest.mark.gpu
 
 
 def run(wl, drafts_np=None):
     d, t, temps, req = dev_inputs(wl)
-    if drafts_np is None:
-        _, tok = ds.q_build_sample(d, wl.B, wl.depth, wl.seed, temps, wl.top_k, req)
-    else:
-        tok = torch.from_numpy(drafts_np.astype(np.int32)).cuda()
+    if drafts_np is None:  # the oracle's drafts, given to both sides
+        drafts_np = oracle_sample(wl, oracle_q(wl))[0].reshape(wl.B, wl.depth)
+    drafts = np.ascontiguousarray(drafts_np, dtype=np.int32)
+    tok = torch.from_numpy(drafts).cuda()
     g = ds.verify_match(t, tok, wl.seed, req)
     torch.cuda.synchronize()
-    drafts = np_(tok)
     ref = O.verify_match(wl.target_f32(), drafts, wl.seed, wl.request_ids)
     return g, ref
 

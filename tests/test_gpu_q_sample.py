@@ -51,6 +51,14 @@ def run_q(x, temps, top_k, ld_pad=0, dtype=torch.float32, offset=0):
     return q, view
 
 
+def host_rows(x, dtype):
+    """The rows the kernels read, made on the host: bf16 rounding by the CPU,
+    widened exactly back to fp32."""
+    if dtype == torch.bfloat16:
+        return torch.from_numpy(x).to(torch.bfloat16).float().numpy()
+    return x
+
+
 @pytest.mark.parametrize("V", [1, 2, 3, 8, 13, 257, 4099, 65537, 129280])
 @pytest.mark.parametrize("top_k", [0, 1, 16, 256])
 def test_q_build_random_rows(oracle, V, top_k):
@@ -70,7 +78,7 @@ def test_q_build_strided_unaligned(oracle, ld_pad, offset, dtype):
     V = 4099
     x = rows_for(V, rng, n_each=1)
     q, view = run_q(x, None, 0, ld_pad=ld_pad, dtype=dtype, offset=offset)
-    xr = view.float().cpu().numpy()  # bf16 widened exactly
+    xr = host_rows(x, dtype)
     compare_q(q, oracle.q_build(xr, None, 0))
     qs, _ = run_q(x, None, 64, ld_pad=ld_pad, dtype=dtype, offset=offset)
     compare_q(qs, oracle.q_build(xr, None, 64))
@@ -90,7 +98,7 @@ def test_q_topk_stream_orders(oracle, top_k, dtype):
     x = np.stack([asc, asc[::-1], tied, tied[::-1],
                   np.repeat(np.arange(V // 640, dtype=np.float32), 640)[:V]])
     q, view = run_q(x, [1.0, 1.0, 0.7, 1.3, 1.0], top_k, dtype=dtype)
-    xr = view.float().cpu().numpy()
+    xr = host_rows(x, dtype)
     compare_q(q, oracle.q_build(xr, [1.0, 1.0, 0.7, 1.3, 1.0], top_k))
 
 

@@ -11,7 +11,8 @@ import torch
 
 import draft_sampling_verification_gb300 as ds
 from draft_sampling_verification_gb300 import workloads as W
-from parity import compare_q, compare_verify, dev_inputs, np_, oracle_q, oracle_verify
+from parity import (compare_q, compare_verify, dev_inputs, np_, oracle_q, oracle_sample,
+                    oracle_verify)
 
 pytestmark = pytest.mark.gpu
 
@@ -50,7 +51,10 @@ def check_oracle(wl, res, modes):
     q, tok, outs = res
     qref = oracle_q(wl)
     compare_q(q, qref)
-    drafts = np_(tok)
+    # the oracle verifies the oracle's own drafts, which the GPU's must equal
+    rtok, _ = oracle_sample(wl, qref)
+    assert np.array_equal(np_(tok).ravel(), rtok)
+    drafts = rtok.reshape(wl.B, wl.depth)
     for m in modes:
         g = outs[m]
         if m == "greedy":

@@ -14,7 +14,8 @@ import torch
 
 import draft_sampling_verification_gb300 as ds
 from draft_sampling_verification_gb300 import workloads as W
-from parity import compare_q, compare_verify, dev_inputs, np_, oracle_q, oracle_verify
+from parity import (compare_q, compare_verify, dev_inputs, np_, oracle_q, oracle_sample,
+                    oracle_verify)
 
 pytestmark = pytest.mark.gpu
 
@@ -30,7 +31,10 @@ def run_workload(oracle, wl):
     torch.cuda.synchronize()
     qref = oracle_q(wl)
     compare_q(q, qref)
-    drafts = np_(tok)
+    # the oracle verifies the oracle's own drafts, which the GPU's must equal
+    rtok, rst = oracle_sample(wl, qref)
+    assert np.array_equal(np_(tok).ravel(), rtok)
+    drafts = rtok.reshape(wl.B, wl.depth)
     assert np.all(np_(sst) == 0)
     out = {}
     for mode in wl.modes:
@@ -104,15 +108,15 @@ def test_refusals_and_early_exit(oracle):
     wl = W.Workload("edge", B, depth, V, xd, xt, "f32", np.ones(B * depth, np.float32), 0, 3,
                     ("greedy", "ratio"), np.arange(B, dtype=np.uint32))
     d, t, temps, req = dev_inputs(wl)
-    q = ds.q_build(d, temps, 0)
-    tok, _ = ds.draft_sample(q, B, depth, V, 3, req)
-    drafts = np_(tok).copy()
+    # q and drafts from the oracle, edited below, then given to both sides
+    qo = oracle_q(wl)
+    drafts = oracle_sample(wl, qo)[0].reshape(B, depth).copy()
     drafts[0, 1] = V            # out of range -> BAD_DRAFT
     xt[1, 0, 9] = np.nan        # NaN in the first row -> NONFINITE
     xt[2, :, :] = -np.inf       # no finite logit -> ZERO_MASS
     xt[3, depth, 3] = np.nan    # NaN in the bonus row: read only if all accepted
     # request 4: draft token with zero q -> BAD_DRAFT (ratio)
-    counts = np_(q["counts"]).copy()
+    counts = qo[0].copy()
     counts[4 * depth, :] = 0
     counts[4 * depth, (drafts[4, 0] + 1) % V] = 1 << 24
     xt[5, 0, :] = -np.inf
@@ -121,8 +125,8 @@ def test_refusals_and_early_exit(oracle):
     wl.target = xt
     t = torch.from_numpy(xt).cuda()
     dt = torch.from_numpy(drafts).cuda()
-    qd = dict(q)
-    qd["counts"] = torch.from_numpy(counts.view(np.int32)).cuda()
+    qd = {"counts": torch.from_numpy(counts.view(np.int32)).cuda(), "ids": None, "nnz": None,
+          "top_k": 0}
     qref = (counts.view(np.uint32), None, None, np.zeros(B * depth, np.int32))
     for mode in ("greedy", "ratio"):
         if mode == "greedy":

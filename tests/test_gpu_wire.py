@@ -10,7 +10,7 @@ import torch
 import draft_sampling_verification_gb300 as ds
 from draft_sampling_verification_gb300 import workloads as W
 from oracle import oracle as O
-from parity import dev_inputs, np_
+from parity import compare_q, dev_inputs, np_, oracle_q
 
 pytestmark = pytest.mark.gpu
 
@@ -156,6 +156,9 @@ def test_workload_rows_round_trip(oracle, name):
     torch.cuda.synchronize()
     assert np.all(np_(st) == 0)
     assert torch.equal(rec, q["counts"])
-    counts = np_(q["counts"]).view(np.uint32)
-    _, cs_ref = O.q_pack(counts, np_(q["ids"]), np_(q["nnz"]), wl.top_k)
+    # the checksums of the oracle's own q, which the GPU's q must equal
+    qref = oracle_q(wl)
+    compare_q(q, qref)
+    counts, ids, nnz, _ = qref
+    _, cs_ref = O.q_pack(counts, ids, nnz, wl.top_k)
     assert np.array_equal(np_(cs).view(np.uint64), cs_ref)
