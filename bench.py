@@ -211,6 +211,16 @@ def algorithmic_bytes(wl, acc_greedy, acc_ratio):
     return {"q_build_sample": q_bytes, "verify": int(rows + resid)}
 
 
+def full_read_bytes(wl):
+    """Bytes a step moves when every request reads all its target rows and
+    one q row back for the residual, whatever the outcome: the upper bound
+    that the outcome-dependent count above falls under."""
+    ab = algorithmic_bytes(wl, None, np.zeros(wl.B, np.int32))
+    esz_t = 4 if wl.target_dtype == "f32" else 2
+    q_row = wl.top_k * 8 + 4 if wl.top_k > 0 else wl.V * 4
+    return ab["q_build_sample"] + wl.B * ((wl.depth + 1) * wl.V * esz_t + q_row)
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
 
@@ -860,6 +870,7 @@ def main():
                 "l2": l2,
                 "draft_positions_per_s": wl.B * wl.depth * world / (ms * 1e-3),
                 "step_algorithmic_bytes": step_bytes,
+                "step_full_read_bytes": full_read_bytes(wl),
                 "step_achieved_gbs": step_bytes / (ms * 1e-3) / 1e9,
                 "kernel_ms": {k: round(v, 4) for k, v in per_kernel.items()},
                 "kernel_algorithmic_bytes": abytes,

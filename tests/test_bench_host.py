@@ -49,6 +49,23 @@ def test_algorithmic_bytes_dense_and_sparse():
     assert ab["verify"] == (1 + wl.depth + 1) * wl.V * esz + wl.V * 4
 
 
+def test_full_read_bytes_per_request():
+    # per request: 5 draft rows read, q written, 6 target rows and one q row
+    # read back, 5 tokens written
+    V = 129280
+    c4 = W.config4(B=1, V=V)
+    assert c4.top_k == 0 and c4.target_dtype == "bf16"
+    assert bench.full_read_bytes(c4) == 5 * V * 4 * 2 + 6 * V * 2 + V * 4 + 5 * 4
+    c3 = W.config3(B=1, V=V)
+    k = c3.top_k
+    assert k > 0 and c3.target_dtype == "f32"
+    assert bench.full_read_bytes(c3) == 5 * V * 4 + 5 * (8 * k + 4) + 6 * V * 4 + (8 * k + 4) \
+        + 5 * 4
+    # the outcome-dependent count never exceeds it
+    acc = np.array([c4.depth], np.int32)
+    assert sum(bench.algorithmic_bytes(c4, acc, acc).values()) <= bench.full_read_bytes(c4)
+
+
 def _args(**kw):
     import types
     a = dict(workload="c1", steps=1, warmup=0, gpus=1)
