@@ -305,6 +305,11 @@ def run_ours(args, rank, world, local_rank):
     for m in wl.modes:
         assert int((outs[m][3] != 0).sum()) == 0, "refused requests in bench"
     acc = {m: outs[m][0].cpu().numpy() for m in wl.modes}
+    # the step's integer outputs, for the comparison with the oracle
+    gpu_out = {"tok": tok.cpu().numpy(), "qst": qst.cpu().numpy().reshape(B, depth)}
+    for m in wl.modes:
+        o = [x.cpu().numpy() for x in outs[m]]
+        gpu_out[m] = (o[0], o[1], o[3]) if m == "greedy" else (o[0], o[1], o[2], o[3])
     abytes = algorithmic_bytes(wl, acc.get("greedy"), acc.get("ratio"))
     if one_launch:
         abytes = {"spec_step": sum(abytes.values())}
@@ -533,7 +538,7 @@ def run_ours(args, rank, world, local_rank):
     l2 = ("inputs larger than L2 (%.2f GB per step)" % (in_bytes / 1e9) if n_copies == 1 else
           "inputs rotated over %d copies (%.2f GB in all, > 3 x L2)" % (
               n_copies, n_copies * in_bytes / 1e9))
-    return wl, ms, per_kernel, abytes, clock_info, e2e, l2, wire, match, chain, sharded
+    return wl, ms, per_kernel, abytes, clock_info, e2e, l2, wire, match, chain, sharded, gpu_out
 
 
 # ------------------------------------------------------------ CPU oracle
@@ -592,7 +597,8 @@ def oracle_pool_init(meta):
 
 
 def oracle_pool_request(b):
-    """One request through the oracle (q build, draft sample, verification)."""
+    """One request through the oracle (q build, draft sample, verification);
+    returns its integer outputs for the comparison with the GPU's."""
     from oracle import oracle as O
     w = _POOL_WL
     x = w["draft"][b]
@@ -603,12 +609,13 @@ def oracle_pool_request(b):
     counts, ids, nnz, st = O.q_build(x, w["temperature"][b * depth:(b + 1) * depth], top_k)
     tok, sst = O.draft_sample(counts, ids, nnz, top_k, 1, depth, seed, req, V=V)
     drafts = tok.reshape(1, depth)
+    out = {"b": b, "tok": tok, "qst": st}
     for m in w["modes"]:
         if m == "greedy":
-            O.verify_greedy(z, drafts)
+            out[m] = O.verify_greedy(z, drafts)
         else:
-            O.verify_ratio(z, drafts, counts, ids, nnz, top_k, seed, req)
-    return b
+            out[m] = O.verify_ratio(z, drafts, counts, ids, nnz, top_k, seed, req)
+    return out
 
 
 class OraclePool:
@@ -647,10 +654,15 @@ class OraclePool:
             raise
         return self
 
-    def run(self, indices):
+    def run(self, indices, keep=None):
+        """Seconds for the oracle over these requests; their outputs are
+        appended to `keep` (a list) when given."""
         t0 = time.perf_counter()
-        list(self.ex.map(oracle_pool_request, list(indices)))
-        return time.perf_counter() - t0
+        res = list(self.ex.map(oracle_pool_request, list(indices)))
+        secs = time.perf_counter() - t0
+        if keep is not None:
+            keep.extend(res)
+        return secs
 
     def __exit__(self, *exc):
         if self.ex is not None:
@@ -663,9 +675,10 @@ class OraclePool:
         return False
 
 
-def cpu_baseline(wl, budget_s):
+def cpu_baseline(wl, budget_s, keep=None):
     """The oracle on the host cores: one thread, then requests spread over a
-    process pool (spawn) of every core this process may run on."""
+    process pool (spawn) of every core this process may run on.  The pool's
+    per-request outputs are appended to `keep` when given."""
     n, secs = oracle_sample_run(wl, wl.B, budget_s)
     rows = n * (wl.depth + 1)
     single = {"value": rows / secs, "unit": "verify rows/s", "cores": 1,
@@ -681,12 +694,70 @@ def cpu_baseline(wl, budget_s):
             return out
         per_req = secs / n
         n_par = int(min(wl.B, max(pool.cores, pool.cores * budget_s / per_req)))
-        psecs = pool.run(range(n_par))
+        psecs = pool.run(range(n_par), keep)
     out.update({"value": n_par * (wl.depth + 1) / psecs, "cores": pool.cores,
                 "sample": "%d of %d requests of the same workload (q build, draft sample, %s "
                           "verification) spread over a pool of %d processes, %.1f s; the "
                           "single-thread figure is beside it" % (n_par, wl.B, "+".join(wl.modes),
                                                                 pool.cores, psecs)})
+    return out
+
+
+FLAG_AMBIG, FLAG_NEAR, FLAG_NEAR_REL = 1, 2, 8  # the oracle's verification flag bits
+BAND_BOUND = 1e-4  # band cases per verify row
+
+
+def parity_band(wl, gpu, ref):
+    """The timed step's integer outputs against the oracle's on the requests
+    the oracle ran (`ref`: its per-request outputs).  Draft tokens, row
+    statuses and greedy outputs must be equal; ratio outputs must be equal
+    outside the oracle's tolerance band.  The band cases are counted from the
+    oracle's flags under both readings of the draw's band: absolute (1e-6 in
+    probability units) and relative (1e-6 of the picked token's own mass)."""
+    depth = wl.depth
+    ref = sorted(ref, key=lambda r: r["b"])
+    idx = np.array([r["b"] for r in ref], np.int64)
+    out = {"requests": int(idx.size), "verify_rows": int(idx.size * (depth + 1)),
+           "bound_per_row": BAND_BOUND}
+    if idx.size == 0:
+        return out
+    tok = np.stack([r["tok"].reshape(depth) for r in ref])
+    qst = np.stack([np.asarray(r["qst"]).reshape(depth) for r in ref])
+    out["draft_tokens_equal"] = bool(np.array_equal(gpu["tok"][idx], tok))
+    out["row_status_equal"] = bool(np.array_equal(gpu["qst"][idx], qst))
+    if "greedy" in wl.modes:
+        acc = np.concatenate([r["greedy"][0] for r in ref])
+        com = np.concatenate([r["greedy"][1] for r in ref])
+        st = np.concatenate([r["greedy"][2] for r in ref])
+        ga, gc, gs = gpu["greedy"]
+        out["greedy_equal"] = bool(np.array_equal(ga[idx], acc) and
+                                   np.array_equal(gc[idx], com) and np.array_equal(gs[idx], st))
+    if "ratio" in wl.modes:
+        acc = np.concatenate([r["ratio"][0] for r in ref])
+        com = np.concatenate([r["ratio"][1] for r in ref])
+        rf = np.concatenate([r["ratio"][2] for r in ref]).astype(np.uint32)
+        st = np.concatenate([r["ratio"][3] for r in ref])
+        ga, gc, gf, gs = gpu["ratio"]
+        gf = gf[idx].astype(np.uint32)
+        same = (ga[idx] == acc) & (gc[idx] == com).all(axis=1) & (gs[idx] == st)
+        ambig = (rf & FLAG_AMBIG) != 0
+        band_abs = ambig | ((rf & FLAG_NEAR) != 0)
+        band_rel = ambig | ((rf & FLAG_NEAR_REL) != 0)
+        rows = out["verify_rows"]
+        out.update({
+            "ratio_mismatch_outside_band": int((~same & ~band_rel).sum()),
+            "ratio_mismatch_in_band": int((~same & band_rel).sum()),
+            "ambiguous_decisions": int(ambig.sum()),
+            "draws_near_boundary_abs": int(((rf & FLAG_NEAR) != 0).sum()),
+            "draws_near_boundary_rel": int(((rf & FLAG_NEAR_REL) != 0).sum()),
+            "band_cases_abs": int(band_abs.sum()), "band_rate_abs": band_abs.sum() / rows,
+            "bound_met_abs": bool(band_abs.sum() <= BAND_BOUND * rows),
+            "band_cases_rel": int(band_rel.sum()), "band_rate_rel": band_rel.sum() / rows,
+            "bound_met_rel": bool(band_rel.sum() <= BAND_BOUND * rows),
+            "gpu_only_flags": int((((gf & (FLAG_AMBIG | FLAG_NEAR)) != 0) & ~band_abs).sum()),
+            "readings": "abs: a draw within 1e-6 (probability units) of a cumulative boundary; "
+                        "rel: within 1e-6 of the picked token's own mass; both count the "
+                        "decisions with |u*q - p| <= 1e-6*q"})
     return out
 
 
@@ -847,7 +918,7 @@ def main():
     import torch
     if world > 1:
         torch.distributed.init_process_group("nccl")
-    wl, ms, per_kernel, abytes, clocks, e2e, l2, wire, match, chain, sharded = run_ours(
+    wl, ms, per_kernel, abytes, clocks, e2e, l2, wire, match, chain, sharded, gpu_out = run_ours(
         args, rank, world, local_rank)
     if rank == 0:
         peaks = load_peaks()
@@ -935,7 +1006,9 @@ def main():
                              "frac": gbs_s / peak},
             }
         if not args.no_cpu:
-            line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+            ref = []
+            line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds, ref)
+            line["parity_band"] = parity_band(wl, gpu_out, ref)
         print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -76,7 +76,9 @@ __device__ __noinline__ void q_row(const qdense::Params& qp, int row, qdense::DS
 template <bool kG, bool kR, int kDt>
 __device__ __noinline__ void verify_call(const vfy::VParams& vp, int b, vfy::VSh2& sh,
                                          unsigned char* dyn, uint64_t* mbar, uint32_t& phase) {
-  vfy::verify_request<kG, kR, kDt>(vp, b, sh, dyn, mbar, phase, nullptr, nullptr);
+  // q rows come from other clusters of this launch: coherent loads of q
+  vfy::verify_request<kG, kR, kDt, vfy::kVCluster, false, true>(vp, b, sh, dyn, mbar, phase,
+                                                                 nullptr, nullptr);
 }
 
 template <bool kG, bool kR, int kDt>

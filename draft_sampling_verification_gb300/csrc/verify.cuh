@@ -82,6 +82,16 @@ struct VSh2 {
   uint32_t dflags;
 };
 
+// A load of q (counts, sparse ids): through the read-only data path when q
+// was written before the launch, a plain (coherent) load when the same launch
+// wrote it (the one-launch step, whose q rows are finished by other clusters
+// and published with release / acquire on the per-request row counter).
+template <bool kCoh, typename T>
+__device__ __forceinline__ T ldq(const T* p) {
+  if (kCoh) return *p;
+  return __ldg(p);
+}
+
 struct OpMaxNaNv {
   __device__ float operator()(float a, float b) const {
     float r;
@@ -120,7 +130,9 @@ __device__ __forceinline__ void am_merge(float& v, int& i, float v2, int i2) {
 // kMatch: the stochastic (match) mode instead of the ratio mode, with the same
 // outputs (r_*): every row draws from its own p (purpose MATCH) and a draw
 // equal to the proposal accepts it.
-template <bool kG, bool kR, int kDt, int NC = kVCluster, bool kMatch = false>
+// kCohQ: q was written by this same launch (see ldq).
+template <bool kG, bool kR, int kDt, int NC = kVCluster, bool kMatch = false,
+          bool kCohQ = false>
 __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh,
                                                unsigned char* vbuf, uint64_t* mbar,
                                                uint32_t& phase, const int32_t* drafts_sm,
@@ -231,7 +243,7 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
       const int64_t qr = (int64_t)b * depth + j;
       if (p.top_k == 0) {
         qrow = p.counts + qr * V;
-        if (tid == 0) cx = cnt_sm ? cnt_sm[j] : __ldg(qrow + x);
+        if (tid == 0) cx = cnt_sm ? cnt_sm[j] : ldq<kCohQ>(qrow + x);
       } else {
         // canonical sparse row: 1 <= nnz <= top_k, ids strictly ascending in
         // [0, V), counts > 0, total M
@@ -470,8 +482,8 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
       int a = 0, e = snnz - 1;
       while (a <= e) {
         const int mid = (a + e) >> 1;
-        const int id = __ldg(sids + mid);
-        if (id == v) return __ldg(scnt + mid);
+        const int id = ldq<kCohQ>(sids + mid);
+        if (id == v) return ldq<kCohQ>(scnt + mid);
         if (id < v) a = mid + 1;
         else e = mid - 1;
       }
@@ -498,7 +510,7 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
               const uint4* qp = reinterpret_cast<const uint4*>(qrow + lo - off) + g * (EPG / 4);
 #pragma unroll
               for (int k = 0; k < EPG / 4; ++k) {
-                const uint4 t4 = __ldg(qp + k);
+                const uint4 t4 = ldq<kCohQ>(qp + k);
                 qv[4 * k] = t4.x;
                 qv[4 * k + 1] = t4.y;
                 qv[4 * k + 2] = t4.z;
@@ -508,7 +520,7 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
 #pragma unroll
               for (int i = 0; i < EPG; ++i) {
                 const int s = g * EPG + i;
-                if (s >= off && s < off + n) qv[i] = __ldg(qrow + (lo - off + s));
+                if (s >= off && s < off + n) qv[i] = ldq<kCohQ>(qrow + (lo - off + s));
               }
             }
           }
@@ -537,11 +549,11 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
       if (sparse_qm) {
         // support ids in this slice: their weight is max(p - q, 0), not p
         for (int i = tid; i < snnz; i += kVThreads) {
-          const int v = __ldg(sids + i);
+          const int v = ldq<kCohQ>(sids + i);
           if (v < lo || v >= lo + n) continue;
           const int s = v - lo + off;
           const float pr = pv(val(s));
-          const float r = fmaxf(__fsub_rn(pr, (float)__ldg(scnt + i) * 0x1p-24f), 0.0f);
+          const float r = fmaxf(__fsub_rn(pr, (float)ldq<kCohQ>(scnt + i) * 0x1p-24f), 0.0f);
           const uint64_t d = wfix(pr) - wfix(r);
           atomicAdd(reinterpret_cast<unsigned long long*>(&sh.bsum[(s / EPG) / 32]),
                     (unsigned long long)(0ull - d));
@@ -646,7 +658,7 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
                 const bool in = (s >= off && s < off + n);
                 float r = pv(z[i]);
                 if (use_q && in) {
-                  const uint32_t q = qrow ? __ldg(qrow + (lo - off + s)) : sparse_q(lo - off + s);
+                  const uint32_t q = qrow ? ldq<kCohQ>(qrow + (lo - off + s)) : sparse_q(lo - off + s);
                   r = fmaxf(__fsub_rn(r, (float)q * 0x1p-24f), 0.0f);
                 }
                 wv[i] = wfix(r);

@@ -59,7 +59,10 @@ enum {
 enum {
     OR_FLAG_AMBIG_ACCEPT = 1u,   /* |u*q - p| <= 1e-6 * q at a tested row    */
     OR_FLAG_NEAR_BOUNDARY = 2u,  /* draw within 1e-6 of a cumulative edge     */
-    OR_FLAG_DEGENERATE = 4u      /* residual mass <= 0, drew from p instead   */
+    OR_FLAG_DEGENERATE = 4u,     /* residual mass <= 0, drew from p instead   */
+    OR_FLAG_NEAR_BOUNDARY_REL = 8u /* draw within 1e-6 of an edge of its own
+                                    token's interval, in units of that
+                                    interval's width                         */
 };
 
 #define OR_M 16777216u                 /* 2^24 */
@@ -478,7 +481,13 @@ void oracle_ratio_accept_many(const uint32_t* U, int64_t n, uint32_t c,
  *   Z <= 0 -> draw from p instead (flag DEGENERATE);
  *   t beyond the rounded total -> the last token with positive weight;
  *   NEAR_BOUNDARY if t lies within 1e-6 (probability units) of either edge
- *   of the chosen token's cumulative interval.
+ *   of the chosen token's cumulative interval;
+ *   NEAR_BOUNDARY_REL if it lies within 1e-6 * r_pick of either edge, r_pick
+ *   the chosen token's own weight: the draw's position inside its token's
+ *   interval is within 1e-6 of an end, as the ratio test's band
+ *   |u*q - p| <= 1e-6*q is relative to q.  This band is contained in the
+ *   absolute one (r_pick <= 1) and a uniform t falls in it with probability
+ *   2e-6 whatever the row.
  * ========================================================================= */
 int32_t oracle_residual_pick(const double* p, const uint32_t* c, int32_t V,
                              uint32_t w, uint32_t* flags)
@@ -512,6 +521,9 @@ int32_t oracle_residual_pick(const double* p, const uint32_t* c, int32_t V,
     }
     if (flags && (fabs(t - prev) <= 1e-6 || fabs(cum - t) <= 1e-6))
         *flags |= OR_FLAG_NEAR_BOUNDARY;
+    if (flags && pick >= 0 &&
+        (fabs(t - prev) <= 1e-6 * r[pick] || fabs(cum - t) <= 1e-6 * r[pick]))
+        *flags |= OR_FLAG_NEAR_BOUNDARY_REL;
     free(r);
     return pick;
 }
@@ -1136,6 +1148,9 @@ static int32_t or_residual_pick_sharded(const double* p, const uint32_t* c, int3
     }
     if (flags && (fabs(t - prev) <= 1e-6 || fabs(cum - t) <= 1e-6))
         *flags |= OR_FLAG_NEAR_BOUNDARY;
+    if (flags && pick >= 0 &&
+        (fabs(t - prev) <= 1e-6 * r[pick] || fabs(cum - t) <= 1e-6 * r[pick]))
+        *flags |= OR_FLAG_NEAR_BOUNDARY_REL;
     free(r);
     free(Zs);
     return pick;

@@ -26,7 +26,7 @@ _lib = None
 M = 1 << 24
 OK, NONFINITE, ZERO_MASS, ALLOC_INCONSISTENT, BAD_TEMPERATURE, BAD_Q, BAD_DRAFT = range(7)
 BAD_CHECKSUM = 9
-FLAG_AMBIG_ACCEPT, FLAG_NEAR_BOUNDARY, FLAG_DEGENERATE = 1, 2, 4
+FLAG_AMBIG_ACCEPT, FLAG_NEAR_BOUNDARY, FLAG_DEGENERATE, FLAG_NEAR_BOUNDARY_REL = 1, 2, 4, 8
 PURPOSE_PROPOSAL, PURPOSE_ACCEPT, PURPOSE_RESIDUAL, PURPOSE_BONUS, PURPOSE_MATCH = 0, 1, 2, 3, 4
 
 _P = ctypes.c_void_p

@@ -25,7 +25,7 @@ def test_pool_requests_match_one_thread(oracle):
     bench._POOL_WL.clear()
     bench._POOL_WL.update(meta)
     for b in range(wl.B):
-        assert bench.oracle_pool_request(b) == b
+        assert bench.oracle_pool_request(b)["b"] == b
     n, secs = bench.oracle_sample_run(wl, wl.B, 60.0)
     assert n == wl.B and secs > 0
 
@@ -36,6 +36,45 @@ def test_cpu_baseline_reports_pool_and_single_thread(oracle):
     assert out["kind"] == "oracle" and out["unit"] == "verify rows/s" and out["value"] > 0
     assert out["single_thread"]["cores"] == 1 and out["single_thread"]["value"] > 0
     assert out["cores"] >= 1
+
+
+def _gpu_like(wl, ref):
+    """GPU-shaped outputs (whole batch) built from the oracle's per-request
+    outputs, as the bench holds them after its step."""
+    ref = sorted(ref, key=lambda r: r["b"])
+    out = {"tok": np.stack([r["tok"].reshape(wl.depth) for r in ref]).astype(np.int32),
+           "qst": np.stack([np.asarray(r["qst"]).reshape(wl.depth) for r in ref])}
+    for m in wl.modes:
+        out[m] = tuple(np.concatenate([np.asarray(x)[None] if np.ndim(x) == 0 else x
+                                       for x in col]) for col in zip(*[r[m] for r in ref]))
+    return out
+
+
+def test_parity_band_counts(oracle):
+    wl = W.config4(B=6, V=1031)
+    ref = []
+    bench.cpu_baseline(wl, 0.5, ref)
+    assert sorted(r["b"] for r in ref) == list(range(len(ref)))
+    gpu = _gpu_like(wl, ref)
+    out = bench.parity_band(wl, gpu, ref)
+    assert out["requests"] == len(ref) and out["verify_rows"] == len(ref) * (wl.depth + 1)
+    assert out["draft_tokens_equal"] and out["row_status_equal"] and out["greedy_equal"]
+    assert out["ratio_mismatch_outside_band"] == 0 and out["gpu_only_flags"] == 0
+    assert out["band_cases_rel"] <= out["band_cases_abs"]
+    # a changed committed token outside the band is a mismatch; a changed
+    # draft token breaks the token equality
+    ga, gc, gf, gs = gpu["ratio"]
+    gc = gc.copy()
+    gc[0, 0] = gc[0, 0] + 1
+    gpu["ratio"] = (ga, gc, gf, gs)
+    gpu["tok"] = gpu["tok"].copy()
+    gpu["tok"][1, 0] += 1
+    bad = bench.parity_band(wl, gpu, ref)
+    assert not bad["draft_tokens_equal"]
+    flags0 = int(np.asarray(ref[0]["ratio"][2]).ravel()[0])
+    in_band = (flags0 & (bench.FLAG_AMBIG | bench.FLAG_NEAR_REL)) != 0
+    assert bad["ratio_mismatch_outside_band"] + bad["ratio_mismatch_in_band"] == 1
+    assert bad["ratio_mismatch_in_band"] == int(in_band)
 
 
 def test_algorithmic_bytes_dense_and_sparse():

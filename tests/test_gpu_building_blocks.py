@@ -128,6 +128,47 @@ def test_library_exp_weights_bit_exact(oracle, lo, hi, step):
     assert np.array_equal(E, refE)
 
 
+def test_library_exp_weights_every_float(oracle):
+    """Every fp32 d in [-28, 0] (1.1e9 values, where the integer weight
+    floor(exp_ds(d) * 2^40) is not zero) and +0, chunk by chunk: the
+    library's exp_ds and weight bit for bit equal to the oracle's.  The
+    clamp region below -28 (weight 0, then exp_ds 0 below -87) is sampled in
+    the test above."""
+    from concurrent.futures import ThreadPoolExecutor
+    lo = int(np.array([-0.0], np.float32).view(np.uint32)[0])      # 0x80000000
+    hi = int(np.array([-28.0], np.float32).view(np.uint32)[0])     # 0xC1E00000
+    chunk = 1 << 26
+    dev = torch.device("cuda")
+    e = torch.empty(chunk, dtype=torch.float32, device=dev)
+    E = torch.empty(chunk, dtype=torch.int64, device=dev)
+
+    def oracle_part(d):  # the oracle's C loop runs with the GIL released
+        return oracle.exp_ds(d)
+
+    with ThreadPoolExecutor(max_workers=16) as pool:
+        starts = list(range(lo, hi + 1, chunk)) + [None]
+        for a in starts:
+            if a is None:  # +0 and the first negative patterns once more
+                bits = np.array([0, lo, lo + 1, hi], np.uint32)
+            else:
+                bits = np.arange(a, min(hi + 1, a + chunk), dtype=np.uint64).astype(np.uint32)
+            d = bits.view(np.float32)
+            n = d.size
+            dt = torch.from_numpy(d).to(dev)
+            _call("dspark_debug_exp_weights", ctypes.c_void_p(dt.data_ptr()), n,
+                  ctypes.c_void_p(e.data_ptr()), ctypes.c_void_p(E.data_ptr()), None)
+            parts = np.array_split(d, 16)
+            ref = np.concatenate(list(pool.map(oracle_part, parts)))
+            torch.cuda.synchronize()
+            ge = e[:n].cpu().numpy()
+            gE = E[:n].cpu().numpy().view(np.uint64)
+            bad = np.flatnonzero(ge.view(np.uint32) != ref.view(np.uint32))
+            assert bad.size == 0, ("exp_ds", d[bad[:5]])
+            refE = np.floor(ref.astype(np.float64) * 2.0 ** 40).astype(np.uint64)
+            bad = np.flatnonzero(gE != refE)
+            assert bad.size == 0, ("weight", d[bad[:5]])
+
+
 def test_library_alloc_scale_matches_fp64():
     """k = RN64(2^24 / RN64(S)), khi = RN32(k), klo = RN32(k - khi) from the
     kernels' integer arithmetic equal numpy's FP64 / FP32 roundings."""

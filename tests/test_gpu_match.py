@@ -1,11 +1,11 @@
 """GPU parity of stochastic (match) verification (dspark_verify_match)
-against the oracle: integer outputs bit for bit on every request that
-neither side flags NEAR_BOUNDARY (a draw within 1e-6 of a cumulative
-boundary, where the GPU's fp32 p may legitimately pick the neighbour), on
-the workloads' rows (fp32 and bf16 targets), the all-accept and all-reject
-extremes, ragged vocabularies and refused rows.  Differences on flagged
-requests must stay under 1e-4 of the verify rows, the bar the ratio
-verifier meets."""
+against the oracle: integer outputs bit for bit on every request except
+those whose draw the ORACLE finds within 1e-6 of the picked token's own mass
+of a cumulative boundary (the relative reading of the band; the GPU's own
+flags excuse nothing), on the workloads' rows (fp32 and bf16 targets), the
+all-accept and all-reject extremes, ragged vocabularies and refused rows.
+Band cases under both readings are counted and printed in pytest's summary;
+the relative reading's must stay under 1e-4 of the verify rows."""
 import numpy as np
 import pytest
 import torch
@@ -13,9 +13,12 @@ import torch
 import draft_sampling_verification_gb300 as ds
 from draft_sampling_verification_gb300 import workloads as W
 from oracle import oracle as O
-from parity import compare_verify, dev_inputs, np_, oracle_q, oracle_sample
+from parity import (BAND_BOUND, VerifyCounts, compare_verify, dev_inputs, np_, oracle_q,
+                    oracle_sample)
 
 pytestmark = pytest.mark.gpu
+
+STATS = VerifyCounts()  # match comparisons of the workload tests
 
 
 def run(wl, drafts_np=None):
@@ -35,14 +38,12 @@ def run(wl, drafts_np=None):
                                      ("c5:8:accept:sparse", {}),
                                      ("c5:8:reject:sparse", {})])
 def test_match_workloads(oracle, name, kw):
+    global STATS
     wl = W.by_name(name, **kw)
     g, ref = run(wl)
-    mis, fmis, fl, n = compare_verify(g, ref, "ratio")
-    assert mis == 0, (name, mis, fmis, fl)
-    # heavy-tailed rows put much of p in tokens narrower than the 1e-6 band,
-    # so many draws are flagged; a flagged request may differ, and such
-    # differences must stay under 1e-4 of the verify rows
-    assert fmis <= max(1, int(1e-4 * n * (wl.depth + 1))), (fmis, fl)
+    c = compare_verify(g, ref, "match")
+    STATS += c
+    assert c.mismatch == 0, (name, c)
     acc = np_(g[0])
     assert np.all(np_(g[3]) == 0)
     if "accept" in name:
@@ -60,7 +61,17 @@ def test_match_ragged_and_refused(oracle, V):
     wl.target[2, depth, 0] = np.inf        # refused only if every proposal matched
     drafts[3, 2] = V                       # an out-of-range draft: BAD_DRAFT
     g, ref = run(wl, drafts)
-    mis, fmis, fl, n = compare_verify(g, ref, "ratio")
-    assert mis == 0, (V, mis, fmis)
+    c = compare_verify(g, ref, "match")
+    assert c.mismatch == 0, (V, c)
     st = np_(g[3])
     assert st[1] == ds.ST_NONFINITE and st[3] == ds.ST_BAD_DRAFT
+
+
+def test_zz_match_band_budget():
+    """Over the workload tests above: the relative band's cases stay under
+    1e-4 of the verify rows (the absolute reading's rate is printed)."""
+    if STATS.rows == 0:
+        pytest.skip("no match verification ran")
+    print("match verification:", STATS)
+    assert STATS.mismatch == 0
+    assert STATS.band_rel <= BAND_BOUND * STATS.rows

@@ -167,8 +167,8 @@ def test_cluster_verify_is_the_sharded_verifier(oracle, target):
     and the residual draw picks the CTA by its residual mass, then the token
     inside.  With V = 129,280 the CTAs' slices (4 for bf16 rows, 8 for fp32)
     are the oracle's contiguous shards, and the outputs equal the sharded
-    oracle's on every request neither side flags.  q and drafts come from
-    the oracle."""
+    oracle's on every request outside the oracle's relative band.  q and
+    drafts come from the oracle."""
     wl = W.config4(B=8)
     n_sh = 4 if target == "bf16" else 8
     _, t, _, req = dev_inputs(wl)
@@ -183,5 +183,5 @@ def test_cluster_verify_is_the_sharded_verifier(oracle, target):
     g = ds.verify_ratio(t, dd, q, wl.seed, req)
     torch.cuda.synchronize()
     ref = O.verify_ratio_sharded(wl.target_f32(), drafts, counts, n_sh, wl.seed, wl.request_ids)
-    mis, fmis, flagged, n = compare_verify(g, ref, "ratio")
-    assert mis == 0 and n == wl.B
+    c = compare_verify(g, ref, "ratio")
+    assert c.mismatch == 0 and c.requests == wl.B, c

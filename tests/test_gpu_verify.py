@@ -2,11 +2,19 @@
 the oracle, at the workloads' full sizes (V = 129,280) and on edge cases.
 
 Greedy outputs are bit-exact.  Ratio outputs (accept length, committed
-tokens, status) are bit-exact except on requests where either side flags a
-decision with |u*q - p| <= 1e-6*q or a final draw within 1e-6 of a
-cumulative boundary; those are counted and must stay under 1e-4 of the rows
-overall, and with these workload sizes that means none.  p is within 1e-6
-absolute per entry.
+tokens, status) are bit-exact on every request except those the ORACLE puts
+in the tolerance band: a decision with |u*q - p| <= 1e-6*q, or a final draw
+within 1e-6 of a cumulative boundary.  The GPU's own flags excuse nothing.
+
+The band of the draw is counted under two readings: absolute (1e-6 in
+probability units, the literal one) and relative (1e-6 of the picked
+token's own mass, which is what makes the bound of 1e-4 band cases per
+verify row meetable on 129,280-token heavy-tailed rows: every token lighter
+than 2e-6 lies wholly inside the absolute band, so an exact verifier's draws
+land in it on a few percent of the rows).  Excused are only the requests in
+the oracle's relative band; the bound is asserted on the relative reading and
+both rates are printed in pytest's summary.  p is within 1e-6 absolute per
+entry.
 """
 import numpy as np
 import pytest
@@ -14,17 +22,18 @@ import torch
 
 import draft_sampling_verification_gb300 as ds
 from draft_sampling_verification_gb300 import workloads as W
-from parity import (compare_q, compare_verify, dev_inputs, np_, oracle_q, oracle_sample,
-                    oracle_verify)
+from parity import (BAND_BOUND, VerifyCounts, compare_q, compare_verify, dev_inputs, np_,
+                    oracle_q, oracle_sample, oracle_verify)
 
 pytestmark = pytest.mark.gpu
 
 P_TOL = 1e-6
 
-STATS = {"rows": 0, "flagged": 0, "mismatch": 0, "flagged_mismatch": 0}
+STATS = VerifyCounts()  # ratio comparisons of this module
 
 
 def run_workload(oracle, wl):
+    global STATS
     d, t, temps, req = dev_inputs(wl)
     q = ds.q_build(d, temps, wl.top_k)
     tok, sst = ds.draft_sample(q, wl.B, wl.depth, wl.V, wl.seed, req)
@@ -45,13 +54,11 @@ def run_workload(oracle, wl):
             g = ds.verify_ratio(t, tok, q, wl.seed, req)
         torch.cuda.synchronize()
         ref = oracle_verify(wl, mode, drafts, qref)
-        out[mode] = compare_verify(g, ref, mode)
-        mis, fmis, fl, n = out[mode]
-        STATS["rows"] += n * (wl.depth + 1)
-        STATS["flagged"] += fl
-        STATS["mismatch"] += mis
-        STATS["flagged_mismatch"] += fmis
-        assert mis == 0, (wl.name, mode, mis)
+        c = compare_verify(g, ref, mode)
+        out[mode] = c
+        if mode == "ratio":
+            STATS += c
+        assert c.mismatch == 0, (wl.name, mode, c)
     return out
 
 
@@ -60,9 +67,8 @@ def run_workload(oracle, wl):
 def test_workload_full_size(oracle, make):
     wl = make()
     res = run_workload(oracle, wl)
-    for mode, (mis, fmis, fl, n) in res.items():
-        print("%s %s: %d requests, %d flagged, %d flagged mismatches" % (wl.name, mode, n, fl,
-                                                                         fmis))
+    for mode, c in res.items():
+        print(wl.name, mode, c)
 
 
 @pytest.mark.parametrize("variant", ["accept", "reject", "mixed"])
@@ -136,8 +142,8 @@ def test_refusals_and_early_exit(oracle):
             g = ds.verify_ratio(t, dt, qd, 3, req)
         torch.cuda.synchronize()
         ref = oracle_verify(wl, mode, drafts, qref)
-        mis, fmis, fl, n = compare_verify(g, ref, mode)
-        assert mis == 0 and fmis == 0
+        c = compare_verify(g, ref, mode)
+        assert c.mismatch == 0, c
         st = np_(g[3])
         assert st[0] == 6 and st[1] == 1 and st[2] == 2
         if mode == "ratio":
@@ -177,11 +183,20 @@ def test_target_probs_within_tolerance(oracle, dtype):
 
 
 def test_zz_ambiguity_budget():
-    """Over everything verified in this module: no mismatch outside the band,
-    and mismatches inside it (flagged) under 1e-4 of the verify rows."""
-    if STATS["rows"] == 0:
+    """Over every ratio verification of this module: no request differs
+    outside the oracle's relative band, and the relative band's cases stay
+    under 1e-4 of the verify rows.  The
+    absolute reading's count is printed beside it: on these heavy-tailed
+    rows it is a property of the inputs (the exact oracle flags them), far
+    above 1e-4, and no implementation could lower it."""
+    if STATS.rows == 0:
         pytest.skip("no verification ran")
-    print("verify rows %d, flagged requests %d, flagged mismatches %d, unflagged mismatches %d"
-          % (STATS["rows"], STATS["flagged"], STATS["flagged_mismatch"], STATS["mismatch"]))
-    assert STATS["mismatch"] == 0
-    assert STATS["flagged_mismatch"] <= max(1, int(1e-4 * STATS["rows"]))
+    print("ratio verification:", STATS)
+    print("band cases per verify row: absolute %.2e, relative %.2e (bound %.0e)"
+          % (STATS.band_abs / STATS.rows, STATS.band_rel / STATS.rows, BAND_BOUND))
+    assert STATS.mismatch == 0
+    assert STATS.band_rel <= BAND_BOUND * STATS.rows
+    # GPU-only flags excuse nothing; they mark draws whose GPU distance to a
+    # boundary is within 1e-6 while the exact one is not, a thin shell of the
+    # absolute band
+    assert STATS.gpu_only <= max(2, STATS.band_abs // 10)

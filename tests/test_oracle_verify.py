@@ -117,6 +117,71 @@ def test_residual_pick_measures(oracle):
     assert tok == 3 and fl & oracle.FLAG_DEGENERATE
 
 
+def band_runs(oracle, p, c, first, bit):
+    """Lengths (in draws) of the runs of draws flagged `bit` at the start and at
+    the end of each token's run of draws [first[v], first[v+1])."""
+    def fl(w):
+        return oracle.residual_pick(p, c, w)[1] & bit
+    out = []
+    for v in range(p.size):
+        a, e = int(first[v]), int(first[v + 1])
+        if e <= a:
+            out.append((0, 0))
+            continue
+        mid = (a + e) // 2
+        lo, hi = a, mid  # first unflagged draw of the leading run
+        while lo < hi:
+            m = (lo + hi) // 2
+            if fl(m):
+                lo = m + 1
+            else:
+                hi = m
+        lead = lo - a
+        lo, hi = mid, e  # first draw of the trailing run
+        while lo < hi:
+            m = (lo + hi) // 2
+            if fl(m):
+                hi = m
+            else:
+                lo = m + 1
+        out.append((lead, e - lo))
+    return np.array(out, np.int64)
+
+
+def test_boundary_band_measures(oracle):
+    """The two readings of "a draw within 1e-6 of a cumulative boundary".
+    Absolute: every edge carries a band of 1e-6 (probability units) on each
+    side, whatever the token's mass.  Relative: the band of a token's edges is
+    1e-6 of that token's own mass, so a uniform draw falls in it with
+    probability 2e-6 on any row; it lies inside the absolute band."""
+    # dyadic masses: every edge sits exactly on a draw, Z = 1
+    p = np.array([2.0 ** -1, 2.0 ** -3, 2.0 ** -3, 2.0 ** -6, 2.0 ** -4, 2.0 ** -6, 2.0 ** -5,
+                  2.0 ** -3])
+    assert p.sum() == 1.0
+    first = np.concatenate([[0], np.cumsum(p) * 2.0 ** 32]).astype(np.int64)
+    rel = band_runs(oracle, p, None, first, oracle.FLAG_NEAR_BOUNDARY_REL)
+    ab = band_runs(oracle, p, None, first, oracle.FLAG_NEAR_BOUNDARY)
+    width = 1e-6 * 2.0 ** 32  # draws per 1e-6 of probability
+    # absolute band: the same run at every edge
+    assert np.all(np.abs(ab - width) <= 1.5)
+    # relative band: runs proportional to the token's own mass, both ends
+    assert np.all(np.abs(rel - p[:, None] * width) <= 1.5)
+    assert abs(rel.sum() / 2.0 ** 32 - 2e-6) <= p.size * 2 * 2.0 ** -32
+    assert np.all(rel <= ab)
+    # residual weights max(p - q, 0): a token's band follows its residual mass
+    c = np.zeros(8, np.uint32)
+    c[0] = 1 << 23          # q(0) = 1/2 = p(0): no residual, no band
+    c[2] = 1 << 20          # q(2) = 1/16: residual 1/16
+    c[4] = (1 << 20) + (1 << 19)  # q(4) = 3/32 > p(4): no residual
+    r = np.maximum(p - c / float(M), 0.0)
+    Z = r.sum()
+    first_r = np.concatenate([[0], np.cumsum(r / Z) * 2.0 ** 32]).astype(np.int64)
+    rel_r = band_runs(oracle, p, c, first_r, oracle.FLAG_NEAR_BOUNDARY_REL)
+    assert np.all(rel_r[r == 0] == 0)
+    t_width = 1e-6 / Z * 2.0 ** 32  # t = w * 2^-32 * Z
+    assert np.all(np.abs(rel_r - r[:, None] * t_width) <= 1.5)
+
+
 # ----------------------------------- exact committed distribution, V = 8
 def accept_prob(oracle, c, p):
     U = np.arange(M, dtype=np.uint32)
