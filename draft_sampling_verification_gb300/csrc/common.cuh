@@ -102,6 +102,78 @@ __device__ __forceinline__ float weight40(float d) {
   return floorf(exp_ds_pow2(fmaxf(d, -30.0f), 40));
 }
 
+// ------------------------------------------------- packed fp32x2 arithmetic
+// Two fp32 lanes per instruction (sm_100 and later).  Written as inline PTX
+// with an explicit rounding modifier so that no multiply and add are ever
+// contracted into one fma: each lane is exactly the single-rounded scalar
+// operation named (mul / add / fma, .rn or .rm).
+__device__ __forceinline__ uint64_t f2_pack(float2 v) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(v.x), "f"(v.y));
+  return r;
+}
+__device__ __forceinline__ float2 f2_unpack(uint64_t r) {
+  float2 v;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+  return v;
+}
+__device__ __forceinline__ float2 mul2_rn(float2 a, float2 b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_pack(a)), "l"(f2_pack(b)));
+  return f2_unpack(d);
+}
+__device__ __forceinline__ float2 add2_rn(float2 a, float2 b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_pack(a)), "l"(f2_pack(b)));
+  return f2_unpack(d);
+}
+__device__ __forceinline__ float2 add2_rm(float2 a, float2 b) {  // rounded down
+  uint64_t d;
+  asm("add.rm.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_pack(a)), "l"(f2_pack(b)));
+  return f2_unpack(d);
+}
+__device__ __forceinline__ float2 fma2_rn(float2 a, float2 b, float2 c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(d)
+      : "l"(f2_pack(a)), "l"(f2_pack(b)), "l"(f2_pack(c)));
+  return f2_unpack(d);
+}
+__device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
+
+// weight40 of two distances at once, the reduction and the polynomial on the
+// packed fp32x2 pipe: every lane goes through exactly the single-rounded
+// operations of weight40, so each result is bit-identical to weight40 of
+// that lane.  Differences from the scalar sequence, all exact: the rint
+// offset carries the +40 of the scaling (1.5 * 2^23 + 40 rounds t as
+// 1.5 * 2^23 does, the parity of the offset being even), so the bits of tm
+// shifted left by 23 are (n + 40) << 23 modulo 2^32 (the offset's own bits
+// vanish there); fma(n, -c, x) equals fma(-n, c, x).  The rounding of
+// t = RN(d * log2(e)) to an integer decides ties (t = k + 1/2 exactly), so
+// that step stays on the scalar pipe: a packed product feeding a packed add
+// measured different there (the rounding of the product was not seen), while
+// the scalar pair matches the oracle on every float.
+__device__ __forceinline__ float2 weight40x2(float2 d) {
+  constexpr float kMag40 = 12582952.0f;  // 1.5 * 2^23 + 40
+  d.x = fmaxf(d.x, -30.0f);
+  d.y = fmaxf(d.y, -30.0f);
+  const float2 tm = make_float2(__fadd_rn(__fmul_rn(d.x, kL2E), kMag40),
+                                __fadd_rn(__fmul_rn(d.y, kL2E), kMag40));
+  const float2 n = add2_rn(tm, f2(-kMag40));
+  float2 r = fma2_rn(n, f2(-kLn2Hi), d);
+  r = fma2_rn(n, f2(-kLn2Lo), r);
+  float2 q = fma2_rn(f2(kInvFact7), r, f2(kInvFact6));
+  q = fma2_rn(q, r, f2(kInvFact5));
+  q = fma2_rn(q, r, f2(kInvFact4));
+  q = fma2_rn(q, r, f2(kInvFact3));
+  q = fma2_rn(q, r, f2(kInvFact2));
+  q = fma2_rn(q, r, f2(1.0f));
+  q = fma2_rn(q, r, f2(1.0f));
+  const float ex = __int_as_float(__float_as_int(q.x) + (__float_as_int(tm.x) << 23));
+  const float ey = __int_as_float(__float_as_int(q.y) + (__float_as_int(tm.y) << 23));
+  return make_float2(floorf(ex), floorf(ey));
+}
+
 // Integer weight E = floor(exp_ds(d) * 2^40) of a token at distance d <= 0
 // from the row maximum.  Below d = -28 the weight is 0 for every float d
 // (exp_ds(d) < 2^-40 there), so the polynomial is skipped.

@@ -10,8 +10,17 @@ __global__ void exp_weights_kernel(const float* d, int64_t n, float* e_out, uint
        i += (int64_t)gridDim.x * blockDim.x) {
     const float e = dspark::exp_ds(d[i]);
     if (e_out) e_out[i] = e;
-    // the weight as the q kernels compute it: floor(exp_ds(d) * 2^40), exact
-    if (E_out) E_out[i] = __float2ull_rz(dspark::weight40(d[i]));
+    // the weight as the q kernels compute it: floor(exp_ds(d) * 2^40), exact;
+    // the scalar form (top-k and sharded rows) and the packed pair form
+    // (dense rows, here with a second lane) must agree, else ~0 is returned
+    if (E_out) {
+      const float w1 = dspark::weight40(d[i]);
+      const float2 w2 = dspark::weight40x2(make_float2(d[i], d[n - 1 - i]));
+      const bool same = __float_as_uint(w1) == __float_as_uint(w2.x) &&
+                        __float_as_uint(dspark::weight40(d[n - 1 - i])) ==
+                            __float_as_uint(w2.y);
+      E_out[i] = same ? __float2ull_rz(w1) : ~0ull;
+    }
   }
 }
 

@@ -206,6 +206,50 @@ __device__ __forceinline__ FloatSplit float_split(float Ef, float khi, float klo
   return o;
 }
 
+// float_split of two weights at once on the packed fp32x2 pipe, lane for
+// lane bit-identical to float_split: floor(p1) is the rounded-down sum
+// p1 + 1.5 * 2^23 (exact for 0 <= p1 < 2^22, and p1 >= 2^22 is never
+// certified: the test below is p1 < kFMax - 2, i.e. floor(p1) < kFMax - 2);
+// 2048 fr is taken as fma(u, 2048, 2048 RN(e1 + p2)) with u = p1 - floor(p1)
+// exact, which equals RN(RN(u + RN(e1 + p2)) * 2048) because scaling by
+// 2^11 commutes with rounding (no value here is subnormal); the same
+// rounded-down sum gives floor(2048 fr).  klo2k = 2048 * klo (exact).  The
+// floor f and the bucket come from the bits of the two sums: bits(t0) =
+// 0x4B400000 + floor(p1), bits(tG) = 0x4B400000 + G with G in [-1, 2049],
+// and 0x4B400000 is a multiple of 2048.
+struct FloatSplit2 {
+  uint32_t word[2], f[2], b[2];
+  bool cert[2], zero[2];
+};
+__device__ __forceinline__ FloatSplit2 float_split2(float2 E, float khi, float klo2k) {
+  constexpr float kMag = 12582912.0f;  // 1.5 * 2^23
+  const float2 K = f2(khi);
+  const float2 p1 = mul2_rn(E, K);
+  const float2 e1 = fma2_rn(E, K, make_float2(-p1.x, -p1.y));
+  const float2 p2s = mul2_rn(E, f2(klo2k));
+  const float2 t0 = add2_rm(p1, f2(kMag));
+  const float2 f0 = add2_rn(t0, f2(-kMag));
+  const float2 u = add2_rn(p1, make_float2(-f0.x, -f0.y));
+  const float2 vs = fma2_rn(e1, f2(2048.0f), p2s);
+  const float2 fb = fma2_rn(u, f2(2048.0f), vs);
+  const float2 tG = add2_rm(fb, f2(kMag));
+  const float2 G = add2_rn(tG, f2(-kMag));
+  const float2 xh = add2_rn(add2_rn(fb, make_float2(-G.x, -G.y)), f2(-0.5f));
+  FloatSplit2 o;
+  const float ee[2] = {E.x, E.y}, pp[2] = {p1.x, p1.y}, hh[2] = {xh.x, xh.y};
+  const uint32_t bt0[2] = {__float_as_uint(t0.x), __float_as_uint(t0.y)};
+  const uint32_t btg[2] = {__float_as_uint(tG.x), __float_as_uint(tG.y)};
+#pragma unroll
+  for (int l = 0; l < 2; ++l) {
+    o.cert[l] = fabsf(hh[l]) < kHalfMargin && pp[l] < (float)(kFMax - 2u);
+    o.f[l] = bt0[l] + (btg[l] >> 11) - (0x4B400000u + (0x4B400000u >> 11));
+    o.b[l] = btg[l] & (kBins - 1u);
+    o.zero[l] = (ee[l] == 0.0f);
+    o.word[l] = o.zero[l] ? 0u : ((o.f[l] << 13) | kPos | o.b[l]);
+  }
+  return o;
+}
+
 __device__ __forceinline__ int esc_find(const DShared& sh, int s) {
   const uint32_t ne = min(sh.n_esc, (uint32_t)kEscCap);
   for (uint32_t j = 0; j < ne; ++j)
@@ -494,33 +538,35 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
   }
 
   // ---- pass B: E = floor(exp_ds(y - m) * 2^40) in place, S = sum E
+  //      (pairs of elements on the packed fp32x2 pipe)
   uint64_t S = 0;
   uint32_t ovf = 0;
+  const float2 mneg = f2(-m);
   if (scale) {
+    const float2 iT2 = f2(invT);
     for (int g = tid; g < ngroups; g += kThr) {
       const float4 x4 = reinterpret_cast<const float4*>(sl)[g];
-      const float xx[4] = {x4.x, x4.y, x4.z, x4.w};
-      float ee[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float y = __fmul_rn(xx[i], invT);
-        // a finite logit whose scaled value overflows to -inf refuses the row
-        ovf |= (y == -INFINITY && xx[i] != -INFINITY) ? 1u : 0u;
-        ee[i] = weight40(__fsub_rn(y, m));
-        S += __float2ull_rz(ee[i]);
-      }
-      reinterpret_cast<float4*>(sl)[g] = make_float4(ee[0], ee[1], ee[2], ee[3]);
+      const float2 ya = mul2_rn(make_float2(x4.x, x4.y), iT2);
+      const float2 yb = mul2_rn(make_float2(x4.z, x4.w), iT2);
+      // a finite logit whose scaled value overflows to -inf refuses the row
+      ovf |= ((ya.x == -INFINITY && x4.x != -INFINITY) || (ya.y == -INFINITY && x4.y != -INFINITY) ||
+              (yb.x == -INFINITY && x4.z != -INFINITY) || (yb.y == -INFINITY && x4.w != -INFINITY))
+                 ? 1u : 0u;
+      const float2 ea = weight40x2(add2_rn(ya, mneg));
+      const float2 eb = weight40x2(add2_rn(yb, mneg));
+      S += __float2ull_rz(ea.x) + __float2ull_rz(ea.y) + __float2ull_rz(eb.x) +
+           __float2ull_rz(eb.y);
+      reinterpret_cast<float4*>(sl)[g] = make_float4(ea.x, ea.y, eb.x, eb.y);
     }
   } else {
 #pragma unroll 2
     for (int g = tid; g < ngroups; g += kThr) {
       const float4 x4 = reinterpret_cast<const float4*>(sl)[g];
-      const float e0 = weight40(__fsub_rn(x4.x, m));
-      const float e1 = weight40(__fsub_rn(x4.y, m));
-      const float e2 = weight40(__fsub_rn(x4.z, m));
-      const float e3 = weight40(__fsub_rn(x4.w, m));
-      S += __float2ull_rz(e0) + __float2ull_rz(e1) + __float2ull_rz(e2) + __float2ull_rz(e3);
-      reinterpret_cast<float4*>(sl)[g] = make_float4(e0, e1, e2, e3);
+      const float2 ea = weight40x2(add2_rn(make_float2(x4.x, x4.y), mneg));
+      const float2 eb = weight40x2(add2_rn(make_float2(x4.z, x4.w), mneg));
+      S += __float2ull_rz(ea.x) + __float2ull_rz(ea.y) + __float2ull_rz(eb.x) +
+           __float2ull_rz(eb.y);
+      reinterpret_cast<float4*>(sl)[g] = make_float4(ea.x, ea.y, eb.x, eb.y);
     }
   }
   for (int i = tid; i < kBins + 16; i += kThr) sh.hist[i] = 0u;
@@ -577,43 +623,50 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
   const int ek = sh.ek;
   const float khi = sh.khi, klo = sh.klo;
 
-  // ---- pass C: words and fraction histogram
+  // ---- pass C: words and fraction histogram (pairs on the fp32x2 pipe)
+  const float klo2k = __fmul_rn(klo, 2048.0f);
   uint32_t F = 0, internal = 0;
   uint32_t gmask = 0;  // bit it: group tid + 256 it holds an element the float split left open
   {
     int it = 0;
     for (int g = tid; g < ngroups; g += kThr, ++it) {
       const float4 e4 = reinterpret_cast<const float4*>(sl)[g];
-      const float ee[4] = {e4.x, e4.y, e4.z, e4.w};
-      uint32_t w[4];
+      const FloatSplit2 fa = float_split2(make_float2(e4.x, e4.y), khi, klo2k);
+      const FloatSplit2 fc = float_split2(make_float2(e4.z, e4.w), khi, klo2k);
       bool any_open = false;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const FloatSplit fs = float_split(ee[i], khi, klo);
-        const bool counted = fs.cert && !fs.zero;
-        any_open = any_open || !(fs.cert || fs.zero);
-        w[i] = fs.word;
+        const FloatSplit2& fs = (i < 2) ? fa : fc;
+        const int l = i & 1;
+        const bool counted = fs.cert[l] && !fs.zero[l];
+        any_open = any_open || !(fs.cert[l] || fs.zero[l]);
         // branch-free: the elements that do not count go to a dummy bin
-        F += counted ? fs.f : 0u;
-        atomicAdd(&sh.hist[counted ? fs.b : kBins + (tid & 15)], 1u);
+        F += counted ? fs.f[l] : 0u;
+        atomicAdd(&sh.hist[counted ? fs.b[l] : kBins + (tid & 15)], 1u);
       }
       gmask |= any_open ? (1u << it) : 0u;
       // a group with an open element keeps its four weights for the refinement
       reinterpret_cast<uint4*>(slu)[g] =
-          any_open ? make_uint4(__float_as_uint(ee[0]), __float_as_uint(ee[1]),
-                                __float_as_uint(ee[2]), __float_as_uint(ee[3]))
-                   : make_uint4(w[0], w[1], w[2], w[3]);
+          any_open ? make_uint4(__float_as_uint(e4.x), __float_as_uint(e4.y),
+                                __float_as_uint(e4.z), __float_as_uint(e4.w))
+                   : make_uint4(fa.word[0], fa.word[1], fc.word[0], fc.word[1]);
     }
   }
   // the flagged groups: the certified elements get their word (counted above),
   // the open ones (about 1 in 2000) the exact split
   for (uint32_t m2 = gmask; m2 != 0u; m2 &= m2 - 1u) {
     const int g = tid + kThr * (__ffs(m2) - 1);
+    const uint4 e4 = reinterpret_cast<const uint4*>(slu)[g];
+    const float ee[4] = {__uint_as_float(e4.x), __uint_as_float(e4.y), __uint_as_float(e4.z),
+                         __uint_as_float(e4.w)};
+    const FloatSplit2 fa = float_split2(make_float2(ee[0], ee[1]), khi, klo2k);
+    const FloatSplit2 fc = float_split2(make_float2(ee[2], ee[3]), khi, klo2k);
     for (int i = 0; i < 4; ++i) {
+      const FloatSplit2& fs = (i < 2) ? fa : fc;
+      const int l = i & 1;
       const int s = 4 * g + i;
-      const float Ef = __uint_as_float(slu[s]);
-      const FloatSplit fs = float_split(Ef, khi, klo);
-      slu[s] = (fs.cert || fs.zero) ? fs.word : exact_word(Ef, mk, ek, sh, s, &F, &internal);
+      slu[s] = (fs.cert[l] || fs.zero[l]) ? fs.word[l]
+                                          : exact_word(ee[i], mk, ek, sh, s, &F, &internal);
     }
   }
   F = warp_reduce(F, OpAddU32());

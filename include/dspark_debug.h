@@ -21,7 +21,10 @@ extern "C" {
  * a draft token at distance d from the row maximum receives
  * ("PP1 q transport and scheduling design", Distribution contract and
  * precision: normalised draft weights; exp_ds is the library's fixed fp32
- * exponential, see dspark_q_build).  Either output may be NULL.
+ * exponential, see dspark_q_build).  Either output may be NULL.  The weight
+ * is computed both as the top-k and sharded kernels compute it (one element)
+ * and as the dense kernel does (two elements at once, paired here with
+ * d[n-1-i]); E_out[i] = ~0 (all ones) if the two ever disagree.
  */
 int dspark_debug_exp_weights(const float* d, int64_t n, float* e_out, uint64_t* E_out,
                              void* stream);
