@@ -139,6 +139,13 @@ __device__ __forceinline__ float2 fma2_rn(float2 a, float2 b, float2 c) {
       : "l"(f2_pack(a)), "l"(f2_pack(b)), "l"(f2_pack(c)));
   return f2_unpack(d);
 }
+__device__ __forceinline__ float2 fma2_rm(float2 a, float2 b, float2 c) {  // rounded down
+  uint64_t d;
+  asm("fma.rm.f32x2 %0, %1, %2, %3;"
+      : "=l"(d)
+      : "l"(f2_pack(a)), "l"(f2_pack(b)), "l"(f2_pack(c)));
+  return f2_unpack(d);
+}
 __device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
 
 // weight40 of two distances at once, the reduction and the polynomial on the

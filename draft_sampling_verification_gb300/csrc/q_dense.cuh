@@ -250,6 +250,27 @@ __device__ __forceinline__ FloatSplit2 float_split2(float2 E, float khi, float k
   return o;
 }
 
+// Exact sum of the integer weights E (integer floats <= 2^40) without a
+// float-to-integer conversion: E = hi * 2^20 + lo with hi = floor(E / 2^20)
+// read from the bits of the round-down sum E * 2^-20 + 2^23, and lo = E -
+// hi * 2^20 (exact) from the bits of lo + 2^23; the bits are summed as 32-bit
+// integers (modulo 2^32, the 2^23 offsets removed at the end: a thread's hi
+// and lo sums stay far below 2^32).
+struct WeightSum {
+  uint32_t hi, lo, n;  // sums of the offset bits, and the number of weights
+};
+__device__ __forceinline__ void sum_weights2(float2 E, WeightSum& w) {
+  const float2 t = fma2_rm(E, f2(0x1p-20f), f2(8388608.0f));
+  const float2 l = add2_rn(fma2_rn(add2_rn(t, f2(-8388608.0f)), f2(-1048576.0f), E),
+                           f2(8388608.0f));
+  w.hi += __float_as_uint(t.x) + __float_as_uint(t.y);
+  w.lo += __float_as_uint(l.x) + __float_as_uint(l.y);
+  w.n += 2u;
+}
+__device__ __forceinline__ uint64_t weight_sum_total(const WeightSum& w) {
+  return ((uint64_t)(w.hi - w.n * 0x4B000000u) << 20) + (uint64_t)(w.lo - w.n * 0x4B000000u);
+}
+
 __device__ __forceinline__ int esc_find(const DShared& sh, int s) {
   const uint32_t ne = min(sh.n_esc, (uint32_t)kEscCap);
   for (uint32_t j = 0; j < ne; ++j)
@@ -539,7 +560,7 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
 
   // ---- pass B: E = floor(exp_ds(y - m) * 2^40) in place, S = sum E
   //      (pairs of elements on the packed fp32x2 pipe)
-  uint64_t S = 0;
+  WeightSum sw = {0u, 0u, 0u};
   uint32_t ovf = 0;
   const float2 mneg = f2(-m);
   if (scale) {
@@ -554,8 +575,8 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
                  ? 1u : 0u;
       const float2 ea = weight40x2(add2_rn(ya, mneg));
       const float2 eb = weight40x2(add2_rn(yb, mneg));
-      S += __float2ull_rz(ea.x) + __float2ull_rz(ea.y) + __float2ull_rz(eb.x) +
-           __float2ull_rz(eb.y);
+      sum_weights2(ea, sw);
+      sum_weights2(eb, sw);
       reinterpret_cast<float4*>(sl)[g] = make_float4(ea.x, ea.y, eb.x, eb.y);
     }
   } else {
@@ -564,11 +585,12 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
       const float4 x4 = reinterpret_cast<const float4*>(sl)[g];
       const float2 ea = weight40x2(add2_rn(make_float2(x4.x, x4.y), mneg));
       const float2 eb = weight40x2(add2_rn(make_float2(x4.z, x4.w), mneg));
-      S += __float2ull_rz(ea.x) + __float2ull_rz(ea.y) + __float2ull_rz(eb.x) +
-           __float2ull_rz(eb.y);
+      sum_weights2(ea, sw);
+      sum_weights2(eb, sw);
       reinterpret_cast<float4*>(sl)[g] = make_float4(ea.x, ea.y, eb.x, eb.y);
     }
   }
+  uint64_t S = weight_sum_total(sw);
   for (int i = tid; i < kBins + 16; i += kThr) sh.hist[i] = 0u;
   S = warp_reduce(S, OpAddU64());
   ovf = warp_reduce(ovf, OpOrU32());

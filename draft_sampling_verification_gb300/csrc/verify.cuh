@@ -9,7 +9,6 @@ namespace {  // device code private to each translation unit that includes it
 
 constexpr int kVCluster = 8;
 constexpr int kVThreads = 256;
-constexpr float kTwo46f = 70368744177664.0f;
 constexpr uint64_t kNearTol = 70368745ull;   // ceil(1e-6 * 2^46)
 
 enum VerifyMode { kGreedy = 0, kRatio = 1 };
@@ -62,6 +61,7 @@ struct VSh2 {
   // ([buffer][writer's rank]), so that after it the merge reads local memory
   VX px[2][kVMaxNC];
   uint64_t bsum[kVMaxBlocks];
+  uint32_t qblk[32 * 8];  // final draw: a sparse q row's counts over one block of ids
   float wm[8], ws[8], wam[8];
   int wai[8];
   uint64_t wz[8], wc[8];
@@ -90,6 +90,25 @@ template <bool kCoh, typename T>
 __device__ __forceinline__ T ldq(const T* p) {
   if (kCoh) return *p;
   return __ldg(p);
+}
+
+// The final draw's fixed-point weight floor(r * 2^46), r in [0, 1], as
+// hi * 2^23 + lo with hi = floor(r 2^23) and lo = floor((r 2^23 - hi) 2^23),
+// read from the bits of round-down sums with 2^23 (each exact: the sums lie
+// in [2^23, 2^24], where floats are the integers): no float-to-integer
+// conversion, and the sums of a block fit 32-bit integers.
+struct Fix46 {
+  uint32_t hi, lo;
+};
+__device__ __forceinline__ Fix46 fix46(float r) {
+  const float a = __fmul_rn(r, 8388608.0f);                     // r * 2^23, exact
+  const float t1 = __fadd_rd(a, 8388608.0f);                    // 2^23 + floor(a)
+  const float f = __fsub_rn(a, __fsub_rn(t1, 8388608.0f));      // a - floor(a), exact
+  const float t2 = __fmaf_rd(f, 8388608.0f, 8388608.0f);        // 2^23 + floor(f 2^23)
+  return {__float_as_uint(t1) - 0x4B000000u, __float_as_uint(t2) - 0x4B000000u};
+}
+__device__ __forceinline__ uint64_t fix46_u64(Fix46 w) {
+  return ((uint64_t)w.hi << 23) + w.lo;
 }
 
 struct OpMaxNaNv {
@@ -216,6 +235,16 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
         const uint32_t bytes = (uint32_t)(g1 - g0) * 16u;
         mbar_arrive_expect_tx(&mbar[c], bytes);
         if (bytes) tma_load_bulk(vbuf + 16 * g0, gbase + 16 * g0, bytes, &mbar[c]);
+      }
+      if (j < depth) {
+        // the next row's part towards L2 while this row is decided: it is
+        // read next unless this row decides every mode
+        const char* nrow = zrow + p.ld * ESZ;
+        const uintptr_t a0 = (reinterpret_cast<uintptr_t>(nrow + (int64_t)lo * ESZ) + 15u) &
+                             ~(uintptr_t)15u;
+        const uintptr_t a1 = reinterpret_cast<uintptr_t>(nrow + (int64_t)(lo + n) * ESZ) &
+                             ~(uintptr_t)15u;
+        if (a1 > a0) prefetch_l2(reinterpret_cast<const void*>(a0), (uint32_t)(a1 - a0));
       }
     }
     if (tid < 2 * EPG) {
@@ -472,58 +501,60 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
 
     // ---- final draw over row j: residual max(p - q, 0) or p itself
     const uint32_t wdraw = draw_u32(p.seed, req, (uint32_t)j, purpose);
-    const float invS = __frcp_rn(S);
+    // p(v) = 2^((z - M) log2(e) - log2(S)) by the hardware base-2 exponential
+    // (relative error a few 2^-23; -inf gives 0), one rounding of the argument
+    const float nlgS = -log2f(S);
     auto pv = [&](float z) -> float {
-      return (z == -INFINITY) ? 0.0f : __fmul_rn(expf(z - M), invS);
+      float e;
+      const float a = __fmaf_rn(__fsub_rn(z, M), 1.4426950408889634f, nlgS);
+      asm("ex2.approx.f32 %0, %1;" : "=f"(e) : "f"(a));
+      return e;
     };
-    auto wfix = [&](float r) -> uint64_t { return __float2ull_rz(__fmul_rn(r, kTwo46f)); };
-    // q of the sparse row at id v (binary search; -1 ids never match)
-    auto sparse_q = [&](int v) -> uint32_t {
-      int a = 0, e = snnz - 1;
-      while (a <= e) {
-        const int mid = (a + e) >> 1;
-        const int id = ldq<kCohQ>(sids + mid);
-        if (id == v) return ldq<kCohQ>(scnt + mid);
-        if (id < v) a = mid + 1;
-        else e = mid - 1;
-      }
-      return 0u;
-    };
+    auto wfix = [&](float r) -> uint64_t { return fix46_u64(fix46(r)); };
     const int nblk = (ng + 31) / 32;
     const bool qvec = qrow != nullptr &&
                       (reinterpret_cast<uintptr_t>(qrow + lo - off) & 15u) == 0u;
+    // the EPG counts of group g of the dense q row (128-bit loads for a full,
+    // aligned group; 0 outside the slice)
+    auto load_q = [&](int g, uint32_t* qv) {
+#pragma unroll
+      for (int i = 0; i < EPG; ++i) qv[i] = 0u;
+      if (qvec && g >= g_first && g <= g_last) {
+        const uint4* qp = reinterpret_cast<const uint4*>(qrow + lo - off) + g * (EPG / 4);
+#pragma unroll
+        for (int k = 0; k < EPG / 4; ++k) {
+          const uint4 t4 = ldq<kCohQ>(qp + k);
+          qv[4 * k] = t4.x;
+          qv[4 * k + 1] = t4.y;
+          qv[4 * k + 2] = t4.z;
+          qv[4 * k + 3] = t4.w;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < EPG; ++i) {
+          const int s = g * EPG + i;
+          if (s >= off && s < off + n) qv[i] = ldq<kCohQ>(qrow + (lo - off + s));
+        }
+      }
+    };
     for (int attempt = 0; attempt < 2; ++attempt) {
       const bool dense_q = use_q && qrow != nullptr;
       const bool sparse_qm = use_q && sids != nullptr;
       uint64_t zs = 0, cs = 0;
+      // the counts of a thread's next group are loaded one step ahead, so that
+      // their latency overlaps the current group's arithmetic
+      uint32_t qn[EPG];
+#pragma unroll
+      for (int i = 0; i < EPG; ++i) qn[i] = 0u;
+      if (dense_q && tid < ng) load_q(tid, qn);
       for (int gb = 0; gb < ng; gb += kVThreads) {
         const int g = gb + tid;
-        uint64_t gsum = 0;
+        uint32_t ghi = 0, glo = 0;  // the group's weights: sum hi * 2^23 + sum lo
+        uint32_t qv[EPG];
+#pragma unroll
+        for (int i = 0; i < EPG; ++i) qv[i] = qn[i];
+        if (dense_q && g + kVThreads < ng) load_q(g + kVThreads, qn);
         if (g < ng) {
-          // the counts first (128-bit loads for a full, aligned group), then
-          // the weights
-          uint32_t qv[EPG];
-#pragma unroll
-          for (int i = 0; i < EPG; ++i) qv[i] = 0u;
-          if (dense_q) {
-            if (qvec && g >= g_first && g <= g_last) {
-              const uint4* qp = reinterpret_cast<const uint4*>(qrow + lo - off) + g * (EPG / 4);
-#pragma unroll
-              for (int k = 0; k < EPG / 4; ++k) {
-                const uint4 t4 = ldq<kCohQ>(qp + k);
-                qv[4 * k] = t4.x;
-                qv[4 * k + 1] = t4.y;
-                qv[4 * k + 2] = t4.z;
-                qv[4 * k + 3] = t4.w;
-              }
-            } else {
-#pragma unroll
-              for (int i = 0; i < EPG; ++i) {
-                const int s = g * EPG + i;
-                if (s >= off && s < off + n) qv[i] = ldq<kCohQ>(qrow + (lo - off + s));
-              }
-            }
-          }
           float z[EPG];
           group(g, z);
 #pragma unroll
@@ -533,17 +564,19 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
               cs += qv[i];
               r = fmaxf(__fsub_rn(r, (float)qv[i] * 0x1p-24f), 0.0f);
             }
-            gsum += wfix(r);
+            const Fix46 w = fix46(r);
+            ghi += w.hi;
+            glo += w.lo;
           }
         }
-        // one block = the 32 groups of one warp in one iteration; gsum is at
-        // most EPG * 2^46 < 2^50 (r <= p <= 1), summed as two 25-bit halves
-        // with the 32-bit warp reduction
-        const uint32_t blo = __reduce_add_sync(0xffffffffu, (uint32_t)(gsum & 0x1FFFFFFull));
-        const uint32_t bhi = __reduce_add_sync(0xffffffffu, (uint32_t)(gsum >> 25));
-        const uint64_t bs = ((uint64_t)bhi << 25) + blo;
+        // one block = the 32 groups of one warp in one iteration: each half
+        // is at most 32 * EPG * 2^23 <= 2^31, summed by the 32-bit warp
+        // reduction
+        const uint32_t bhi = __reduce_add_sync(0xffffffffu, ghi);
+        const uint32_t blo = __reduce_add_sync(0xffffffffu, glo);
+        const uint64_t bs = ((uint64_t)bhi << 23) + blo;
         if (lane == 0 && gb / 32 + warp < nblk) sh.bsum[gb / 32 + warp] = bs;
-        zs += gsum;
+        zs += ((uint64_t)ghi << 23) + glo;
       }
       __syncthreads();
       if (sparse_qm) {
@@ -649,6 +682,31 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
             const int g = blk * 32 + lane;
             uint64_t wv[EPG];
             uint64_t gsum = 0;
+            // the block's counts: a dense row's by 128-bit loads, issued
+            // before any arithmetic; a sparse row's support ids that fall in
+            // the block's id range, found by the whole warp and scattered
+            // into shared memory
+            uint32_t qv[EPG];
+#pragma unroll
+            for (int i = 0; i < EPG; ++i) qv[i] = 0u;
+            if (use_q && qrow && g < ng) load_q(g, qv);
+            if (use_q && sids) {
+              const int v0 = lo - off + blk * 32 * EPG;  // id of the block's first position
+#pragma unroll
+              for (int i = 0; i < EPG; ++i) sh.qblk[i * 32 + lane] = 0u;
+              __syncwarp();
+              for (int k = lane; k < snnz; k += 32) {
+                const int id = ldq<kCohQ>(sids + k);
+                const int rel = id - v0;
+                if (rel >= 0 && rel < 32 * EPG) sh.qblk[rel] = ldq<kCohQ>(scnt + k);
+              }
+              __syncwarp();
+#pragma unroll
+              for (int i = 0; i < EPG; ++i) {
+                const int s = g * EPG + i;
+                qv[i] = (s >= off && s < off + n) ? sh.qblk[lane * EPG + i] : 0u;
+              }
+            }
             if (g < ng) {
               float z[EPG];
               group(g, z);
@@ -657,10 +715,7 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
                 const int s = g * EPG + i;
                 const bool in = (s >= off && s < off + n);
                 float r = pv(z[i]);
-                if (use_q && in) {
-                  const uint32_t q = qrow ? ldq<kCohQ>(qrow + (lo - off + s)) : sparse_q(lo - off + s);
-                  r = fmaxf(__fsub_rn(r, (float)q * 0x1p-24f), 0.0f);
-                }
+                if (use_q && in) r = fmaxf(__fsub_rn(r, (float)qv[i] * 0x1p-24f), 0.0f);
                 wv[i] = wfix(r);
                 gsum += wv[i];
               }
