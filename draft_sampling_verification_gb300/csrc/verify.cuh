@@ -111,6 +111,16 @@ __device__ __forceinline__ uint64_t fix46_u64(Fix46 w) {
   return ((uint64_t)w.hi << 23) + w.lo;
 }
 
+constexpr float kLog2e = 1.4426950408889634f;
+
+// 2^x by the hardware approximation (ex2.approx: a few units in the last place
+// of relative error; 2^-inf = 0)
+__device__ __forceinline__ float ex2_approx(float x) {
+  float e;
+  asm("ex2.approx.f32 %0, %1;" : "=f"(e) : "f"(x));
+  return e;
+}
+
 struct OpMaxNaNv {
   __device__ float operator()(float a, float b) const {
     float r;
@@ -350,13 +360,14 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
     float cm = sh.wm[0];  // the CTA's max
     for (int w = 1; w < kVThreads / 32; ++w) cm = OpMaxNaNv()(cm, sh.wm[w]);
     if (kD && need_r) {
-      // the sum of exp relative to the CTA's max: a plain sum
+      // the sum of exp relative to the CTA's max: a plain sum, each term by
+      // the hardware base-2 exponential (relative error a few 2^-23)
       if (cm > -INFINITY && cm < INFINITY)
         for (int g = tid; g < ng; g += kVThreads) {
           float z[EPG];
           group(g, z);
 #pragma unroll
-          for (int i = 0; i < EPG; ++i) sm += expf(__fsub_rn(z[i], cm));
+          for (int i = 0; i < EPG; ++i) sm += ex2_approx(__fmul_rn(__fsub_rn(z[i], cm), kLog2e));
         }
       sm = warp_reduce(sm, OpAddF());
       if (lane == 0) sh.ws[warp] = sm;
@@ -505,10 +516,7 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
     // (relative error a few 2^-23; -inf gives 0), one rounding of the argument
     const float nlgS = -log2f(S);
     auto pv = [&](float z) -> float {
-      float e;
-      const float a = __fmaf_rn(__fsub_rn(z, M), 1.4426950408889634f, nlgS);
-      asm("ex2.approx.f32 %0, %1;" : "=f"(e) : "f"(a));
-      return e;
+      return ex2_approx(__fmaf_rn(__fsub_rn(z, M), kLog2e, nlgS));
     };
     auto wfix = [&](float r) -> uint64_t { return fix46_u64(fix46(r)); };
     const int nblk = (ng + 31) / 32;
