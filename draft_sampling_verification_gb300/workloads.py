@@ -24,11 +24,15 @@ Recipes (sizes at full scale):
 * C4  B=256: Zipf draft fp32, target = bf16(draft + N(0, 0.7^2)); per
   (request, position) exactly 10 % of ids (a seeded affine selection) masked
   to -inf in both the draft row and its target row (target row 5 has its own
-  mask); 1 % of draft rows carry a
-  top logit shared by g in {3, 5, 7} ids spread over the vocabulary and the
-  whole row snapped to a 1/4 grid, so many tokens (the argmax group among
-  them) share identical remainders and the lowest-id rule decides the grant;
-  dense q; greedy and ratio; seed 3.
+  mask); 1 % of draft rows carry a top logit shared by g in {3, 5, 7} ids
+  spread over the vocabulary (0.5 above the row's own maximum), so the draft
+  argmax sits on g tied remainders.  In each such row two more unmasked
+  ids, the tuners, get the logits (group logit - delta) and (group logit -
+  delta_fine), the offsets chosen per row with the oracle
+  (tests/golden/make_c4_ties.py, stored in tests/golden/c4_tie_rows.json) so
+  that the group straddles the grant threshold: some of its members get the
+  remaining ticket and the rest do not, and the lowest-id rule decides
+  which; dense q; greedy and ratio; seed 3.
 * C5  sweep B in {1, 8, 32, 128, 512, 1024} with the C3 generators, sparse
   top-256 or dense q, three target variants: ``mixed`` (as C3), ``accept``
   (draft argmax raised by 30 nats so q is one-hot, target = draft), and
@@ -37,6 +41,8 @@ Recipes (sizes at full scale):
 """
 from __future__ import annotations
 
+import json
+import os
 from dataclasses import dataclass, field
 from math import gcd
 
@@ -200,31 +206,62 @@ def config3(B=64, V=V_FULL, depth=DEPTH, rng=None, top_k=TOP_K, variant="mixed",
                     _req(B), {"variant": variant})
 
 
-def config4(B=256, V=V_FULL, depth=DEPTH, rng=None, tie_fraction=0.01, mask_fraction=0.10):
+_C4_TIES = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "tests",
+                        "golden", "c4_tie_rows.json")
+
+
+def c4_tie_tuning():
+    """The stored tuner offsets of the C4 tie rows (B = 256), or None."""
+    try:
+        with open(_C4_TIES) as f:
+            return json.load(f)
+    except OSError:
+        return None
+
+
+def config4(B=256, V=V_FULL, depth=DEPTH, rng=None, tie_fraction=0.01, mask_fraction=0.10,
+            tuning="stored"):
+    """tuning: "stored" applies the stored tuner offsets when they were made
+    for this workload (B = 256 at full size, default generator), None leaves
+    every tuner at its own Zipf logit (the raw rows the offsets are chosen on)."""
+    table = c4_tie_tuning() if (tuning == "stored" and rng is None) else None
+    if table is not None and (table.get("B"), table.get("V"), table.get("depth")) != (B, V, depth):
+        table = None
     rng = rng or np.random.default_rng(1004)
     xd = zipf_rows(rng, B * depth, V).reshape(B, depth, V)
     n_mask = int(round(mask_fraction * V))
     masks = affine_masks(rng, B * (depth + 1), V, n_mask).reshape(B, depth + 1, V)
     tie_rows = []
-    n_tie = max(1, int(round(tie_fraction * B * depth))) if V >= 8 else 0
+    n_tie = max(1, int(round(tie_fraction * B * depth))) if V >= 16 else 0
+    offsets = {(e["b"], e["j"]): (np.float32(float.fromhex(e["delta"])),
+                                  np.float32(float.fromhex(e["delta_fine"])))
+               for e in (table or {}).get("rows", [])}
     for r in rng.choice(B * depth, size=min(n_tie, B * depth), replace=False):
         b, j = divmod(int(r), depth)
         g = int(rng.choice([3, 5, 7]))
         free = np.flatnonzero(~masks[b, j])
-        ids = np.sort(rng.choice(free, size=min(g, free.size), replace=False))
-        row = np.round(xd[b, j] * 4.0) / 4.0
-        row[ids] = row.max() + np.float32(0.5)
-        xd[b, j] = row.astype(np.float32)
-        tie_rows.append((b, j, ids.tolist()))
+        pick = rng.choice(free, size=g + 2, replace=False)
+        ids = np.sort(pick[:g])
+        tuners = [int(pick[g]), int(pick[g + 1])]
+        top = np.float32(xd[b, j].max() + np.float32(0.5))
+        xd[b, j, ids] = top
+        if (b, j) in offsets:
+            for t, dlt in zip(tuners, offsets[(b, j)]):
+                xd[b, j, t] = np.float32(top - dlt)
+        tie_rows.append((b, j, ids.tolist(), tuners))
     xt = np.empty((B, depth + 1, V), np.float32)
     xt[:, :depth] = xd + _normal(rng, (B, depth, V), 0.7)
     xt[:, depth] = zipf_rows(rng, B, V) + _normal(rng, (B, V), 0.7)
     for b in range(B):
         xd[b][masks[b, :depth]] = -np.inf
         xt[b][masks[b]] = -np.inf
+    notes = {"tie_rows": tie_rows}
+    if table is not None:
+        notes.update({k: table[k] for k in ("tie_rows_straddling", "lowest_id_decisive_rows")
+                      if k in table})
     return Workload("C4 B=%d zipf fp32 draft / bf16 target dense, 10%% mask, 1%% ties" % B, B,
                     depth, V, xd, f32_to_bf16_bits(xt), "bf16", _temps(B, depth, 1.0), 0, 3,
-                    ("greedy", "ratio"), _req(B), {"tie_rows": tie_rows})
+                    ("greedy", "ratio"), _req(B), notes)
 
 
 def config5(B, variant="mixed", top_k=TOP_K, V=V_FULL, depth=DEPTH, rng=None):

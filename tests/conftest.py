@@ -43,9 +43,10 @@ def pytest_terminal_summary(terminalreporter):
         tr.write_line(
             "%s: %d requests, %d rows; ambiguous decisions %d; draws near a boundary: "
             "absolute %d, relative %d; band cases absolute %d (%.2e per row, %s), relative %d "
-            "(%.2e per row, %s); GPU-only flags %d; mismatches outside the relative band %d, "
-            "inside %d" % (mode, c.requests, c.rows, c.ambig, c.near_abs, c.near_rel, c.band_abs,
-                           c.band_abs / rows, "bound met" if c.band_abs <= parity.BAND_BOUND * rows
-                           else "bound NOT met", c.band_rel, c.band_rel / rows,
-                           "bound met" if c.band_rel <= parity.BAND_BOUND * rows
-                           else "bound NOT met", c.gpu_only, c.mismatch, c.band_mismatch))
+            "(%.2e per row, %s); GPU-only flags %d; requests differing outside the band %d, "
+            "inside it %d, outside the relative band %d"
+            % (mode, c.requests, c.rows, c.ambig, c.near_abs, c.near_rel, c.band_abs,
+               c.band_abs / rows, "bound met" if c.band_abs <= parity.BAND_BOUND * rows
+               else "bound NOT met", c.band_rel, c.band_rel / rows,
+               "bound met" if c.band_rel <= parity.BAND_BOUND * rows else "bound NOT met",
+               c.gpu_only, c.mismatch, c.band_mismatch, c.rel_mismatch))

@@ -72,7 +72,7 @@ def test_parity_band_counts(oracle):
     bad = bench.parity_band(wl, gpu, ref)
     assert not bad["draft_tokens_equal"]
     flags0 = int(np.asarray(ref[0]["ratio"][2]).ravel()[0])
-    in_band = (flags0 & (bench.FLAG_AMBIG | bench.FLAG_NEAR_REL)) != 0
+    in_band = (flags0 & (bench.FLAG_AMBIG | bench.FLAG_NEAR)) != 0
     assert bad["ratio_mismatch_outside_band"] + bad["ratio_mismatch_in_band"] == 1
     assert bad["ratio_mismatch_in_band"] == int(in_band)
 

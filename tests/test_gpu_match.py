@@ -1,11 +1,12 @@
 """GPU parity of stochastic (match) verification (dspark_verify_match)
 against the oracle: integer outputs bit for bit on every request except
-those whose draw the ORACLE finds within 1e-6 of the picked token's own mass
-of a cumulative boundary (the relative reading of the band; the GPU's own
-flags excuse nothing), on the workloads' rows (fp32 and bf16 targets), the
+those whose draw the ORACLE finds within 1e-6 (probability units) of a
+cumulative boundary (the benchmark definition's band; the GPU's own flags
+excuse nothing), on the workloads' rows (fp32 and bf16 targets), the
 all-accept and all-reject extremes, ragged vocabularies and refused rows.
-Band cases under both readings are counted and printed in pytest's summary;
-the relative reading's must stay under 1e-4 of the verify rows."""
+Band cases under both readings (absolute, and relative to the picked
+token's own mass) are counted and printed in pytest's summary; the relative
+reading's must stay under 1e-4 of the verify rows."""
 import numpy as np
 import pytest
 import torch

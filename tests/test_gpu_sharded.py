@@ -167,7 +167,7 @@ def test_cluster_verify_is_the_sharded_verifier(oracle, target):
     and the residual draw picks the CTA by its residual mass, then the token
     inside.  With V = 129,280 the CTAs' slices (4 for bf16 rows, 8 for fp32)
     are the oracle's contiguous shards, and the outputs equal the sharded
-    oracle's on every request outside the oracle's relative band.  q and
+    oracle's on every request outside the oracle's band.  q and
     drafts come from the oracle."""
     wl = W.config4(B=8)
     n_sh = 4 if target == "bf16" else 8

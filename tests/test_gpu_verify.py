@@ -3,18 +3,19 @@ the oracle, at the workloads' full sizes (V = 129,280) and on edge cases.
 
 Greedy outputs are bit-exact.  Ratio outputs (accept length, committed
 tokens, status) are bit-exact on every request except those the ORACLE puts
-in the tolerance band: a decision with |u*q - p| <= 1e-6*q, or a final draw
-within 1e-6 of a cumulative boundary.  The GPU's own flags excuse nothing.
+in the benchmark definition's tolerance band: a decision with
+|u*q - p| <= 1e-6*q, or a final draw within 1e-6 (probability units) of a
+cumulative boundary.  The GPU's own flags excuse nothing.
 
-The band of the draw is counted under two readings: absolute (1e-6 in
-probability units, the literal one) and relative (1e-6 of the picked
-token's own mass, which is what makes the bound of 1e-4 band cases per
-verify row meetable on 129,280-token heavy-tailed rows: every token lighter
-than 2e-6 lies wholly inside the absolute band, so an exact verifier's draws
-land in it on a few percent of the rows).  Excused are only the requests in
-the oracle's relative band; the bound is asserted on the relative reading and
-both rates are printed in pytest's summary.  p is within 1e-6 absolute per
-entry.
+Band cases are counted under two readings of the draw's band: the absolute
+one above (the definition's) and a relative one (1e-6 of the picked token's
+own mass).  On 129,280-token heavy-tailed rows every token lighter than 2e-6
+lies wholly inside the absolute band, so even the exact oracle flags a few
+percent of the rows and the bound of 1e-4 band cases per verify row cannot
+be met under that reading; the relative reading's count meets it and is
+asserted.  Both counts, and the requests that differ inside the band and
+outside the relative one, are printed in pytest's summary.  p is within
+1e-6 absolute per entry.
 """
 import numpy as np
 import pytest
@@ -73,8 +74,9 @@ def test_workload_full_size(oracle, make):
 
 @pytest.mark.parametrize("variant", ["accept", "reject", "mixed"])
 @pytest.mark.parametrize("top_k", [256, 0])
-def test_sweep_variants(oracle, variant, top_k):
-    wl = W.config5(8, variant=variant, top_k=top_k)
+@pytest.mark.parametrize("B", [8, 128])
+def test_sweep_variants(oracle, variant, top_k, B):
+    wl = W.config5(B, variant=variant, top_k=top_k)
     res = run_workload(oracle, wl)
     acc = None
     if variant == "accept":
@@ -184,11 +186,11 @@ def test_target_probs_within_tolerance(oracle, dtype):
 
 def test_zz_ambiguity_budget():
     """Over every ratio verification of this module: no request differs
-    outside the oracle's relative band, and the relative band's cases stay
-    under 1e-4 of the verify rows.  The
-    absolute reading's count is printed beside it: on these heavy-tailed
-    rows it is a property of the inputs (the exact oracle flags them), far
-    above 1e-4, and no implementation could lower it."""
+    outside the oracle's band, and the relative reading's band cases stay
+    under 1e-4 of the verify rows.  The absolute reading's count is printed
+    beside it: on these heavy-tailed rows it is a property of the inputs (the
+    exact oracle flags them), far above 1e-4, and no implementation could
+    lower it."""
     if STATS.rows == 0:
         pytest.skip("no verification ran")
     print("ratio verification:", STATS)

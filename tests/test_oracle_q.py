@@ -280,3 +280,25 @@ def test_draft_sample_refuses_wrong_mass(oracle):
     counts[0, 3] += 1
     tok, st = oracle.draft_sample(counts, None, None, 0, 1, 1, seed=5)
     assert st[0] == 5 and tok[0] == -1
+
+
+@pytest.mark.slow
+def test_c4_tie_rows_straddle_the_threshold(oracle):
+    """C4's tied-argmax rows (1 % of the draft rows): with the stored tuner
+    offsets the oracle splits every tied group at the grant threshold, some
+    members getting the remaining ticket and the others not, the members
+    granted being the lowest ids ("PP1 q transport and scheduling design",
+    Distribution contract and precision: ties by lowest global token id)."""
+    from draft_sampling_verification_gb300 import workloads as W
+    wl = W.config4()
+    assert wl.notes.get("tie_rows_straddling") == len(wl.notes["tie_rows"]) >= 12
+    assert wl.notes.get("lowest_id_decisive_rows", 0) >= len(wl.notes["tie_rows"])
+    for b, j, ids, tuners in wl.notes["tie_rows"]:
+        x = wl.draft[b, j]
+        assert np.all(x[ids] == x.max()) and np.isfinite(x[tuners]).all()
+        counts, _, _, st = oracle.q_build(x[None, :], None, 0)
+        c = counts[0, ids]
+        assert st[0] == 0 and c.max() == c.min() + 1, (b, j, c)
+        # the lowest ids of the group hold the extra ticket
+        granted = c == c.max()
+        assert np.all(granted[:int(granted.sum())]), (b, j, c)
