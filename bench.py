@@ -479,13 +479,12 @@ def run_ours(args, rank, world, local_rank):
         gbias.manual_seed(1234)
         bias = torch.randn((64, V), generator=gbias, device=dev, dtype=torch.float32)
         anchors = torch.from_numpy((req_np % V).astype(np.int32)).to(dev)
-        cws = torch.empty((rows_d * V,), dtype=torch.float32, device=dev)
         ctok = torch.empty((B, depth), dtype=torch.int32, device=dev)
         cst = torch.empty((rows_d,), dtype=torch.int32, device=dev)
         cmg = torch.empty((B, depth), dtype=torch.float32, device=dev)
 
         def chain_step():
-            ds.dspark_q_chain_sample(xd, B, depth, temps, bias, anchors, wl.seed, req, cws,
+            ds.dspark_q_chain_sample(xd, B, depth, temps, bias, anchors, wl.seed, req, None,
                                      counts, ctok, cst, cmg, stream)
 
         for _ in range(max(3, args.warmup)):

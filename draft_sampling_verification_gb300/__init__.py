@@ -235,7 +235,7 @@ def dspark_q_chain_sample(draft_logits, B, depth, temperature, bias, anchors, se
                           request_ids, workspace, counts, draft_tokens, row_status, margins=None,
                           stream=None):
     """draft_logits [B*depth, V] (or [B, depth, V]); bias [n_bias, V] fp32 or None;
-    anchors int32 [B]; workspace fp32 with B*depth*V elements."""
+    anchors int32 [B]; workspace unused (may be None)."""
     rows, V, ld = _rows(draft_logits)
     if rows != B * depth:
         raise ValueError("draft_logits must hold B*depth rows")
@@ -390,13 +390,12 @@ def q_chain_sample(draft_logits, B, depth, seed, anchors, bias=None, temperature
     margins [B, depth])."""
     rows, V, _ = _rows(draft_logits)
     dev = draft_logits.device
-    ws = _empty((rows * V,), torch.float32, dev)
     counts = _empty((rows, V), torch.int32, dev)
     status = _empty((rows,), torch.int32, dev)
     tokens = _empty((B, depth), torch.int32, dev)
     margins = _empty((B, depth), torch.float32, dev)
     dspark_q_chain_sample(draft_logits, B, depth, temperature, bias, anchors, seed, request_ids,
-                          ws, counts, tokens, status, margins, stream)
+                          None, counts, tokens, status, margins, stream)
     q = {"counts": counts, "ids": None, "nnz": None, "status": status, "top_k": 0}
     return q, tokens, margins
 

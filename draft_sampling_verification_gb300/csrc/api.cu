@@ -41,9 +41,8 @@ cudaError_t launch_q_sharded(const void* x, int dtype, int64_t ld, int B, int de
 cudaError_t launch_q_chain(const void* x, int dtype, int64_t ld, int B, int depth, int V,
                            const float* temperature, const float* bias, int64_t bias_ld,
                            int n_bias, const int32_t* anchors, uint64_t seed,
-                           const uint32_t* request_ids, float* workspace, uint32_t* counts,
-                           int32_t* tokens, int32_t* status, float* margins,
-                           cudaStream_t stream);
+                           const uint32_t* request_ids, uint32_t* counts, int32_t* tokens,
+                           int32_t* status, float* margins, cudaStream_t stream);
 cudaError_t launch_verify_match(const void* z, int dtype, int64_t ld, int B, int depth, int V,
                                 const int32_t* drafts, uint64_t seed,
                                 const uint32_t* request_ids, int32_t* accept_len,
@@ -488,7 +487,8 @@ int dspark_q_chain_sample(const void* draft_logits, int32_t dtype, int64_t ld, i
   if (B < 0 || (int64_t)B * depth > kMaxGridRows) return DSPARK_ERR_SIZE;
   if (bias && (n_bias < 1 || bias_ld < V)) return DSPARK_ERR_SIZE;
   if (B == 0) return 0;
-  if (!draft_logits || !anchors || !workspace || !counts || !draft_tokens || !row_status)
+  // the workspace is no longer used (z is formed in shared memory); it may be NULL
+  if (!draft_logits || !anchors || !counts || !draft_tokens || !row_status)
     return DSPARK_ERR_NULL;
   const void* four[] = {anchors, workspace, counts, draft_tokens, row_status, margins,
                         temperature, request_ids, bias};
@@ -497,7 +497,7 @@ int dspark_q_chain_sample(const void* draft_logits, int32_t dtype, int64_t ld, i
   if (!aligned(draft_logits, esize(dtype))) return DSPARK_ERR_ALIGN;
   return launch_result(dspark::launch_q_chain(
       draft_logits, dtype, ld, B, depth, V, temperature, bias, bias_ld, bias ? n_bias : 1,
-      anchors, seed, request_ids, workspace, counts, draft_tokens, row_status, margins,
+      anchors, seed, request_ids, counts, draft_tokens, row_status, margins,
       static_cast<cudaStream_t>(stream)));
 }
 

@@ -5,13 +5,13 @@
 // logits at each step).
 //
 // One 8-CTA cluster per request walks its draft rows in order.  For row j
-// every CTA writes z = RN(x + bias[prev mod n_bias]) over its eighth of the
-// row into the caller's workspace and keeps the top two finite z; the
-// workspace writes are made visible to the bulk copies (an async-proxy fence,
-// then a cluster barrier), and the dense q build with its draft draw (the
-// q_dense row code) runs on z.  The drawn token goes to every CTA through
-// distributed shared memory and conditions row j + 1.  A refused row refuses
-// the rest of its chain with the same status.
+// the dense q build with its draft draw (the q_dense row code) runs on
+// z = RN(x + bias[prev mod n_bias]), formed in shared memory as each CTA's
+// eighth of the base row lands (the bias row is read alongside), and the
+// same pass keeps the row's two largest finite z for the margin.  The drawn
+// token goes to every CTA through distributed shared memory and conditions
+// row j + 1; the next row's base part is prefetched into L2 meanwhile.  A
+// refused row refuses the rest of its chain with the same status.
 #include <cfloat>
 
 #include "q_dense.cuh"
@@ -23,37 +23,23 @@ using qdense::kCl;
 using qdense::kThr;
 
 struct ChainParams {
-  const void* x;  // base logits, row r at x + r * ld elements
-  int dtype;
-  int64_t ld;
   const float* bias;  // [n_bias][bias_ld] or null
   int64_t bias_ld;
   int n_bias;
   const int32_t* anchors;  // [B]
-  float* ws;               // [B * depth][V]: z rows
   float* margins;          // [B * depth] or null
   int depth;
   int V;
 };
 
 struct ChainShared {
-  float t1[kCl], t2[kCl];  // pushed to rank 0: each CTA's top two finite z
-  int tok, st;             // pushed by rank 0: the row's token and status
+  int tok, st;  // pushed by rank 0: the row's token and status
 };
 
-// top two of {a1, a2} and {b1, b2} (a1 >= a2, b1 >= b2)
-__device__ __forceinline__ void top2_merge(float& a1, float& a2, float b1, float b2) {
-  if (b1 > a1) {
-    a2 = fmaxf(a1, b2);
-    a1 = b1;
-  } else {
-    a2 = fmaxf(a2, b1);
-  }
-}
-
 __device__ __noinline__ void chain_q_row(const qdense::Params& qp, int row, qdense::DShared& sh,
-                                         float* sl, uint64_t* mbar, uint32_t& phase) {
-  qdense::q_dense_row(qp, row, sh, sl, mbar, phase, nullptr);
+                                         float* sl, uint64_t* mbar, uint32_t& phase,
+                                         int next_row, const float* zbias) {
+  qdense::q_dense_row(qp, row, sh, sl, mbar, phase, nullptr, next_row, true, zbias);
 }
 
 __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThr, 3)
@@ -62,10 +48,9 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThr, 3)
   __shared__ qdense::DShared sh;
   __shared__ uint64_t mbar[qdense::kTma];
   __shared__ ChainShared cs;
-  __shared__ float wt1[kThr / 32], wt2[kThr / 32];
   extern __shared__ __align__(128) float sl[];
   const int rank = (int)cluster.block_rank();
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x;
   if (tid == 0) {
     for (int c = 0; c < qdense::kTma; ++c) mbar_init(&mbar[c], 1);
     mbar_init_fence();
@@ -74,13 +59,10 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThr, 3)
   uint32_t phase = 0;
   const int b = blockIdx.x / kCl;
   const int V = cp.V, depth = cp.depth;
-  const int chunk = (V + kCl - 1) / kCl;
-  const int lo = min(V, rank * chunk), hi = min(V, lo + chunk);
-  const int esz = (cp.dtype == DSPARK_F32) ? 4 : 2;
+  const int lo = min(V, rank * qp.chunk), hi = min(V, lo + qp.chunk);
   const int anchor = cp.anchors[b];
   int prev = anchor;
   int refused = (anchor < 0 || anchor >= V) ? DSPARK_ST_BAD_DRAFT : DSPARK_ST_OK;
-
   for (int j = 0; j < depth; ++j) {
     const int row = b * depth + j;
     if (refused != DSPARK_ST_OK) {
@@ -92,45 +74,8 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThr, 3)
       }
       continue;
     }
-    // ---- z over this CTA's range, and its top two finite values
-    const char* xrow = reinterpret_cast<const char*>(cp.x) + (int64_t)row * cp.ld * esz;
     const float* brow = cp.bias ? cp.bias + (int64_t)(prev % cp.n_bias) * cp.bias_ld : nullptr;
-    float* zrow = cp.ws + (int64_t)row * V;
-    float t1 = -INFINITY, t2 = -INFINITY;
-    for (int v = lo + tid; v < hi; v += kThr) {
-      const float x = load_logit(xrow, cp.dtype, v);
-      const float z = brow ? __fadd_rn(x, __ldg(brow + v)) : x;
-      zrow[v] = z;
-      if (z > -INFINITY && z < INFINITY) top2_merge(t1, t2, z, -INFINITY);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float o1 = __shfl_xor_sync(0xffffffffu, t1, o);
-      const float o2 = __shfl_xor_sync(0xffffffffu, t2, o);
-      top2_merge(t1, t2, o1, o2);
-    }
-    if (lane == 0) {
-      wt1[warp] = t1;
-      wt2[warp] = t2;
-    }
-    // the workspace rows are read next by bulk copies (the async proxy)
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-      float c1 = wt1[0], c2 = wt2[0];
-      for (int w = 1; w < kThr / 32; ++w) top2_merge(c1, c2, wt1[w], wt2[w]);
-      ChainShared* r0 = cluster.map_shared_rank(&cs, 0);
-      r0->t1[rank] = c1;
-      r0->t2[rank] = c2;
-    }
-    cluster.sync();
-    float m1 = -INFINITY, m2 = -INFINITY;
-    if (rank == 0 && tid == 0)
-      for (int r = 0; r < kCl; ++r) top2_merge(m1, m2, cs.t1[r], cs.t2[r]);
-
-    // ---- the dense q of z and its draft draw
-    chain_q_row(qp, row, sh, sl, mbar, phase);
+    chain_q_row(qp, row, sh, sl, mbar, phase, (j + 1 < depth) ? row + 1 : -1, brow);
 
     // ---- the drawn token (and status) to every CTA
     __threadfence();
@@ -141,6 +86,7 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThr, 3)
       if (cp.margins) {
         float mg = 0.0f;
         if (st == DSPARK_ST_OK) {
+          const float m1 = sh.top1, m2 = sh.top2;
           mg = (m2 == -INFINITY) ? FLT_MAX : __fsub_rn(m1, m2);
           if (!(mg <= FLT_MAX)) mg = FLT_MAX;
         }
@@ -164,13 +110,12 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThr, 3)
 cudaError_t launch_q_chain(const void* x, int dtype, int64_t ld, int B, int depth, int V,
                            const float* temperature, const float* bias, int64_t bias_ld,
                            int n_bias, const int32_t* anchors, uint64_t seed,
-                           const uint32_t* request_ids, float* workspace, uint32_t* counts,
-                           int32_t* tokens, int32_t* status, float* margins,
-                           cudaStream_t stream) {
+                           const uint32_t* request_ids, uint32_t* counts, int32_t* tokens,
+                           int32_t* status, float* margins, cudaStream_t stream) {
   qdense::Params qp;
-  qp.x = workspace;
-  qp.dtype = DSPARK_F32;
-  qp.ld = V;
+  qp.x = x;
+  qp.dtype = dtype;
+  qp.ld = ld;
   qp.n_rows = B * depth;
   qp.V = V;
   qp.temperature = temperature;
@@ -183,7 +128,7 @@ cudaError_t launch_q_chain(const void* x, int dtype, int64_t ld, int B, int dept
   qp.seed = seed;
   qp.request_ids = request_ids;
   qp.depth = depth;
-  ChainParams cp{x, dtype, ld, bias, bias_ld, n_bias, anchors, workspace, margins, depth, V};
+  ChainParams cp{bias, bias_ld, n_bias, anchors, margins, depth, V};
   const int smem = (qchunk + 4) * 4;
   cudaError_t e =
       cudaFuncSetAttribute(q_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

@@ -61,6 +61,7 @@ struct __align__(16) Push {
   uint32_t fl3[kCl];    // after pass C: bit1 internal (escape list full)
   uint32_t csum[kCl];   // sum of the counts written before member grants
   uint32_t ncand[kCl];  // members of the threshold bin
+  float t1[kCl], t2[kCl];  // Markov chain rows: each CTA's two largest finite z
 };
 
 // Many-member path: member positions compacted per window, then the table of
@@ -117,6 +118,8 @@ struct DShared {
   uint32_t sel_above, sel_count, scan_base;
   uint32_t draw;  // the row's 24-bit draft draw (fused draw only)
   uint32_t n_merged;  // many-member path: non-empty merged table slots
+  float top1, top2;   // Markov chain rows: the row's two largest finite z
+  float wt1[kWarps], wt2[kWarps];
 };
 constexpr int kAllCap = kBins * 4 / (int)sizeof(Cand);
 
@@ -135,6 +138,16 @@ struct Params {
   const uint32_t* request_ids;
   int depth;
 };
+
+// top two of {a1, a2} and {b1, b2} (a1 >= a2, b1 >= b2)
+__device__ __forceinline__ void top2_merge(float& a1, float& a2, float b1, float b2) {
+  if (b1 > a1) {
+    a2 = fmaxf(a1, b2);
+    a1 = b1;
+  } else {
+    a2 = fmaxf(a2, b1);
+  }
+}
 
 __device__ __forceinline__ float fmax_nan(float a, float b) {
   float r;
@@ -404,10 +417,14 @@ __device__ void ordered_ranks(cg::cluster_group& cluster, DShared& sh, int ngrou
 // ready[row / depth] is incremented once the row's counts, status and token
 // are visible device-wide.  When next_row >= 0, this CTA's part of that row
 // is prefetched into L2 while this row is built (the same cluster takes it
-// next, so its bulk copies then read L2).
+// next, so its bulk copies then read L2).  A Markov chain row (chain true)
+// builds z = RN(x + bias) with the bias row zbias (fp32, element v at
+// zbias[v]; z = x when zbias is null), formed in shared memory as the slice
+// lands, and sh.top1 / sh.top2 get the row's two largest finite z.
 __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& sh, float* sl,
                                             uint64_t* mbar, uint32_t& phase, uint32_t* ready,
-                                            int next_row = -1) {
+                                            int next_row = -1, bool chain = false,
+                                            const float* zbias = nullptr) {
   cg::cluster_group cluster = cg::this_cluster();
   uint32_t* slu = reinterpret_cast<uint32_t*>(sl);
 
@@ -484,34 +501,121 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
   }
   __syncthreads();
 
-  // ---- pass A: NaN-propagating max of the raw logits
+  // ---- pass A: NaN-propagating max of the raw logits (of z for a chain row)
   float mx = -INFINITY;
+  float zt1 = -INFINITY, zt2 = -INFINITY;  // chain rows: the thread's two largest finite z
+  // chain rows: the bias values of a group (0 outside the slice), by one
+  // 128-bit load when the bias row is aligned like the slice's groups
+  const bool bvec = zbias && ((reinterpret_cast<uintptr_t>(zbias + (lo - off)) & 15u) == 0u);
+  auto bias4 = [&](int g) -> float4 {
+    if (bvec && g >= g_first && g <= g_last)
+      return __ldg(reinterpret_cast<const float4*>(zbias + (lo - off)) + g);
+    float b[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int s = 4 * g + i;
+      b[i] = (s >= off && s < off + n) ? __ldg(zbias + (lo - off + s)) : 0.0f;
+    }
+    return make_float4(b[0], b[1], b[2], b[3]);
+  };
+  constexpr int kBPre = 4;  // groups of a chunk per thread whose bias is loaded ahead
   for (int c = 0; c < kTma; ++c) {
     int g0 = use_tma ? chunk_lo[c] : (c == 0 ? 0 : ngroups);
     int g1 = use_tma ? chunk_lo[c + 1] : ngroups;
     if (c == 0) g0 = 0;                 // the head edge group
     if (c == kTma - 1) g1 = ngroups;    // the tail edge group
+    float4 bpre[kBPre];
+    if (zbias) {
+      // loaded before the wait for the chunk's copy, so the two overlap
+#pragma unroll
+      for (int k = 0; k < kBPre; ++k) {
+        const int g = g0 + tid + k * kThr;
+        bpre[k] = (g < g1) ? bias4(g) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      }
+    }
     if (use_tma) {
       if (tid == 0 && !mbar_wait_bounded(&mbar[c], phase)) sh.timeout = 1;
       __syncthreads();
     }
-    for (int g = g0 + tid; g < g1; g += kThr) {
-      const float4 v = reinterpret_cast<const float4*>(sl)[g];
-      mx = fmax_nan(mx, fmax_nan(fmax_nan(v.x, v.y), fmax_nan(v.z, v.w)));
+    if (!chain) {
+      for (int g = g0 + tid; g < g1; g += kThr) {
+        const float4 v = reinterpret_cast<const float4*>(sl)[g];
+        mx = fmax_nan(mx, fmax_nan(fmax_nan(v.x, v.y), fmax_nan(v.z, v.w)));
+      }
+    } else {
+      // z = RN(x + bias) in place (the -inf padding of the edge groups stays)
+      int k = 0;
+      for (int g = g0 + tid; g < g1; g += kThr, ++k) {
+        const float4 v = reinterpret_cast<const float4*>(sl)[g];
+        float z[4] = {v.x, v.y, v.z, v.w};
+        if (zbias) {
+          float4 b4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+          for (int kk = 0; kk < kBPre; ++kk)
+            if (kk == k) b4 = bpre[kk];
+          if (k >= kBPre) b4 = bias4(g);
+          const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int s = 4 * g + i;
+            if (s >= off && s < off + n) z[i] = __fadd_rn(z[i], bb[i]);
+          }
+          reinterpret_cast<float4*>(sl)[g] = make_float4(z[0], z[1], z[2], z[3]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          mx = fmax_nan(mx, z[i]);
+          if (z[i] > -INFINITY && z[i] < INFINITY) {
+            if (z[i] > zt1) {
+              zt2 = zt1;
+              zt1 = z[i];
+            } else {
+              zt2 = fmaxf(zt2, z[i]);
+            }
+          }
+        }
+      }
     }
   }
   if (use_tma) phase ^= 1u;
   mx = warp_reduce(mx, OpMaxNaN());
   if (lane == 0) sh.wredf[warp] = mx;
+  if (chain) {
+    // the CTA's two largest finite z (warp 0 of the block, then pushed)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float o1 = __shfl_xor_sync(0xffffffffu, zt1, o);
+      const float o2 = __shfl_xor_sync(0xffffffffu, zt2, o);
+      top2_merge(zt1, zt2, o1, o2);
+    }
+    if (lane == 0) {
+      sh.wt1[warp] = zt1;
+      sh.wt2[warp] = zt2;
+    }
+  }
   __syncthreads();
   if (warp == 0) {
     const float m2 = warp0_combine(sh.wredf, -INFINITY, OpMaxNaN());
+    float c1 = -INFINITY, c2 = -INFINITY;
+    if (chain) {
+      for (int w = 0; w < kWarps; ++w) top2_merge(c1, c2, sh.wt1[w], sh.wt2[w]);
+    }
     if (lane < kCl) {
       *cluster.map_shared_rank(&sh.push.mx[rank], lane) = m2;
       *cluster.map_shared_rank(&sh.push.fl1[rank], lane) = sh.timeout ? 4u : 0u;
+      if (chain) {
+        *cluster.map_shared_rank(&sh.push.t1[rank], lane) = c1;
+        *cluster.map_shared_rank(&sh.push.t2[rank], lane) = c2;
+      }
     }
   }
   cluster.sync();  // S1
+  if (chain && warp == 1 && lane == 0) {
+    float c1 = -INFINITY, c2 = -INFINITY;
+    for (int r = 0; r < kCl; ++r) top2_merge(c1, c2, sh.push.t1[r], sh.push.t2[r]);
+    sh.top1 = c1;
+    sh.top2 = c2;
+  }
   if (warp == 0) {
     float mm = -INFINITY;
     uint32_t fl = 0;
@@ -874,7 +978,12 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
     weight_split_ef(weight40(__fsub_rn(y, m)), &Ei, &se);
     return frac_key(alloc_split(Ei, se, mk, ek));
   };
-  auto x_at = [&](int s) -> float { return load_logit(xrow, p.dtype, (int64_t)(lo - off + s)); };
+  // the logit of slice position s again (the slice holds other values by
+  // now); a chain row's is z = RN(x + bias)
+  auto x_at = [&](int s) -> float {
+    const float x = load_logit(xrow, p.dtype, (int64_t)(lo - off + s));
+    return zbias ? __fadd_rn(x, __ldg(zbias + (lo - off + s))) : x;
+  };
   auto exact_key = [&](int s) -> uint64_t { return key_of_x(x_at(s)); };
   const uint32_t my_cand = sh.n_cand;
   for (uint32_t j = tid; j < min(my_cand, (uint32_t)kCandCap); j += kThr)

@@ -415,10 +415,10 @@ int dspark_target_probs(const void* target_logits, int32_t dtype, int64_t ld, in
  * on); an anchor outside [0, V) refuses the request with BAD_DRAFT.
  *
  * draft_logits [B*depth][ld] (fp32 or bf16); bias [n_bias][bias_ld] fp32
- * (bias_ld >= V, n_bias >= 1) or NULL; anchors[B]; workspace: B*depth*V fp32
- * of device memory owned by the caller (z rows; overwritten); counts
- * [B*depth][V], draft_tokens[B][depth], row_status[B*depth] as in
- * dspark_q_build_sample.
+ * (bias_ld >= V, n_bias >= 1) or NULL; anchors[B]; workspace: unused (z is
+ * formed in shared memory), may be NULL, kept for the argument order of
+ * earlier versions; counts [B*depth][V], draft_tokens[B][depth],
+ * row_status[B*depth] as in dspark_q_build_sample.
  */
 int dspark_q_chain_sample(const void* draft_logits, int32_t dtype, int64_t ld, int32_t B,
                           int32_t depth, int32_t V, const float* temperature, const float* bias,
