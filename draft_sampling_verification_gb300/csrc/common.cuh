@@ -302,6 +302,43 @@ __device__ __forceinline__ uint64_t frac_key(const AllocSplit& a) {
 // FP64 operations would round it, with integer arithmetic only (FP64 is slow
 // on this GPU): k = mk * 2^ek with mk in [2^52, 2^53); also khi = RN32(k) and
 // klo = RN32(k - khi).
+// floor(2^116 / m) and the remainder *rem, for m in (2^52, 2^53), without a
+// 128-bit division (a long software loop on the GPU): Newton's iteration
+// y <- y + y (2^116 - y m) / 2^116 from a seed of the fp32 reciprocal of m's
+// top 32 bits (relative error below 2^-22), twice (error below 2^-44, then a
+// few units), then exact corrections on the 128-bit remainder.
+__device__ __forceinline__ uint64_t div_2p116(uint64_t m, uint64_t* rem) {
+  const unsigned __int128 num = (unsigned __int128)1 << 116;
+  const uint32_t mh = (uint32_t)(m >> 21);  // [2^31, 2^32)
+  const float f = __fmul_rn(__frcp_rn(__uint2float_rn(mh)), 0x1p95f);  // ~ 2^95 / mh <= 2^64
+  uint64_t y = (f >= 0x1p64f) ? ~0ull : __float2ull_rz(f);
+#pragma unroll
+  for (int it = 0; it < 2; ++it) {
+    const unsigned __int128 p = (unsigned __int128)y * m;
+    // e = 2^116 - y m, |e| < 2^95; y += y e / 2^116 with e taken to 2^52
+    if (p <= num) {
+      const uint64_t eh = (uint64_t)((num - p) >> 52);
+      y += (uint64_t)(((unsigned __int128)y * eh) >> 64);
+    } else {
+      const uint64_t eh = (uint64_t)((p - num) >> 52);
+      y -= (uint64_t)(((unsigned __int128)y * eh) >> 64);
+    }
+  }
+  // exact: y m <= 2^116 < (y + 1) m (a few steps at most; bounded)
+  unsigned __int128 p = (unsigned __int128)y * m;
+  for (int i = 0; i < 64 && p > num; ++i) {
+    --y;
+    p -= m;
+  }
+  unsigned __int128 r = num - p;
+  for (int i = 0; i < 64 && r >= m; ++i) {
+    ++y;
+    r -= m;
+  }
+  *rem = (uint64_t)r;
+  return y;
+}
+
 struct AllocScale {
   uint64_t mk;
   int ek;
@@ -339,9 +376,8 @@ __device__ __forceinline__ AllocScale alloc_scale(uint64_t S) {
     ke = 24 - E - 104;
   } else {
     // q = floor(2^116 / m) in (2^63, 2^64); drop 11 bits with round-to-nearest-even
-    const unsigned __int128 num = (unsigned __int128)1 << 116;
-    const uint64_t q = (uint64_t)(num / m);
-    const uint64_t r = (uint64_t)(num - (unsigned __int128)q * m);
+    uint64_t r;
+    const uint64_t q = div_2p116(m, &r);
     t = q >> 11;
     const uint32_t d = (uint32_t)(q & 2047u);
     if (d > 1024u || (d == 1024u && (r != 0ull || (t & 1ull)))) ++t;
