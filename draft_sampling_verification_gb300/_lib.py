@@ -47,6 +47,8 @@ SIGNATURES = {
     "dspark_debug_philox": [_P, _U64, _I64, _P, _P],
     "dspark_debug_alloc_scale": [_P, _I64, _P, _P, _P, _P, _P],
     "dspark_debug_wait": [_I32, _P, _U32, _P, _P],
+    "dspark_checked_status": [_P],
+    "dspark_debug_check_selftest": [_P],
 }
 
 _lock = threading.Lock()

@@ -21,6 +21,10 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libdspark.so")
+# the bounds-checked build (DSPARK_CHECKED): every checked index site tests
+# its bound and counts failures (dspark_checked_status); for tests only
+OUT_CHECKED = os.path.join(PKG, "_build_checked")
+LIB_CHECKED = os.path.join(OUT_CHECKED, "libdspark_checked.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,
@@ -39,8 +43,11 @@ def _newest(paths):
     return max((os.path.getmtime(p) for p in paths), default=0.0)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    os.makedirs(OUT, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
+          checked: bool = False) -> str:
+    out_dir, lib = (OUT_CHECKED, LIB_CHECKED) if checked else (OUT, LIB)
+    extra = ["-DDSPARK_CHECKED"] if checked else []
+    os.makedirs(out_dir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     headers = glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))
     newest_header = _newest(headers)
@@ -48,11 +55,11 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     jobs = []
     objs = []
     for s in srcs:
-        o = os.path.join(OUT, os.path.basename(s)[:-3] + ".o")
+        o = os.path.join(out_dir, os.path.basename(s)[:-3] + ".o")
         objs.append(o)
         if force or not os.path.exists(o) or os.path.getmtime(o) < max(os.path.getmtime(s),
                                                                          newest_header):
-            cmd = [exe] + NVCC_FLAGS + (["-Xptxas", "-v"] if ptxas_info else []) + \
+            cmd = [exe] + NVCC_FLAGS + extra + (["-Xptxas", "-v"] if ptxas_info else []) + \
                   ["-c", s, "-o", o]
             jobs.append(cmd)
 
@@ -67,16 +74,17 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
                     sys.stderr.write(r.stdout + r.stderr)
                 if r.returncode != 0:
                     raise RuntimeError("nvcc failed: " + " ".join(cmd))
-    if force or jobs or not os.path.exists(LIB) or os.path.getmtime(LIB) < _newest(objs):
-        tmp = LIB + ".%d.tmp" % os.getpid()
+    if force or jobs or not os.path.exists(lib) or os.path.getmtime(lib) < _newest(objs):
+        tmp = lib + ".%d.tmp" % os.getpid()
         cmd = [exe] + ARCH + ["-shared", "-o", tmp] + objs
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             sys.stderr.write(r.stdout + r.stderr)
             raise RuntimeError("nvcc link failed")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv,
+                checked="--checked" in sys.argv))

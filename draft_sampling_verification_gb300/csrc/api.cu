@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include "dspark.h"
+#include "dspark_debug.h"
 
 namespace dspark {
 cudaError_t launch_q_topk(const void* x, int dtype, int64_t ld, int n_rows, int V,
@@ -65,6 +66,17 @@ cudaError_t launch_spec_step(const void* xd, int d_dtype, int64_t ld_d, const vo
 cudaError_t launch_target_probs(const void* z, int dtype, int64_t ld, int n_rows, int V,
                                 float* p_out, int32_t* argmax, int32_t* status,
                                 cudaStream_t stream);
+#ifdef DSPARK_CHECKED
+cudaError_t dspark_check_collect_chain(uint32_t* out);
+cudaError_t dspark_check_collect_debug(uint32_t* out);
+cudaError_t dspark_check_collect_q_dense(uint32_t* out);
+cudaError_t dspark_check_collect_q_topk(uint32_t* out);
+cudaError_t dspark_check_collect_q_wire(uint32_t* out);
+cudaError_t dspark_check_collect_sample(uint32_t* out);
+cudaError_t dspark_check_collect_spec(uint32_t* out);
+cudaError_t dspark_check_collect_tp(uint32_t* out);
+cudaError_t dspark_check_collect_verify(uint32_t* out);
+#endif
 }  // namespace dspark
 
 namespace {
@@ -103,6 +115,27 @@ int launch_result(cudaError_t e) { return e == cudaSuccess ? 0 : (int)e; }
 extern "C" {
 
 const char* dspark_version(void) { return "dspark-gb300 0.1 (" DSPARK_QSEM ", sm_103a)"; }
+
+int dspark_checked_status(uint32_t* out) {
+  if (!out) return DSPARK_ERR_NULL;
+  out[0] = out[1] = 0u;
+#ifdef DSPARK_CHECKED
+  out[2] = 1u;
+  cudaError_t e = cudaSuccess;
+  cudaError_t (*collect[])(uint32_t*) = {
+      dspark::dspark_check_collect_chain, dspark::dspark_check_collect_debug,
+      dspark::dspark_check_collect_q_dense, dspark::dspark_check_collect_q_topk,
+      dspark::dspark_check_collect_q_wire, dspark::dspark_check_collect_sample,
+      dspark::dspark_check_collect_spec, dspark::dspark_check_collect_tp,
+      dspark::dspark_check_collect_verify};
+  for (auto fn : collect)
+    if (e == cudaSuccess) e = fn(out);
+  return e == cudaSuccess ? 0 : (int)e;
+#else
+  out[2] = 0u;
+  return 0;
+#endif
+}
 
 int dspark_q_build(const void* draft_logits, int32_t dtype, int64_t ld, int32_t n_rows, int32_t V,
                    const float* temperature, int32_t top_k, uint32_t* counts, int32_t* sparse_ids,

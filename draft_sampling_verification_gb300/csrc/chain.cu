@@ -12,6 +12,7 @@
 // token goes to every CTA through distributed shared memory and conditions
 // row j + 1; the next row's base part is prefetched into L2 meanwhile.  A
 // refused row refuses the rest of its chain with the same status.
+#define DSPARK_TU 1  // this file's number in the checked build's site codes
 #include <cfloat>
 
 #include "q_dense.cuh"
@@ -139,5 +140,7 @@ cudaError_t launch_q_chain(const void* x, int dtype, int64_t ld, int B, int dept
   q_chain_kernel<<<B * kCl, kThr, smem, stream>>>(qp, cp);
   return cudaGetLastError();
 }
+
+DSPARK_CHECK_COLLECTOR(chain)
 
 }  // namespace dspark

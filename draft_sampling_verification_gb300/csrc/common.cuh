@@ -18,6 +18,49 @@ namespace dspark {
 
 constexpr uint32_t kM = DSPARK_M;
 
+// ------------------------------------------------- bounds-checked build
+// In the checked build of the library (compiled with DSPARK_CHECKED), every
+// DSPARK_CHECK(cond) site tests an index against its bound before the access
+// it guards; a failing site skips the access (a load yields a neutral value)
+// and is recorded in this translation unit's counters: the number of
+// failures and the first failing site (source line + 10000 * DSPARK_TU, the
+// file's number).  dspark_checked_status reads and clears them.  No trap, no
+// assert.  In the normal build the macro is the constant true: the condition
+// is not even evaluated.
+#ifndef DSPARK_TU
+#define DSPARK_TU 0
+#endif
+#ifdef DSPARK_CHECKED
+static __device__ uint32_t g_check_fail;
+static __device__ uint32_t g_check_site;
+__device__ __forceinline__ bool check_ok(bool ok, uint32_t site) {
+  if (!ok) {
+    atomicAdd(&g_check_fail, 1u);
+    atomicCAS(&g_check_site, 0u, site);
+  }
+  return ok;
+}
+#define DSPARK_CHECK(cond) (::dspark::check_ok((cond), (uint32_t)(__LINE__ + 10000 * DSPARK_TU)))
+// this translation unit's counters added into out[0] (failures) and out[1]
+// (first site, if none yet), then cleared (host; synchronises the device)
+static inline cudaError_t check_collect(uint32_t* out) {
+  uint32_t v[2] = {0u, 0u};
+  cudaError_t e = cudaMemcpyFromSymbol(&v[0], g_check_fail, 4);
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&v[1], g_check_site, 4);
+  const uint32_t zero = 0u;
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_check_fail, &zero, 4);
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_check_site, &zero, 4);
+  out[0] += v[0];
+  if (out[1] == 0u) out[1] = v[1];
+  return e;
+}
+#define DSPARK_CHECK_COLLECTOR(name) \
+  cudaError_t dspark_check_collect_##name(uint32_t* out) { return ::dspark::check_collect(out); }
+#else
+#define DSPARK_CHECK(cond) true
+#define DSPARK_CHECK_COLLECTOR(name)
+#endif
+
 // ---------------------------------------------------------------- Philox
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as
 // easy as 1, 2, 3", SC'11): ten rounds of two 32x32->64 multiplies of

@@ -1,5 +1,6 @@
 // debug.cu -- element-wise access to exp_ds / the integer weights and to
 // Philox4x32-10 (include/dspark_debug.h).
+#define DSPARK_TU 2  // this file's number in the checked build's site codes
 #include "common.cuh"
 #include "dspark_debug.h"
 
@@ -22,6 +23,12 @@ __global__ void exp_weights_kernel(const float* d, int64_t n, float* e_out, uint
       E_out[i] = same ? __float2ull_rz(w1) : ~0ull;
     }
   }
+}
+
+// one failing checked site (a comparison that is false for the one thread),
+// guarding no access: the checked build's counters must record it
+__global__ void check_selftest_kernel(int never) {
+  if (!DSPARK_CHECK(threadIdx.x == (unsigned)never)) return;
 }
 
 __global__ void alloc_scale_kernel(const uint64_t* S, int64_t n, uint64_t* mk, int32_t* ek,
@@ -67,6 +74,12 @@ int grid_for(int64_t n) {
 }  // namespace
 
 extern "C" {
+
+int dspark_debug_check_selftest(void* stream) {
+  check_selftest_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(-1);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? 0 : (int)e;
+}
 
 int dspark_debug_exp_weights(const float* d, int64_t n, float* e_out, uint64_t* E_out,
                              void* stream) {
@@ -122,3 +135,7 @@ int dspark_debug_wait(int32_t which, const uint32_t* count, uint32_t target, int
 }
 
 }  // extern "C"
+
+namespace dspark {
+DSPARK_CHECK_COLLECTOR(debug)
+}  // namespace dspark

@@ -43,6 +43,7 @@
 // copies then read L2.  (A persistent grid of G clusters taking rows
 // r, r + G, ... measured 15% slower: fixed placements keep the slow CTAs
 // slow, where fresh clusters rebalance.)
+#define DSPARK_TU 3  // this file's number in the checked build's site codes
 #include <mutex>
 
 #include "q_dense.cuh"
@@ -130,5 +131,7 @@ cudaError_t launch_q_dense(const void* x, int dtype, int64_t ld, int n_rows, int
   q_dense_kernel<<<n_rows * kCl, kThr, smem, stream>>>(p, q_dense_wave(smem));
   return cudaGetLastError();
 }
+
+DSPARK_CHECK_COLLECTOR(q_dense)
 
 }  // namespace dspark

@@ -179,7 +179,7 @@ __device__ __noinline__ uint32_t exact_word(float Ef, uint64_t mk, int ek, DShar
   const int sh11 = a.t - 11;
   const uint32_t b = (!pos || sh11 >= 64) ? 0u : (uint32_t)(a.rnum >> sh11);
   *F += a.f;
-  if (pos) atomicAdd(&sh.hist[b], 1u);
+  if (pos && DSPARK_CHECK(b < (uint32_t)kBins)) atomicAdd(&sh.hist[b], 1u);
   const uint32_t low = (pos ? kPos : 0u) | b;
   if (a.f < kFMax) return (a.f << 13) | low;
   const uint32_t q = atomicAdd(&sh.n_esc, 1u);
@@ -357,7 +357,9 @@ __device__ void select_cluster(cg::cluster_group& cluster, DShared& sh, int nbin
       uint32_t g = 0;
       if (i < per)
 #pragma unroll
-        for (int r = 0; r < kCl; ++r) g += cluster.map_shared_rank(&sh.hist[0], r)[sb * per + i];
+        for (int r = 0; r < kCl; ++r)
+          if (DSPARK_CHECK(sb * per + i < nbins))
+            g += cluster.map_shared_rank(&sh.hist[0], r)[sb * per + i];
       sh.gfi[i] = g;
     }
     __syncwarp();
@@ -440,6 +442,9 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
   const int ngroups = (off + n + 3) >> 2;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint32_t* crow = p.counts + (int64_t)row * V;
+  const int slice_cap = p.chunk + 4;  // floats of the slice buffer
+  // this CTA's count position s of the row (checked build: inside [lo, hi))
+  auto in_row = [&](int s) -> bool { return DSPARK_CHECK(lo - off + s >= lo && lo - off + s < hi); };
 
   // ---- temperature, barriers, slice
   const bool use_tma_dtype = (p.dtype == DSPARK_F32);
@@ -488,15 +493,17 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
       const int g = (tid < 4) ? 0 : ngroups - 1;
       if (g >= 0 && !(n_int > 0 && g >= g_first && g <= g_last)) {
         const int s = 4 * g + (tid & 3);
-        sl[s] = (s >= off && s < off + n) ? __ldg(xbase + s) : -INFINITY;
+        if (DSPARK_CHECK(s < slice_cap))
+          sl[s] = (s >= off && s < off + n) ? __ldg(xbase + s) : -INFINITY;
       }
     }
   } else {
     for (int g = tid; g < ngroups; g += kThr)
       for (int i = 0; i < 4; ++i) {
         const int s = 4 * g + i;
-        sl[s] = (s >= off && s < off + n) ? load_logit(xrow, p.dtype, (int64_t)(lo - off + s))
-                                          : -INFINITY;
+        if (DSPARK_CHECK(s < slice_cap))
+          sl[s] = (s >= off && s < off + n) ? load_logit(xrow, p.dtype, (int64_t)(lo - off + s))
+                                            : -INFINITY;
       }
   }
   __syncthreads();
@@ -642,12 +649,12 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
   if (sh.status != DSPARK_ST_OK) {
     const int st = sh.status;
     for (int v = lo + tid; v < hi; v += kThr) crow[v] = 0u;
-    if (rank == 0 && tid == 0) {
+    if (rank == 0 && tid == 0 && DSPARK_CHECK(row < p.n_rows)) {
       p.status[row] = st;
       if (p.tokens) p.tokens[row] = -1;
     }
     cluster.sync();  // peers may still read this CTA's pub
-    if (ready && rank == 0 && tid == 0) {
+    if (ready && rank == 0 && tid == 0 && DSPARK_CHECK(row / p.depth < (p.n_rows + p.depth - 1) / p.depth)) {
       __threadfence();
       atomicAdd(&ready[row / p.depth], 1u);
     }
@@ -734,12 +741,12 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
   if (sh.status != DSPARK_ST_OK) {
     const int st = sh.status;
     for (int v = lo + tid; v < hi; v += kThr) crow[v] = 0u;
-    if (rank == 0 && tid == 0) {
+    if (rank == 0 && tid == 0 && DSPARK_CHECK(row < p.n_rows)) {
       p.status[row] = st;
       if (p.tokens) p.tokens[row] = -1;
     }
     cluster.sync();
-    if (ready && rank == 0 && tid == 0) {
+    if (ready && rank == 0 && tid == 0 && DSPARK_CHECK(row / p.depth < (p.n_rows + p.depth - 1) / p.depth)) {
       __threadfence();
       atomicAdd(&ready[row / p.depth], 1u);
     }
@@ -768,7 +775,8 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
         any_open = any_open || !(fs.cert[l] || fs.zero[l]);
         // branch-free: the elements that do not count go to a dummy bin
         F += counted ? fs.f[l] : 0u;
-        atomicAdd(&sh.hist[counted ? fs.b[l] : kBins + (tid & 15)], 1u);
+        const uint32_t bin = counted ? fs.b[l] : kBins + (tid & 15);
+        if (DSPARK_CHECK(bin < (uint32_t)(kBins + 16))) atomicAdd(&sh.hist[bin], 1u);
       }
       gmask |= any_open ? (1u << it) : 0u;
       // a group with an open element keeps its four weights for the refinement
@@ -791,8 +799,9 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
       const FloatSplit2& fs = (i < 2) ? fa : fc;
       const int l = i & 1;
       const int s = 4 * g + i;
-      slu[s] = (fs.cert[l] || fs.zero[l]) ? fs.word[l]
-                                          : exact_word(ee[i], mk, ek, sh, s, &F, &internal);
+      if (DSPARK_CHECK(s < slice_cap))
+        slu[s] = (fs.cert[l] || fs.zero[l]) ? fs.word[l]
+                                            : exact_word(ee[i], mk, ek, sh, s, &F, &internal);
     }
   }
   F = warp_reduce(F, OpAddU32());
@@ -856,7 +865,9 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
         uint32_t g = 0;
         if (i < kFine)
 #pragma unroll
-          for (int r = 0; r < kCl; ++r) g += cluster.map_shared_rank(&sh.hist[0], r)[sb * kFine + i];
+          for (int r = 0; r < kCl; ++r)
+            if (DSPARK_CHECK(sb * kFine + i < kBins))
+              g += cluster.map_shared_rank(&sh.hist[0], r)[sb * kFine + i];
         sh.gfi[i] = g;
       }
       __syncwarp();
@@ -901,7 +912,7 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
       mmask |= (valid && xm == 0u) ? (1u << it) : 0u;
       const bool full = valid && g >= g_first && g <= g_last;  // all four inside the slice
       uint32_t gsum = 0;
-      if (full) {
+      if (full && in_row(4 * g) && in_row(4 * g + 3)) {
         gsum = c0 + c1 + c2 + c3;
         if (vec) {
           reinterpret_cast<uint4*>(cbase)[g] = make_uint4(c0, c1, c2, c3);
@@ -927,8 +938,8 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
         // an escape is stored by the correction below, which expects esc_c here
         const uint32_t w = slu[s];
         const uint32_t c = (w + carry_k) >> 13;
-        if (w != kEsc) cbase[s] = c;
-        atomicAdd(&sh.bsum[g / 32], c);
+        if (w != kEsc && in_row(s)) cbase[s] = c;
+        if (DSPARK_CHECK(g / 32 < kBlkCap)) atomicAdd(&sh.bsum[g / 32], c);
       }
     }
     // escapes: the right count, and the block sum corrected
@@ -937,8 +948,8 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
       if (s < off || s >= off + n) continue;
       const uint32_t low = sh.esc[j].low;
       const uint32_t c = sh.esc[j].f + ((low > thr) ? 1u : 0u);
-      cbase[s] = c;
-      atomicAdd(&sh.bsum[(s >> 2) >> 5], c - esc_c);
+      if (in_row(s)) cbase[s] = c;
+      if (DSPARK_CHECK(((s >> 2) >> 5) < kBlkCap)) atomicAdd(&sh.bsum[(s >> 2) >> 5], c - esc_c);
       if (low == thr) {
         const uint32_t q = atomicAdd(&sh.n_cand, 1u);
         if (q < (uint32_t)kCandCap) {
@@ -966,7 +977,8 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
   if (warp == 0 && status == DSPARK_ST_OK) {
     const int nblk = (ngroups + 31) / 32;
     uint32_t t = 0;
-    for (int k = lane; k < nblk; k += 32) t += sh.bsum[k];
+    for (int k = lane; k < nblk; k += 32)
+      if (DSPARK_CHECK(k < kBlkCap)) t += sh.bsum[k];
     t = __reduce_add_sync(0xffffffffu, t);
     if (lane == 0) sh.wred32[0] = t;
   }
@@ -981,6 +993,7 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
   // the logit of slice position s again (the slice holds other values by
   // now); a chain row's is z = RN(x + bias)
   auto x_at = [&](int s) -> float {
+    if (!in_row(s)) return 0.0f;
     const float x = load_logit(xrow, p.dtype, (int64_t)(lo - off + s));
     return zbias ? __fadd_rn(x, __ldg(zbias + (lo - off + s))) : x;
   };
@@ -1002,7 +1015,7 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
       nc = sh.push.ncand[lane];
       sh.peers_csum[lane] = cs;
       sh.peers_ncand[lane] = nc;
-      sh.grants[lane] = 0u;
+      sh.grants[lane] = 0u;  // lane < kCl
       over = nc > (uint32_t)kCandCap ? 1u : 0u;
     }
     over = warp_reduce(over, OpOrU32());
@@ -1030,8 +1043,8 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
       slu[s] = w | kGrant;
       f = w >> 13;
     }
-    crow[lo - off + s] = f + 1u;
-    atomicAdd(&sh.bsum[(s >> 2) >> 5], 1u);
+    if (in_row(s)) crow[lo - off + s] = f + 1u;
+    if (DSPARK_CHECK(((s >> 2) >> 5) < kBlkCap)) atomicAdd(&sh.bsum[(s >> 2) >> 5], 1u);
   };
 
   if (R > 0 && fits && Rin > 0) {
@@ -1045,6 +1058,7 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
         base += sh.peers_ncand[r];
         ++r;
       }
+      if (!DSPARK_CHECK((t - base) < (uint32_t)kCandCap && t < kAllCap)) continue;
       const Cand* src = cluster.map_shared_rank(&sh.cand[0], r) + (t - base);
       Cand e;
       e.key = src->key;
@@ -1073,7 +1087,7 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
       for (int o = tpm >> 1; o > 0; o >>= 1) before += __shfl_xor_sync(0xffffffffu, before, o);
       if (i < (int)total && part == 0 && before < Rin) {
         const int owner = vi / p.chunk;
-        atomicAdd(&sh.grants[owner], 1u);
+        if (DSPARK_CHECK(owner >= 0 && owner < kCl)) atomicAdd(&sh.grants[owner], 1u);
         if (owner == rank) grant_member(all[i].s);
       }
     }
@@ -1126,7 +1140,10 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
       const uint32_t incl = block_inclusive_scan(cnt, sh.wred32, &tot);
       uint32_t o = incl - cnt;
       for (int i = 0; i < kPer; ++i)
-        if ((bits >> i) & 1u) ms.list[o++] = (uint16_t)(p0 + i);
+        if ((bits >> i) & 1u) {
+          if (DSPARK_CHECK(o < (uint32_t)kWin)) ms.list[o] = (uint16_t)(p0 + i);
+          ++o;
+        }
       __syncthreads();
       // four rounds of members at a time: their logits are reloaded together
       for (uint32_t j4 = 0; j4 < tot; j4 += 4 * kThr) {
@@ -1217,6 +1234,7 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
         const uint32_t c = *cluster.map_shared_rank(&ms.tcnt[slot], r);
         if (c == 0u) continue;
         const uint32_t q = atomicAdd(&sh.n_merged, 1u);
+        if (!DSPARK_CHECK(q < (uint32_t)(kCl * kTab))) continue;
         ms.merged.key[q] = *cluster.map_shared_rank(&ms.tkey[slot], r);
         ms.merged.cnt[q] = c;
       }
@@ -1261,7 +1279,8 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
           set_low(sp, thr);
         }
         const unsigned at = __ballot_sync(0xffffffffu, stt == 2);
-        if (lane == 0) atm[(s0 - a0) >> 5] = at;
+        if (lane == 0 && DSPARK_CHECK(warp * kAtSteps + ((s0 - a0) >> 5) < kWarps * kAtSteps))
+          atm[(s0 - a0) >> 5] = at;
         wat += (uint32_t)__popc(at);
       }
       if (lane == 0) sh.wcnt[warp] = wat;
@@ -1372,7 +1391,7 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
   __syncthreads();  // member counts are written before any zeroing below
   if (status != DSPARK_ST_OK)
     for (int v = lo + tid; v < hi; v += kThr) crow[v] = 0u;
-  if (rank == 0 && tid == 0) {
+  if (rank == 0 && tid == 0 && DSPARK_CHECK(row < p.n_rows)) {
     p.status[row] = status;
     if (p.tokens && status != DSPARK_ST_OK) p.tokens[row] = -1;
   }
@@ -1416,7 +1435,7 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
         uint32_t gs = 0;
         if (g < ngroups)
           for (int i = 0; i < 4; ++i) {
-            cv[i] = count_of(sh, slu, 4 * g + i, thr);
+            cv[i] = DSPARK_CHECK(4 * g + i < slice_cap) ? count_of(sh, slu, 4 * g + i, thr) : 0u;
             gs += cv[i];
           }
         uint32_t incl = gs;
@@ -1441,13 +1460,13 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
         if (msk) token = __shfl_sync(0xffffffffu, token, __ffs(msk) - 1);
       }
       if (lane == 0) {
-        p.tokens[row] = token;
+        if (DSPARK_CHECK(row < p.n_rows)) p.tokens[row] = token;
         signal = ready != nullptr;
       }
     }
   }
   cluster.barrier_wait();  // no CTA leaves while a peer may still read its shared memory
-  if (signal) {
+  if (signal && DSPARK_CHECK(row / p.depth < (p.n_rows + p.depth - 1) / p.depth)) {
     // every CTA's counts were written before its arrive, the token before
     // this point: make them visible device-wide, then count the row done
     __threadfence();

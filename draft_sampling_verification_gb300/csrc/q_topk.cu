@@ -33,6 +33,7 @@
 // The allocation then runs on the at most k survivors (support_alloc.cuh):
 // FP64 as the method states it, the nonzero counts in ascending id order,
 // and the draft draw on them.
+#define DSPARK_TU 4  // this file's number in the checked build's site codes
 #include "support_alloc.cuh"
 
 namespace dspark {
@@ -457,6 +458,7 @@ __global__ void __launch_bounds__(kKThr, 3) q_topk_kernel(KParams p) {
     float thr0 = -INFINITY;  // candidates: y > thr0
     if (nb > kKSample) {
       const int seg = h0 + (((tid >> 2) * (nb / 64)) & ~7) + (tid & 3) * 8;
+      (void)DSPARK_CHECK(seg >= h0 && seg + 8 <= h0 + nb);
       float sx[8], sy[8];
       if (f32) {
         const float4* g4 = reinterpret_cast<const float4*>(xrow + (int64_t)seg * 4);
@@ -628,5 +630,7 @@ cudaError_t launch_q_topk(const void* x, int dtype, int64_t ld, int n_rows, int 
   q_topk_kernel<<<n_rows, kKThr, smem, stream>>>(p);
   return cudaGetLastError();
 }
+
+DSPARK_CHECK_COLLECTOR(q_topk)
 
 }  // namespace dspark

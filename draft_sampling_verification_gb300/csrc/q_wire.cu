@@ -16,6 +16,7 @@
 //
 // One CTA of 256 threads per row.  Dense rows whose start is 16-byte aligned
 // move 4 elements per 128-bit access; other rows one element per access.
+#define DSPARK_TU 5  // this file's number in the checked build's site codes
 #include "common.cuh"
 
 namespace dspark {
@@ -264,5 +265,7 @@ cudaError_t launch_q_validate(const float* q, const int32_t* ids, const int32_t*
   q_validate_kernel<<<n_rows, kWThr, 0, stream>>>(p);
   return cudaGetLastError();
 }
+
+DSPARK_CHECK_COLLECTOR(q_wire)
 
 }  // namespace dspark

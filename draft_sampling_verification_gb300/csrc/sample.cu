@@ -8,6 +8,7 @@
 // the segment holding D, and that warp scans its segment in id order.
 // Sparse rows (<= 1024 entries) are checked for canonical form and scanned
 // by one warp.
+#define DSPARK_TU 6  // this file's number in the checked build's site codes
 #include "common.cuh"
 
 namespace dspark {
@@ -113,7 +114,8 @@ __global__ void __launch_bounds__(kSThreads) draft_sample_kernel(SParams p) {
           if ((uint64_t)D < base + tile) {
             const bool hit = (base + incl > (uint64_t)D) && (base + incl - c <= (uint64_t)D);
             const unsigned m = __ballot_sync(0xffffffffu, hit && c > 0u);
-            if (lane == 0 && m) result = ids[i0 + __ffs(m) - 1];
+            if (lane == 0 && m && DSPARK_CHECK(i0 + __ffs(m) - 1 < nz))
+              result = ids[i0 + __ffs(m) - 1];
             break;
           }
           base += tile;
@@ -148,5 +150,7 @@ cudaError_t launch_draft_sample(const uint32_t* counts, const int32_t* ids, cons
   draft_sample_kernel<<<B * depth, kSThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
+
+DSPARK_CHECK_COLLECTOR(sample)
 
 }  // namespace dspark

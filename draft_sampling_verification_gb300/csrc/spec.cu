@@ -18,6 +18,7 @@
 //               finished row increments the request's counter in the
 //               workspace; the verifying cluster waits on it with a bounded
 //               wait).  It pays off only while all items fit in one wave.
+#define DSPARK_TU 7  // this file's number in the checked build's site codes
 #include <mutex>
 
 #include "q_dense.cuh"
@@ -108,6 +109,8 @@ __global__ void __cluster_dims__(qdense::kCl, 1, 1) __launch_bounds__(qdense::kT
     bool is_v;
     int idx;
     decode_item(k, wp, &is_v, &idx);
+    if (!DSPARK_CHECK(is_v ? (idx >= 0 && idx < wp.B) : (idx >= 0 && idx < wp.B * wp.depth)))
+      continue;
     if (!is_v) {
       q_row(qp, idx, sh.q, reinterpret_cast<float*>(dyn), mbar, phase, wp.ready);
       continue;
@@ -301,5 +304,7 @@ uint32_t* static_spec_workspace() {
   }
   return addr[dev];
 }
+
+DSPARK_CHECK_COLLECTOR(spec)
 
 }  // namespace dspark

@@ -143,8 +143,10 @@ __device__ void support_alloc_emit(int st, int ns, int k, const uint32_t* keys,
         pos += pre;
         before += pre ? o.y : 0u;
       }
-      ids_out[pos] = (int32_t)idi;
-      cnt_out[pos] = c;
+      if (DSPARK_CHECK(pos < (uint32_t)k)) {
+        ids_out[pos] = (int32_t)idi;
+        cnt_out[pos] = c;
+      }
       if (before <= D && D - before < c) sh.found = (int32_t)idi;
     }
     nnz = block_reduce(nnz, OpAddU32(), sh.red32);

@@ -35,6 +35,7 @@
 // global top k is a subset of the union of the local ones) and allocates the
 // tickets on that support.  The leader's draw over the support in id order is
 // the draw that picks the shard by its count total, then the token inside.
+#define DSPARK_TU 8  // this file's number in the checked build's site codes
 #include "support_alloc.cuh"
 
 namespace dspark {
@@ -799,5 +800,7 @@ cudaError_t launch_q_sharded(const void* x, int dtype, int64_t ld, int B, int de
   if (tokens) tp_draw_kernel<<<units, kTpThr, 0, stream>>>(p);
   return cudaGetLastError();
 }
+
+DSPARK_CHECK_COLLECTOR(tp)
 
 }  // namespace dspark

@@ -13,6 +13,7 @@
 // in every CTA), and the request stops at the deciding row, so rows after
 // the first rejection are never read.  The correction / bonus draw re-reads
 // row L (an L2 hit) and scans exact 46-bit fixed-point residual weights.
+#define DSPARK_TU 9  // this file's number in the checked build's site codes
 #include "verify.cuh"
 
 namespace dspark {
@@ -389,5 +390,7 @@ cudaError_t launch_target_probs(const void* z, int dtype, int64_t ld, int n_rows
   target_probs_kernel<<<n_rows * kVCluster, kVThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
+
+DSPARK_CHECK_COLLECTOR(verify)
 
 }  // namespace dspark

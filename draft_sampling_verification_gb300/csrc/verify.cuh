@@ -205,12 +205,20 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
   int writer = -1;
   bool drawn = false;
 
+  // the slice buffer holds chunk elements plus one 16-byte group of slack
+  const int slice_groups = (p.chunk * ESZ + 32) / 16;
   auto val = [&](int s) -> float {
+    if (!DSPARK_CHECK(s >= 0 && s < slice_groups * EPG)) return -INFINITY;
     if (kDt == DSPARK_F32) return vf[s];
     return __uint_as_float(((uint32_t)vh[s]) << 16);
   };
   // the EPG values of group g
   auto group = [&](int g, float* z) {
+    if (!DSPARK_CHECK(g >= 0 && g < slice_groups)) {
+#pragma unroll
+      for (int i = 0; i < EPG; ++i) z[i] = -INFINITY;
+      return;
+    }
     if (kDt == DSPARK_F32) {
       const float4 q = reinterpret_cast<const float4*>(vbuf)[g];
       z[0] = q.x;
@@ -282,7 +290,8 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
       const int64_t qr = (int64_t)b * depth + j;
       if (p.top_k == 0) {
         qrow = p.counts + qr * V;
-        if (tid == 0) cx = cnt_sm ? cnt_sm[j] : ldq<kCohQ>(qrow + x);
+        if (tid == 0 && DSPARK_CHECK(x >= 0 && x < V))
+          cx = cnt_sm ? cnt_sm[j] : ldq<kCohQ>(qrow + x);
       } else {
         // canonical sparse row: 1 <= nnz <= top_k, ids strictly ascending in
         // [0, V), counts > 0, total M
@@ -299,6 +308,7 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
           if (tid == 0) sh.q_ok = 0;
         } else {
           for (int i = tid; i < nz; i += kVThreads) {
+            if (!DSPARK_CHECK(i < p.top_k)) break;
             const int id = ids[i];
             const uint32_t cc = cn[i];
             if (id < 0 || id >= V || cc == 0u || (i > 0 && ids[i - 1] >= id)) sh.q_ok = 0;
@@ -315,7 +325,7 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
         snnz = nz;
       }
       if (tid == 0) {
-        zx = load_logit(zrow, kDt, x);
+        zx = DSPARK_CHECK(x >= 0 && x < V) ? load_logit(zrow, kDt, x) : -INFINITY;
         U = draw_u32(p.seed, req, (uint32_t)j, DSPARK_PURPOSE_ACCEPT) >> 8;
       }
     }
@@ -596,6 +606,7 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
           const float pr = pv(val(s));
           const float r = fmaxf(__fsub_rn(pr, (float)ldq<kCohQ>(scnt + i) * 0x1p-24f), 0.0f);
           const uint64_t d = wfix(pr) - wfix(r);
+          if (!DSPARK_CHECK((s / EPG) / 32 < kVMaxBlocks)) continue;
           atomicAdd(reinterpret_cast<unsigned long long*>(&sh.bsum[(s / EPG) / 32]),
                     (unsigned long long)(0ull - d));
           zs -= d;
@@ -667,7 +678,7 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
           int blk = -1;
           for (int k0 = 0; k0 < nblk && blk < 0; k0 += 32) {
             const int k = k0 + lane;
-            const uint64_t v = (k < nblk) ? sh.bsum[k] : 0ull;
+            const uint64_t v = (k < nblk && DSPARK_CHECK(k < kVMaxBlocks)) ? sh.bsum[k] : 0ull;
             uint64_t incl = v;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -794,7 +805,7 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
 
   // outputs: greedy and ratio refusals by rank 0; after a ratio draw, by the
   // CTA that found the token
-  if (kG && rank == 0 && tid == 0) {
+  if (kG && rank == 0 && tid == 0 && DSPARK_CHECK(b < p.B && L_g <= depth)) {
     int32_t* com = p.g_committed + (int64_t)b * (depth + 1);
     if (st_g != DSPARK_ST_OK) {
       p.g_accept_len[b] = 0;
@@ -808,7 +819,7 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
     p.g_status[b] = st_g;
   }
   const bool i_write = drawn ? (writer == rank) : (rank == 0);
-  if (kD && i_write && tid == 0) {
+  if (kD && i_write && tid == 0 && DSPARK_CHECK(b < p.B && L <= depth)) {
     int32_t* com = p.r_committed + (int64_t)b * (depth + 1);
     if (st_r != DSPARK_ST_OK) {
       p.r_accept_len[b] = 0;

@@ -64,6 +64,29 @@ int dspark_debug_philox(const uint32_t* ctr, uint64_t seed, int64_t n, uint32_t*
 int dspark_debug_wait(int32_t which, const uint32_t* count, uint32_t target, int32_t* status,
                       void* stream);
 
+/*
+ * dspark_checked_status -- the record of the bounds-checked build.  The
+ * library can be built with DSPARK_CHECKED (libdspark_checked.so): every
+ * index into a fixed-capacity shared-memory array, every index that comes
+ * from data (token ids, sparse ids, histogram bins, table slots, slots taken
+ * with an atomic counter) and every output row / element offset is tested
+ * against its bound before the access; a failing test skips the access (a
+ * load yields a neutral value) and is counted -- no trap, no assert.  This
+ * call (host; it synchronises the device) sets out[0] = the failures since
+ * the last call, out[1] = the first failing site (source line + 10000 * the
+ * source file's number), out[2] = 1 in the checked build and 0 in the normal
+ * one (whose out[0], out[1] are 0), and clears the counters.  out is a host
+ * array of 3 words.  Returns 0, DSPARK_ERR_NULL, or a CUDA error (> 0).
+ */
+int dspark_checked_status(uint32_t* out);
+
+/*
+ * One kernel of one thread whose single checked site fails (it guards no
+ * access): in the checked build the next dspark_checked_status reports one
+ * failure at that site; in the normal build it does nothing.
+ */
+int dspark_debug_check_selftest(void* stream);
+
 #ifdef __cplusplus
 }
 #endif
