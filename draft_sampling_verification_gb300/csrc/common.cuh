@@ -509,6 +509,15 @@ __device__ __forceinline__ uint32_t warp_reduce(uint32_t v, OpAddU32) {
 __device__ __forceinline__ uint32_t warp_reduce(uint32_t v, OpOrU32) {
   return __reduce_or_sync(0xffffffffu, v);
 }
+// 64-bit sums over a full warp by three 32-bit warp reductions of 24-, 24-
+// and 16-bit pieces (each sum stays below 2^29): exact for any total below
+// 2^64, and measured far faster than shuffling 64-bit values five times.
+__device__ __forceinline__ uint64_t warp_reduce(uint64_t v, OpAddU64) {
+  const uint32_t a = __reduce_add_sync(0xffffffffu, (uint32_t)v & 0xFFFFFFu);
+  const uint32_t b = __reduce_add_sync(0xffffffffu, (uint32_t)(v >> 24) & 0xFFFFFFu);
+  const uint32_t c = __reduce_add_sync(0xffffffffu, (uint32_t)(v >> 48));
+  return (uint64_t)a + ((uint64_t)b << 24) + ((uint64_t)c << 48);
+}
 
 // Inclusive scan over the block for one uint32 per thread; returns the
 // inclusive prefix, *total gets the block total.  scratch >= 32 words.

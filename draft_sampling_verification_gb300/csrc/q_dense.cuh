@@ -623,16 +623,17 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
     sh.top1 = c1;
     sh.top2 = c2;
   }
-  if (warp == 0) {
+  // the cluster's values by one lane straight from shared memory: warp
+  // shuffles and reductions queue behind the other CTAs' shared-memory
+  // traffic here, and these few lines hold the whole CTA
+  if (warp == 0 && lane == 0) {
     float mm = -INFINITY;
     uint32_t fl = 0;
-    if (lane < kCl) {
-      mm = sh.push.mx[lane];
-      fl = sh.push.fl1[lane];
+    for (int r = 0; r < kCl; ++r) {
+      mm = fmax_nan(mm, sh.push.mx[r]);
+      fl |= sh.push.fl1[r];
     }
-    mm = warp_reduce(mm, OpMaxNaN());
-    fl = warp_reduce(fl, OpOrU32());
-    if (lane == 0) {
+    {
       int st = DSPARK_ST_OK;
       float m = mm;
       if (scale) m = __fmul_rn(mm, invT);
@@ -711,24 +712,26 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
   }
   __syncthreads();
   if (warp == 0) {
-    const uint64_t s2 = warp0_combine(sh.wred64, (uint64_t)0, OpAddU64());
-    const uint32_t o2 = warp0_combine(sh.wred32, 0u, OpOrU32());
+    uint64_t s2 = 0;
+    uint32_t o2 = 0;
+    for (int w = 0; w < kWarps; ++w) {  // every lane, the same sums
+      s2 += sh.wred64[w];
+      o2 |= sh.wred32[w];
+    }
     if (lane < kCl) {
       *cluster.map_shared_rank(&sh.push.S[rank], lane) = s2;
       *cluster.map_shared_rank(&sh.push.fl2[rank], lane) = o2;
     }
   }
   cluster.sync();  // S2
-  if (warp == 0) {
+  if (warp == 0 && lane == 0) {
     uint64_t sv = 0;
     uint32_t fl = 0;
-    if (lane < kCl) {
-      sv = sh.push.S[lane];
-      fl = sh.push.fl2[lane];
+    for (int r = 0; r < kCl; ++r) {
+      sv += sh.push.S[r];
+      fl |= sh.push.fl2[r];
     }
-    sv = warp_reduce(sv, OpAddU64());
-    fl = warp_reduce(fl, OpOrU32());
-    if (lane == 0) {
+    {
       const AllocScale ks = alloc_scale(sv);  // sv >= 2^40: the max has weight 2^40
       sh.mk = ks.mk;
       sh.ek = ks.ek;

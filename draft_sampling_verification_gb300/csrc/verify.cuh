@@ -404,43 +404,32 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
     }
     cluster.sync();
     if (warp == 0) {
-      // every CTA's partials, from local memory (lane r holds rank r), then
-      // merged in rank order by every lane (identical in every CTA)
-      float pm = -INFINITY, ps = 0.0f, pav = -INFINITY;
-      int pai = 0x7FFFFFFF;
-      uint32_t pfl = 0;
-      if (lane < NC) {
-        const VX& e = sh.px[xi][lane];
-        pm = e.m;
-        ps = e.s;
-        pav = e.amv;
-        pai = e.ami;
-        pfl = e.fl;
-      }
-      // a tree over the NC lanes (lane 0 ends with the row's values, the same
-      // in every CTA): the flags, the max and the argmax (lowest id among the
-      // maxima) are exact; each slice's sum is rescaled to the row max in its
-      // own lane, and the rescaled sums are added pairwise
-      const bool bad = __any_sync(0xffffffffu, !(pm < INFINITY));  // NaN or +inf
-      float m = (pm < INFINITY) ? pm : -INFINITY;
-      uint32_t fl = pfl;
-      float av = pav;
-      int ai = pai;
+      // every CTA's partials, from local memory, merged by one lane in rank
+      // order (identical in every CTA): warp shuffles queue behind the other
+      // CTAs' shared-memory traffic here, and the whole cluster waits on
+      // this.  The flags, the max and the argmax (lowest id among the maxima)
+      // are exact; each slice's sum is rescaled to the row max and the
+      // rescaled sums are added in rank order.
+      bool bad = false;
+      float m = -INFINITY, s = 0.0f, av = -INFINITY;
+      int ai = 0x7FFFFFFF;
+      uint32_t fl = 0;
+      if (lane == 0) {
 #pragma unroll
-      for (int o = NC / 2; o > 0; o >>= 1) {
-        fl |= __shfl_xor_sync(0xffffffffu, fl, o);
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if (kG && need_g) {
-          const float av2 = __shfl_xor_sync(0xffffffffu, av, o);
-          const int ai2 = __shfl_xor_sync(0xffffffffu, ai, o);
-          am_merge(av, ai, av2, ai2);
+        for (int r = 0; r < NC; ++r) {
+          const VX& e = sh.px[xi][r];
+          bad = bad || !(e.m < INFINITY);  // NaN or +inf
+          if (e.m < INFINITY) m = fmaxf(m, e.m);
+          fl |= e.fl;
+          if (kG && need_g) am_merge(av, ai, e.amv, e.ami);
         }
-      }
-      float s = 0.0f;
-      if (kD && need_r) {
-        s = (pm > -INFINITY && pm < INFINITY && m > -INFINITY) ? ps * expf(pm - m) : 0.0f;
+        if (kD && need_r && m > -INFINITY) {
 #pragma unroll
-        for (int o = NC / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+          for (int r = 0; r < NC; ++r) {
+            const VX& e = sh.px[xi][r];
+            if (e.m > -INFINITY && e.m < INFINITY) s += e.s * expf(e.m - m);
+          }
+        }
       }
       if (lane == 0) {
         sh.M = bad ? NAN : m;
@@ -639,16 +628,16 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
       }
       cluster.sync();
       if (warp == 0) {
-        // every CTA's masses, from local memory (lane r holds rank r); exact sums
-        uint64_t zr = 0, cr = 0;
-        if (lane < NC) {
-          zr = sh.px[xi][lane].z;
-          cr = sh.px[xi][lane].cs;
-        }
-        const uint64_t before = warp_reduce(lane < rank ? zr : 0ull, OpAddU64());
-        const uint64_t Z = warp_reduce(zr, OpAddU64());
-        const uint64_t CS = warp_reduce(cr, OpAddU64());
+        // every CTA's masses, from local memory, summed exactly by one lane
         if (lane == 0) {
+          uint64_t before = 0, Z = 0, CS = 0;
+#pragma unroll
+          for (int r = 0; r < NC; ++r) {
+            const uint64_t zr = sh.px[xi][r].z;
+            if (r < rank) before += zr;
+            Z += zr;
+            CS += sh.px[xi][r].cs;
+          }
           sh.Z = Z;
           sh.before = before;
           sh.CS = CS;
