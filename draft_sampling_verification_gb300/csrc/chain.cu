@@ -8,9 +8,10 @@
 // the dense q build with its draft draw (the q_dense row code) runs on
 // z = RN(x + bias[prev mod n_bias]), formed in shared memory as each CTA's
 // eighth of the base row lands (the bias row is read alongside), and the
-// same pass keeps the row's two largest finite z for the margin.  The drawn
-// token goes to every CTA through distributed shared memory and conditions
-// row j + 1; the next row's base part is prefetched into L2 meanwhile.  A
+// same pass keeps the row's two largest z for the margin.  The CTA that
+// draws the token stores it into every CTA's shared memory before the row's
+// last cluster barrier, and it conditions row j + 1; the next row's base part
+// is prefetched into L2 meanwhile, its bias part when the row starts.  A
 // refused row refuses the rest of its chain with the same status.
 #define DSPARK_TU 1  // this file's number in the checked build's site codes
 #include <cfloat>
@@ -33,14 +34,10 @@ struct ChainParams {
   int V;
 };
 
-struct ChainShared {
-  int tok, st;  // pushed by rank 0: the row's token and status
-};
-
-__device__ __noinline__ void chain_q_row(const qdense::Params& qp, int row, qdense::DShared& sh,
-                                         float* sl, uint64_t* mbar, uint32_t& phase,
-                                         int next_row, const float* zbias) {
-  qdense::q_dense_row(qp, row, sh, sl, mbar, phase, nullptr, next_row, true, zbias);
+__device__ __noinline__ int chain_q_row(const qdense::Params& qp, int row, qdense::DShared& sh,
+                                        float* sl, uint64_t* mbar, uint32_t& phase,
+                                        int next_row, const float* zbias) {
+  return qdense::q_dense_row(qp, row, sh, sl, mbar, phase, nullptr, next_row, true, zbias);
 }
 
 __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThr, 3)
@@ -48,7 +45,6 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThr, 3)
   cg::cluster_group cluster = cg::this_cluster();
   __shared__ qdense::DShared sh;
   __shared__ uint64_t mbar[qdense::kTma];
-  __shared__ ChainShared cs;
   extern __shared__ __align__(128) float sl[];
   const int rank = (int)cluster.block_rank();
   const int tid = threadIdx.x;
@@ -76,33 +72,22 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThr, 3)
       continue;
     }
     const float* brow = cp.bias ? cp.bias + (int64_t)(prev % cp.n_bias) * cp.bias_ld : nullptr;
-    chain_q_row(qp, row, sh, sl, mbar, phase, (j + 1 < depth) ? row + 1 : -1, brow);
-
-    // ---- the drawn token (and status) to every CTA
-    __threadfence();
-    cluster.sync();
-    if (rank == 0 && tid == 0) {
-      const int tok = *reinterpret_cast<volatile const int32_t*>(qp.tokens + row);
-      const int st = *reinterpret_cast<volatile const int32_t*>(qp.status + row);
-      if (cp.margins) {
-        float mg = 0.0f;
-        if (st == DSPARK_ST_OK) {
-          const float m1 = sh.top1, m2 = sh.top2;
-          mg = (m2 == -INFINITY) ? FLT_MAX : __fsub_rn(m1, m2);
-          if (!(mg <= FLT_MAX)) mg = FLT_MAX;
-        }
-        cp.margins[row] = mg;
+    const int st = chain_q_row(qp, row, sh, sl, mbar, phase, (j + 1 < depth) ? row + 1 : -1, brow);
+    // the drawn token is in this CTA's shared memory (stored before the
+    // row's last cluster barrier), the status the same in every CTA
+    const int tok = sh.chain_tok;
+    if (cp.margins && rank == 0 && tid == 0) {
+      float mg = 0.0f;
+      if (st == DSPARK_ST_OK) {
+        const float m1 = sh.top1, m2 = sh.top2;
+        mg = (m2 == -INFINITY) ? FLT_MAX : __fsub_rn(m1, m2);
+        if (!(mg <= FLT_MAX)) mg = FLT_MAX;
       }
-      for (int r = 0; r < kCl; ++r) {
-        ChainShared* peer = cluster.map_shared_rank(&cs, r);
-        peer->tok = tok;
-        peer->st = st;
-      }
+      cp.margins[row] = mg;
     }
-    cluster.sync();
-    if (cs.st != DSPARK_ST_OK || cs.tok < 0) refused = (cs.st != DSPARK_ST_OK) ? cs.st
-                                                                               : DSPARK_ST_INTERNAL;
-    else prev = cs.tok;
+    if (st != DSPARK_ST_OK) refused = st;
+    else if (tok < 0) refused = DSPARK_ST_INTERNAL;
+    else prev = tok;
   }
 }
 

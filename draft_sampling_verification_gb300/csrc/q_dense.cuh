@@ -119,6 +119,7 @@ struct DShared {
   uint32_t draw;  // the row's 24-bit draft draw (fused draw only)
   uint32_t n_merged;  // many-member path: non-empty merged table slots
   float top1, top2;   // Markov chain rows: the row's two largest finite z
+  int chain_tok;      // Markov chain rows: the drawn token, stored by the drawing CTA
   float wt1[kWarps], wt2[kWarps];
 };
 constexpr int kAllCap = kBins * 4 / (int)sizeof(Cand);
@@ -422,11 +423,13 @@ __device__ void ordered_ranks(cg::cluster_group& cluster, DShared& sh, int ngrou
 // next, so its bulk copies then read L2).  A Markov chain row (chain true)
 // builds z = RN(x + bias) with the bias row zbias (fp32, element v at
 // zbias[v]; z = x when zbias is null), formed in shared memory as the slice
-// lands, and sh.top1 / sh.top2 get the row's two largest finite z.
-__device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& sh, float* sl,
-                                            uint64_t* mbar, uint32_t& phase, uint32_t* ready,
-                                            int next_row = -1, bool chain = false,
-                                            const float* zbias = nullptr) {
+// lands, and sh.top1 / sh.top2 get the row's two largest finite z; its
+// drawn token reaches every CTA's sh.chain_tok.  Returns the row's status,
+// the same in every CTA of the cluster.
+__device__ __forceinline__ int q_dense_row(const Params& p, int row, DShared& sh, float* sl,
+                                           uint64_t* mbar, uint32_t& phase, uint32_t* ready,
+                                           int next_row = -1, bool chain = false,
+                                           const float* zbias = nullptr) {
   cg::cluster_group cluster = cg::this_cluster();
   uint32_t* slu = reinterpret_cast<uint32_t*>(sl);
 
@@ -481,6 +484,12 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
       if (bytes) tma_load_bulk(sl + 4 * g0, xbase + 4 * g0, bytes, &mbar[c]);
     }
   }
+  if (zbias && tid == 64) {
+    // a chain row's bias part, into L2 for the loads of chunks 1 .. kTma-1
+    const uintptr_t a0 = (reinterpret_cast<uintptr_t>(zbias + lo) + 15u) & ~(uintptr_t)15u;
+    const uintptr_t a1 = reinterpret_cast<uintptr_t>(zbias + hi) & ~(uintptr_t)15u;
+    if (a1 > a0) l2_prefetch_bulk(reinterpret_cast<const void*>(a0), (uint32_t)(a1 - a0));
+  }
   if (tid == 32 && p.tokens) {
     // the draft draw, while the slice lands
     const int b = row / p.depth, j = row % p.depth;
@@ -525,24 +534,26 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
     }
     return make_float4(b[0], b[1], b[2], b[3]);
   };
-  constexpr int kBPre = 4;  // groups of a chunk per thread whose bias is loaded ahead
+  constexpr int kBPre = 4;  // groups of a chunk per thread whose bias is loaded together
   for (int c = 0; c < kTma; ++c) {
     int g0 = use_tma ? chunk_lo[c] : (c == 0 ? 0 : ngroups);
     int g1 = use_tma ? chunk_lo[c + 1] : ngroups;
     if (c == 0) g0 = 0;                 // the head edge group
     if (c == kTma - 1) g1 = ngroups;    // the tail edge group
+    if (use_tma) {
+      if (tid == 0 && !mbar_wait_bounded(&mbar[c], phase)) sh.timeout = 1;
+      __syncthreads();
+    }
+    // chain rows: the chunk's bias values, loaded together once the chunk
+    // has landed (from L2: the row's bias part was prefetched at its start).
+    // Loading them before the wait, or a chunk ahead, measured slower.
     float4 bpre[kBPre];
     if (zbias) {
-      // loaded before the wait for the chunk's copy, so the two overlap
 #pragma unroll
       for (int k = 0; k < kBPre; ++k) {
         const int g = g0 + tid + k * kThr;
         bpre[k] = (g < g1) ? bias4(g) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
       }
-    }
-    if (use_tma) {
-      if (tid == 0 && !mbar_wait_bounded(&mbar[c], phase)) sh.timeout = 1;
-      __syncthreads();
     }
     if (!chain) {
       for (int g = g0 + tid; g < g1; g += kThr) {
@@ -569,17 +580,13 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
           }
           reinterpret_cast<float4*>(sl)[g] = make_float4(z[0], z[1], z[2], z[3]);
         }
+        // the two largest z (with multiplicity); a row holding +inf or NaN
+        // is refused, and -inf changes neither
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           mx = fmax_nan(mx, z[i]);
-          if (z[i] > -INFINITY && z[i] < INFINITY) {
-            if (z[i] > zt1) {
-              zt2 = zt1;
-              zt1 = z[i];
-            } else {
-              zt2 = fmaxf(zt2, z[i]);
-            }
-          }
+          zt2 = fmaxf(zt2, fminf(zt1, z[i]));
+          zt1 = fmaxf(zt1, z[i]);
         }
       }
     }
@@ -617,6 +624,9 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
     }
   }
   cluster.sync();  // S1
+  // every thread of this CTA has read the previous row's token by now, and
+  // no peer stores this row's before S4
+  if (chain && tid == 64) sh.chain_tok = -1;
   if (chain && warp == 1 && lane == 0) {
     float c1 = -INFINITY, c2 = -INFINITY;
     for (int r = 0; r < kCl; ++r) top2_merge(c1, c2, sh.push.t1[r], sh.push.t2[r]);
@@ -659,7 +669,7 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
       __threadfence();
       atomicAdd(&ready[row / p.depth], 1u);
     }
-    return;
+    return st;
   }
   const float m = sh.m;
   if (next_row >= 0 && use_tma_dtype && tid == 0) {
@@ -753,7 +763,7 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
       __threadfence();
       atomicAdd(&ready[row / p.depth], 1u);
     }
-    return;
+    return st;
   }
   const uint64_t mk = sh.mk;
   const int ek = sh.ek;
@@ -1400,8 +1410,9 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
   }
   bool signal = ready && status != DSPARK_ST_OK && rank == 0 && tid == 0;
   // every remote read of this CTA's shared memory is done: arrive now, wait
-  // before leaving
-  cluster.barrier_arrive();
+  // before leaving.  A chain row arrives after the draw instead, whose token
+  // the drawing CTA stores into every CTA's sh.chain_tok first.
+  if (!chain) cluster.barrier_arrive();
 
   // ---- fused draft draw: the CTA whose range holds D finds the block of 32
   // groups holding it from the block sums, then the token inside it (warp 0)
@@ -1466,8 +1477,10 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
         if (DSPARK_CHECK(row < p.n_rows)) p.tokens[row] = token;
         signal = ready != nullptr;
       }
+      if (chain && lane < kCl) *cluster.map_shared_rank(&sh.chain_tok, lane) = token;
     }
   }
+  if (chain) cluster.barrier_arrive();
   cluster.barrier_wait();  // no CTA leaves while a peer may still read its shared memory
   if (signal && DSPARK_CHECK(row / p.depth < (p.n_rows + p.depth - 1) / p.depth)) {
     // every CTA's counts were written before its arrive, the token before
@@ -1475,6 +1488,7 @@ __device__ __forceinline__ void q_dense_row(const Params& p, int row, DShared& s
     __threadfence();
     atomicAdd(&ready[row / p.depth], 1u);
   }
+  return status;
 }
 
 }  // namespace
