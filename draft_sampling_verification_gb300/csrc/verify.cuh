@@ -62,7 +62,7 @@ struct VSh2 {
   VX px[2][kVMaxNC];
   uint64_t bsum[kVMaxBlocks];
   uint32_t qblk[32 * 8];  // final draw: a sparse q row's counts over one block of ids
-  float wm[8], ws[8], wam[8];
+  float wm[8], ws[8];
   int wai[8];
   uint64_t wz[8], wc[8];
   float M, S, AMV;
@@ -110,6 +110,18 @@ __device__ __forceinline__ Fix46 fix46(float r) {
 __device__ __forceinline__ uint64_t fix46_u64(Fix46 w) {
   return ((uint64_t)w.hi << 23) + w.lo;
 }
+// fix46 of two weights on the packed fp32x2 pipe, lane for lane the scalar
+// steps (-floor(a) is formed as 2^23 - t1, exactly), added to (hi, lo) as the
+// raw bits of t1 and t2: each element adds 0x4B000000 to both, which the
+// caller removes once per group (sums modulo 2^32, the true sums far below).
+__device__ __forceinline__ void fix46x2_add(float2 r, uint32_t& hi, uint32_t& lo) {
+  const float2 a = mul2_rn(r, f2(8388608.0f));
+  const float2 t1 = add2_rm(a, f2(8388608.0f));
+  const float2 f = add2_rn(a, fma2_rn(t1, f2(-1.0f), f2(8388608.0f)));
+  const float2 t2 = fma2_rm(f, f2(8388608.0f), f2(8388608.0f));
+  hi += __float_as_uint(t1.x) + __float_as_uint(t1.y);
+  lo += __float_as_uint(t2.x) + __float_as_uint(t2.y);
+}
 
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -128,6 +140,13 @@ struct OpMaxNaNv {
     return r;
   }
 };
+
+// max of two bf16 pairs, lane by lane; NaN when either lane is NaN
+__device__ __forceinline__ uint32_t bf16x2_max_nan(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
 
 struct OpAddF {
   __device__ float operator()(float a, float b) const { return __fadd_rn(a, b); }
@@ -337,63 +356,80 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
     }
     __syncthreads();
 
-    // ---- row statistics of this slice
-    float mx = -INFINITY, sm = 0.0f, amv = -INFINITY;
-    int ami = 0x7FFFFFFF;
+    // ---- row statistics of this slice.  Pass 1: the max, group by group
+    // (bf16 pairs by one packed max), and for the greedy argmax the group
+    // where each thread first met its own maximum.  Pass 2: the sum of exp
+    // relative to the CTA's max; the CTA's argmax is the lowest id holding
+    // that max, found in those groups.
+    const bool trk = kG && need_g;
+    float mx = -INFINITY, tmx = -INFINITY;
+    int tg = -1;
     for (int g = tid; g < ng; g += kVThreads) {
-      float z[EPG];
-      group(g, z);
-#pragma unroll
-      for (int i = 0; i < EPG; ++i) {
-        mx = OpMaxNaNv()(mx, z[i]);
-        if (kG && need_g && z[i] > amv) {
-          amv = z[i];
-          ami = lo - off + g * EPG + i;
+      float gm = -INFINITY;
+      if (DSPARK_CHECK(g < slice_groups)) {
+        if (kDt == DSPARK_F32) {
+          const float4 q = reinterpret_cast<const float4*>(vbuf)[g];
+          gm = OpMaxNaNv()(OpMaxNaNv()(q.x, q.y), OpMaxNaNv()(q.z, q.w));
+        } else {
+          const uint4 q = reinterpret_cast<const uint4*>(vbuf)[g];
+          const uint32_t m2 = bf16x2_max_nan(bf16x2_max_nan(q.x, q.y), bf16x2_max_nan(q.z, q.w));
+          gm = OpMaxNaNv()(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xFFFF0000u));
         }
       }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      mx = OpMaxNaNv()(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      if (kG && need_g) {
-        const float a2 = __shfl_xor_sync(0xffffffffu, amv, o);
-        const int i2 = __shfl_xor_sync(0xffffffffu, ami, o);
-        am_merge(amv, ami, a2, i2);
+      mx = OpMaxNaNv()(mx, gm);
+      if (trk && gm > tmx) {
+        tmx = gm;
+        tg = g;
       }
     }
-    if (lane == 0) {
-      sh.wm[warp] = mx;
-      sh.wam[warp] = amv;
-      sh.wai[warp] = ami;
-    }
+    mx = warp_reduce(mx, OpMaxNaNv());
+    if (lane == 0) sh.wm[warp] = mx;
     __syncthreads();
     float cm = sh.wm[0];  // the CTA's max
     for (int w = 1; w < kVThreads / 32; ++w) cm = OpMaxNaNv()(cm, sh.wm[w]);
-    if (kD && need_r) {
-      // the sum of exp relative to the CTA's max: a plain sum, each term by
-      // the hardware base-2 exponential (relative error a few 2^-23)
-      if (cm > -INFINITY && cm < INFINITY)
-        for (int g = tid; g < ng; g += kVThreads) {
-          float z[EPG];
-          group(g, z);
+    const bool cm_fin = cm > -INFINITY && cm < INFINITY;
+    int ami = 0x7FFFFFFF;
+    if (trk && cm_fin && tg >= 0 && tmx == cm) {
+      float z[EPG];
+      group(tg, z);
 #pragma unroll
-          for (int i = 0; i < EPG; ++i) sm += ex2_approx(__fmul_rn(__fsub_rn(z[i], cm), kLog2e));
-        }
-      sm = warp_reduce(sm, OpAddF());
-      if (lane == 0) sh.ws[warp] = sm;
-      __syncthreads();
+      for (int i = EPG - 1; i >= 0; --i)
+        if (z[i] == cm) ami = lo - off + tg * EPG + i;
     }
+    float sm = 0.0f;
+    if (kD && need_r && cm_fin) {
+      // each term by the hardware base-2 exponential (relative error a few
+      // 2^-23) of RN(RN(z - cm) log2 e), pairs of arguments on the packed
+      // pipe, the terms added in element order
+      for (int g = tid; g < ng; g += kVThreads) {
+        float z[EPG];
+        group(g, z);
+#pragma unroll
+        for (int i = 0; i < EPG; i += 2) {
+          const float2 t = mul2_rn(add2_rn(make_float2(z[i], z[i + 1]), f2(-cm)), f2(kLog2e));
+          sm += ex2_approx(t.x);
+          sm += ex2_approx(t.y);
+        }
+      }
+    }
+    if (kD && need_r) sm = warp_reduce(sm, OpAddF());
+    if (trk) ami = __reduce_min_sync(0xffffffffu, ami);
+    if (lane == 0) {
+      sh.ws[warp] = sm;
+      sh.wai[warp] = ami;
+    }
+    __syncthreads();
     if (tid == 0) {
-      float m = cm, s = 0.0f, av = sh.wam[0];
-      int ai = sh.wai[0];
+      float s = 0.0f;
+      int ai = 0x7FFFFFFF;
       for (int w = 0; w < kVThreads / 32; ++w) {
         if (kD && need_r) s += sh.ws[w];
-        if (kG && need_g && w > 0) am_merge(av, ai, sh.wam[w], sh.wai[w]);
+        if (trk) ai = min(ai, sh.wai[w]);
       }
       VX& e = sh.x[xi];
-      e.m = m;
+      e.m = cm;
       e.s = s;
-      e.amv = av;
+      e.amv = (ai != 0x7FFFFFFF) ? cm : -INFINITY;
       e.ami = ai;
       e.fl = sh.timeout ? 1u : 0u;
     }
@@ -564,17 +600,25 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
         if (g < ng) {
           float z[EPG];
           group(g, z);
+          // pairs on the packed fp32x2 pipe: p as pv, max(p - c 2^-24, 0)
+          // (c 2^-24 is exact, so one fma), the fixed-point weight as fix46
+          uint32_t gc = 0;
 #pragma unroll
-          for (int i = 0; i < EPG; ++i) {
-            float r = pv(z[i]);
+          for (int i = 0; i < EPG; i += 2) {
+            const float2 t = fma2_rn(add2_rn(make_float2(z[i], z[i + 1]), f2(-M)), f2(kLog2e),
+                                     f2(nlgS));
+            float2 r = make_float2(ex2_approx(t.x), ex2_approx(t.y));
             if (dense_q) {
-              cs += qv[i];
-              r = fmaxf(__fsub_rn(r, (float)qv[i] * 0x1p-24f), 0.0f);
+              gc += qv[i] + qv[i + 1];
+              r = fma2_rn(make_float2((float)qv[i], (float)qv[i + 1]), f2(-0x1p-24f), r);
+              r.x = fmaxf(r.x, 0.0f);
+              r.y = fmaxf(r.y, 0.0f);
             }
-            const Fix46 w = fix46(r);
-            ghi += w.hi;
-            glo += w.lo;
+            fix46x2_add(r, ghi, glo);
           }
+          ghi -= (uint32_t)EPG * 0x4B000000u;
+          glo -= (uint32_t)EPG * 0x4B000000u;
+          cs += gc;
         }
         // one block = the 32 groups of one warp in one iteration: each half
         // is at most 32 * EPG * 2^23 <= 2^31, summed by the 32-bit warp
