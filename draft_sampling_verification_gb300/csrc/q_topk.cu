@@ -117,15 +117,52 @@ __device__ __forceinline__ float key_float(uint32_t k) {
 // entries) of val(i) over the entries i < n with take(i).  *above gets the
 // number of taken entries with a larger value, *equal the number equal to
 // it.  Called by every thread (n uniform); it starts with a __syncthreads()
-// and its result is uniform.  The lanes of a warp that fall in one bin add
-// to it with a single atomic: candidate values share their high bits, so
-// plain per-lane atomics would serialise on a few bins.
+// and its result is uniform.
+// The bytes above the highest bit where the taken values' min and max differ
+// are common to all of them, so the 8-bit digit passes start at the byte
+// holding that bit.  In a pass, the lanes of a warp that fall in one bin add
+// to it with a single atomic (candidate values share their high bits, so
+// plain per-lane atomics would serialise on a few bins).  Once the selected
+// bin holds at most 32 values, they are gathered and one warp finishes.
 template <typename Val, typename Take>
 __device__ uint32_t select_desc(int n, uint32_t r, Val val, Take take, KShared& sh,
                                 uint32_t* above, uint32_t* equal) {
-  const int lane = threadIdx.x & 31;
-  uint32_t prefix = 0, mask = 0, above_acc = 0, eq = 0;
-  for (int shift = 24; shift >= 0; shift -= 8) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __syncthreads();
+  uint32_t vmin = 0xFFFFFFFFu, vmax = 0u, cnt = 0u;
+  for (int i = (int)threadIdx.x; i < n; i += kKThr)
+    if (take(i)) {
+      const uint32_t v = val(i);
+      vmin = min(vmin, v);
+      vmax = max(vmax, v);
+      ++cnt;
+    }
+  vmin = __reduce_min_sync(0xffffffffu, vmin);
+  vmax = __reduce_max_sync(0xffffffffu, vmax);
+  cnt = __reduce_add_sync(0xffffffffu, cnt);
+  if (lane == 0) {
+    sh.red32[warp] = vmin;
+    sh.red32[kKWarps + warp] = vmax;
+    sh.red32[2 * kKWarps + warp] = cnt;
+  }
+  __syncthreads();
+  vmin = 0xFFFFFFFFu;
+  vmax = 0u;
+  cnt = 0u;
+  for (int w = 0; w < kKWarps; ++w) {
+    vmin = min(vmin, sh.red32[w]);
+    vmax = max(vmax, sh.red32[kKWarps + w]);
+    cnt += sh.red32[2 * kKWarps + w];
+  }
+  if (vmin >= vmax) {  // every taken value is the same
+    *above = 0u;
+    *equal = cnt;
+    return vmin;
+  }
+  int shift = (31 - __clz(vmin ^ vmax)) & ~7;
+  uint32_t mask = (shift == 24) ? 0u : ~((1u << (shift + 8)) - 1u);
+  uint32_t prefix = vmin & mask, above_acc = 0, eq = cnt;
+  for (; shift >= 0; shift -= 8) {
     __syncthreads();
     sh.hist[threadIdx.x] = 0u;  // kKThr == 256 bins
     __syncthreads();
@@ -143,19 +180,19 @@ __device__ uint32_t select_desc(int n, uint32_t r, Val val, Take take, KShared& 
     __syncthreads();
     if (threadIdx.x < 32) {
       // lane l scans bins 255 - 8l down to 248 - 8l
-      uint32_t c[8], s = 0;
+      uint32_t c[8], sacc = 0;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         c[j] = sh.hist[255 - 8 * lane - j];
-        s += c[j];
+        sacc += c[j];
       }
-      uint32_t incl = s;
+      uint32_t incl = sacc;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += t;
       }
-      const uint32_t excl = incl - s;
+      const uint32_t excl = incl - sacc;
       if (excl < r && r <= incl) {
         uint32_t acc = excl;
 #pragma unroll
@@ -176,6 +213,40 @@ __device__ uint32_t select_desc(int n, uint32_t r, Val val, Take take, KShared& 
     above_acc += ab;
     prefix |= d << shift;
     mask |= 255u << shift;
+    if (shift > 0 && eq <= 32u) {
+      // the selected bin's values, gathered; warp 0 takes the r-th largest
+      if (threadIdx.x == 0) sh.n_tmp = 0u;
+      __syncthreads();
+      for (int i = (int)threadIdx.x; i < n; i += kKThr)
+        if (take(i)) {
+          const uint32_t v = val(i);
+          if ((v & mask) == prefix) {
+            const uint32_t j = atomicAdd(&sh.n_tmp, 1u);
+            if (DSPARK_CHECK(j < 32u)) sh.hist[j] = v;
+          }
+        }
+      __syncthreads();
+      if (warp == 0) {
+        const uint32_t v = (lane < (int)eq) ? sh.hist[lane] : 0u;
+        uint32_t gt = 0, ge = 0;
+        for (int m = 0; m < (int)eq; ++m) {
+          const uint32_t u = __shfl_sync(0xffffffffu, v, m);
+          gt += (u > v) ? 1u : 0u;
+          ge += (u >= v) ? 1u : 0u;
+        }
+        const bool hit = lane < (int)eq && gt < r && r <= ge;
+        const unsigned msk = __ballot_sync(0xffffffffu, hit);
+        if (msk != 0u && lane == __ffs(msk) - 1) {
+          sh.sel_digit = v;
+          sh.sel_above = gt;
+          sh.sel_equal = ge - gt;
+        }
+      }
+      __syncthreads();
+      *above = above_acc + sh.sel_above;
+      *equal = sh.sel_equal;
+      return sh.sel_digit;
+    }
   }
   *above = above_acc;
   *equal = eq;
