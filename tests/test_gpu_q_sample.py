@@ -102,6 +102,43 @@ def test_q_topk_stream_orders(oracle, top_k, dtype):
     compare_q(q, oracle.q_build(xr, [1.0, 1.0, 0.7, 1.3, 1.0], top_k))
 
 
+@pytest.mark.parametrize("V", [4099, 129280])
+@pytest.mark.parametrize("top_k", [2, 7, 256, 1000, 1024])
+def test_q_topk_allocation_edges(oracle, V, top_k):
+    """Supports that steer the allocation's selects and its id ordering:
+    equal logits (every remainder equal, the grants go to the lowest ids;
+    with k a power of two every remainder is zero and nothing is granted),
+    two tied groups, support ids packed at the start of the row with one at
+    its end (one id bucket holds nearly all of them), ties at the support's
+    cut, and a single finite value."""
+    if top_k > V:
+        pytest.skip("top_k > V")
+    rng = np.random.default_rng(V + top_k)
+    rows = []
+    r = np.full(V, -np.inf, np.float32)
+    pos = rng.choice(V, size=min(V, top_k + 3), replace=False)
+    r[pos] = 1.0                                        # k + 3 equal logits
+    rows.append(r)
+    r = np.full(V, -np.inf, np.float32)
+    pos = rng.choice(V, size=min(V, top_k + 5), replace=False)
+    r[pos[: len(pos) // 2]] = 2.0                       # two tied groups
+    r[pos[len(pos) // 2:]] = 1.0
+    rows.append(r)
+    r = rng.normal(-40, 1, V).astype(np.float32)
+    r[: top_k - 1] = rng.normal(3, 1, top_k - 1)        # ids 0 .. k-2 and V-1
+    r[V - 1] = 2.5
+    rows.append(r)
+    r = np.round(rng.normal(0, 1, V) * 2).astype(np.float32) / 2   # ties at the cut
+    rows.append(r)
+    r = np.full(V, -np.inf, np.float32)
+    r[rng.integers(V)] = 0.5                            # one finite value
+    rows.append(r)
+    x = np.stack(rows)
+    temps = np.array([1.0, 0.7, 1.0, 1.3, 1.0], np.float32)
+    q, _ = run_q(x, temps, top_k)
+    compare_q(q, oracle.q_build(x, temps, top_k))
+
+
 def test_q_topk_batch_invariance():
     rng = np.random.default_rng(19)
     V = 129280
