@@ -91,6 +91,8 @@ struct TpShared {
   float rf[32];
   uint32_t hist[kTpBins];
   int found;
+  int gs_bstar;     // grant_state: the threshold bin and the tickets inside it
+  uint32_t gs_rin;
 };
 
 struct OpMaxNaNTp {
@@ -285,9 +287,11 @@ __global__ void __launch_bounds__(kTpThr) tp_floors_kernel(TpParams p) {
 }
 
 // The threshold bin and the tickets granted inside it, from every rank's
-// partials (each rank computes the same values).
-__device__ __forceinline__ int grant_state(const TpParams& p, const TpRow& w, int st,
-                                           uint32_t* R, int* bstar, uint32_t* Rin) {
+// partials (each rank computes the same values).  Every thread of the block
+// calls it: the ranks' histograms are added into sh.hist, and a scan over the
+// bins from the top (eight per thread) finds the bin holding the R-th ticket.
+__device__ int grant_state(const TpParams& p, const TpRow& w, int st, TpShared& sh,
+                           uint32_t* R, int* bstar, uint32_t* Rin) {
   *R = 0;
   *bstar = -1;
   *Rin = 0;
@@ -300,17 +304,51 @@ __device__ __forceinline__ int grant_state(const TpParams& p, const TpRow& w, in
   if (F == 0 || F > (uint64_t)kM || (uint64_t)kM - F > npos) return DSPARK_ST_ALLOC_INCONSISTENT;
   *R = (uint32_t)((uint64_t)kM - F);
   if (*R == 0) return st;
-  uint32_t above = 0;
-  for (int b = kTpBins - 1; b >= 0; --b) {
+  static_assert(kTpBins == 8 * kTpThr, "eight bins per thread");
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  __syncthreads();  // earlier readers of sh.hist are done
+  for (int b = t; b < kTpBins; b += kTpThr) {
     uint32_t c = 0;
     for (int s = 0; s < p.n_sh; ++s) c += w.hist[s][b];
-    if (above + c >= *R) {
-      *bstar = b;
-      *Rin = *R - above;
-      break;
-    }
-    above += c;
+    sh.hist[b] = c;
   }
+  if (t == 0) {
+    sh.gs_bstar = -1;
+    sh.gs_rin = 0u;
+  }
+  __syncthreads();
+  // thread t holds bins kTpBins - 8t - 1 down to kTpBins - 8t - 8
+  const int bt = kTpBins - 8 * t - 1;
+  uint32_t c[8], tot = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    c[j] = sh.hist[bt - j];
+    tot += c[j];
+  }
+  uint32_t incl = tot;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  if (lane == 31) sh.r32[warp] = incl;
+  __syncthreads();
+  for (int w2 = 0; w2 < warp; ++w2) incl += sh.r32[w2];
+  const uint32_t excl = incl - tot, r = *R;
+  if (excl < r && r <= incl) {
+    uint32_t acc = excl;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (acc < r && r <= acc + c[j]) {
+        sh.gs_bstar = bt - j;
+        sh.gs_rin = r - acc;
+      }
+      acc += c[j];
+    }
+  }
+  __syncthreads();
+  *bstar = sh.gs_bstar;
+  *Rin = sh.gs_rin;
   return st;
 }
 
@@ -344,6 +382,7 @@ __device__ __forceinline__ bool grant_one(const TpParams& p, const Shard& d, int
 }
 
 __global__ void __launch_bounds__(kTpThr) tp_grant_kernel(TpParams p) {
+  __shared__ TpShared sh;
   const Shard d = shard_of(p);
   TpRow& w = p.ws[d.row];
   bool badT;
@@ -352,7 +391,7 @@ __global__ void __launch_bounds__(kTpThr) tp_grant_kernel(TpParams p) {
   int st = row_state(p, w, badT, &m);
   uint32_t R, Rin;
   int bstar;
-  st = grant_state(p, w, st, &R, &bstar, &Rin);
+  st = grant_state(p, w, st, sh, &R, &bstar, &Rin);
   if (st != DSPARK_ST_OK || R == 0) return;
   uint64_t S = 0;
   for (int s = 0; s < p.n_sh; ++s) S += w.S[s];
@@ -394,7 +433,7 @@ __global__ void __launch_bounds__(kTpThr) tp_threshold_kernel(TpParams p) {
   int st = row_state(p, w, badT, &m);
   uint32_t R, Rin;
   int bstar;
-  st = grant_state(p, w, st, &R, &bstar, &Rin);
+  st = grant_state(p, w, st, sh, &R, &bstar, &Rin);
   bool over = false;
   for (int s = 0; s < p.n_sh; ++s) over |= w.over[s] != 0u;
   if (st == DSPARK_ST_OK && R > 0 && over) st = DSPARK_ST_INTERNAL;
