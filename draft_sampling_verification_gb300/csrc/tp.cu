@@ -511,12 +511,19 @@ __global__ void __launch_bounds__(kTpThr) tp_threshold_kernel(TpParams p) {
 }
 
 // Each rank grants its marked members above T, and its quota of members at
-// T to its lowest ids (an id-ordered block scan), and sums its counts.
+// T to its lowest ids, and sums its counts.  The members at T are listed as
+// they are met and ranked by id afterwards; more of them than the list holds
+// (long exact ties) are granted by an id-ordered block scan instead.
+constexpr int kTpAtCap = 1024;
 __global__ void __launch_bounds__(kTpThr) tp_ties_kernel(TpParams p) {
   __shared__ TpShared sh;
+  __shared__ int32_t at_ids[kTpAtCap];
+  __shared__ uint32_t n_at;
   const Shard d = shard_of(p);
   TpRow& w = p.ws[d.row];
   uint64_t C = 0;
+  if (threadIdx.x == 0) n_at = 0u;
+  __syncthreads();
   if (w.st == DSPARK_ST_OK) {
     bool badT;
     const float invT = inv_temp(p, d.row, &badT);
@@ -528,27 +535,55 @@ __global__ void __launch_bounds__(kTpThr) tp_ties_kernel(TpParams p) {
     const uint64_t T = w.T;
     const uint32_t quota = w.quota[d.s];
     uint32_t* crow = p.counts + (int64_t)d.row * p.V;
-    uint32_t base = 0;  // members at T in this shard with a lower id
-    for (int v0 = d.lo; v0 < d.hi; v0 += kTpThr) {
-      const int v = v0 + threadIdx.x;
-      uint32_t c = v < d.hi ? crow[v] : 0u;
-      const bool marked = (c & kTpMark) != 0u;
-      uint32_t at = 0;
-      if (marked) {
+    for (int v = d.lo + (int)threadIdx.x; v < d.hi; v += kTpThr) {
+      uint32_t c = crow[v];
+      if ((c & kTpMark) != 0u) {
         c &= ~kTpMark;
         const uint64_t key = frac_key(split_of(y_of(p, d.row, v, invT), m, k.mk, k.ek));
-        if (key > T) c += 1u;
-        else if (key == T) at = 1u;
+        if (key > T) {
+          c += 1u;
+        } else if (key == T && quota > 0u) {
+          const uint32_t j = atomicAdd(&n_at, 1u);
+          if (j < (uint32_t)kTpAtCap) at_ids[j] = v;
+        }
+        crow[v] = c;
       }
-      if (quota > 0u && __syncthreads_or(at)) {  // uniform over the block
-        uint32_t tot;
-        const uint32_t incl = block_inclusive_scan(at, sh.r32, &tot);
-        if (at && base + incl - 1u < quota) c += 1u;
-        base += tot;
-        __syncthreads();
-      }
-      if (marked) crow[v] = c;
       C += c;
+    }
+    __syncthreads();
+    const uint32_t na = n_at;
+    if (na <= (uint32_t)kTpAtCap) {
+      // the quota's lowest ids among the listed members
+      for (uint32_t i = threadIdx.x; i < na; i += kTpThr) {
+        const int32_t vi = at_ids[i];
+        uint32_t rank = 0;
+        for (uint32_t j = 0; j < na; ++j) rank += (at_ids[j] < vi) ? 1u : 0u;
+        if (rank < quota) {
+          crow[vi] += 1u;
+          C += 1u;
+        }
+      }
+    } else {
+      // every member at T again, in id order (their counts are unmarked now)
+      uint32_t base = 0;
+      for (int v0 = d.lo; v0 < d.hi; v0 += kTpThr) {
+        const int v = v0 + (int)threadIdx.x;
+        uint32_t at = 0;
+        if (v < d.hi) {
+          const AllocSplit a = split_of(y_of(p, d.row, v, invT), m, k.mk, k.ek);
+          at = (a.rnum != 0ull && frac_key(a) == T) ? 1u : 0u;
+        }
+        if (__syncthreads_or(at)) {  // uniform over the block
+          uint32_t tot;
+          const uint32_t incl = block_inclusive_scan(at, sh.r32, &tot);
+          if (at && base + incl - 1u < quota) {
+            crow[v] += 1u;
+            C += 1u;
+          }
+          base += tot;
+          __syncthreads();
+        }
+      }
     }
   }
   C = block_reduce(C, OpAddU64(), sh.r64);
@@ -568,18 +603,26 @@ __global__ void __launch_bounds__(kTpThr) tp_draw_kernel(TpParams p) {
   const uint32_t req = p.request_ids ? p.request_ids[b] : (uint32_t)b;
   const uint64_t D = draw_u32(p.seed, req, (uint32_t)j, DSPARK_PURPOSE_PROPOSAL) >> 8;
   if (!(D >= before && D - before < w.C[d.s])) return;
-  const uint64_t t = D - before;
-  // block scan over the shard, 256 ids at a time
-  uint64_t base = 0;
-  for (int v0 = d.lo; v0 < d.hi; v0 += kTpThr) {
-    const int v = v0 + threadIdx.x;
-    const uint32_t c = v < d.hi ? p.counts[(int64_t)d.row * p.V + v] : 0u;
-    uint32_t tot;
-    const uint32_t incl = block_inclusive_scan(c, sh.r32, &tot);
-    if (c > 0u && base + incl > t && base + incl - c <= t) p.tokens[d.row] = v;
-    base += tot;
-    __syncthreads();
-    if (base > t) break;
+  const uint32_t t = (uint32_t)(D - before);  // < the shard's total <= 2^24
+  // each thread sums a contiguous run of the shard; one block scan finds the
+  // run holding t, and its thread walks it
+  const uint32_t* crow = p.counts + (int64_t)d.row * p.V;
+  const int L = (d.hi - d.lo + kTpThr - 1) / kTpThr;
+  const int a0 = min(d.hi, d.lo + (int)threadIdx.x * L), a1 = min(d.hi, a0 + L);
+  uint32_t mine = 0;
+  for (int v = a0; v < a1; ++v) mine += crow[v];
+  uint32_t tot;
+  const uint32_t incl = block_inclusive_scan(mine, sh.r32, &tot);
+  const uint32_t excl = incl - mine;
+  if (mine > 0u && excl <= t && t < incl) {
+    uint32_t cum = excl;
+    for (int v = a0; v < a1; ++v) {
+      cum += crow[v];
+      if (t < cum) {
+        p.tokens[d.row] = v;
+        break;
+      }
+    }
   }
 }
 
