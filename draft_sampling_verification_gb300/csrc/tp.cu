@@ -401,7 +401,9 @@ __global__ void __launch_bounds__(kTpThr) tp_grant_kernel(TpParams p) {
     uint64_t key = kTpEmpty;
     const bool member = v < d.hi && grant_one(p, d, v, invT, m, k, bstar, &key);
     // count the members' fractions in the shard's table (open addressing),
-    // one atomic per distinct fraction in the warp
+    // one atomic per distinct fraction in the warp (members are rare: most
+    // warps skip the match)
+    if (!__any_sync(0xffffffffu, member)) continue;
     const unsigned grp = __match_any_sync(0xffffffffu, member ? key : kTpEmpty);
     if (member && (int)(threadIdx.x & 31u) == __ffs(grp) - 1) {
       uint32_t h = (uint32_t)((key * 0x9E3779B97F4A7C15ull) >> 54) & (kTpTab - 1);
