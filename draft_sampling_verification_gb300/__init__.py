@@ -27,7 +27,8 @@ SCHEDULE_AUTO, SCHEDULE_ONE_LAUNCH, SCHEDULE_SEPARATE = 0, 1, 2
 PURPOSE_PROPOSAL, PURPOSE_ACCEPT, PURPOSE_RESIDUAL, PURPOSE_BONUS, PURPOSE_MATCH = 0, 1, 2, 3, 4
 
 __all__ = ["dspark_q_build", "dspark_q_build_sample", "dspark_draft_sample", "dspark_verify_greedy",
-           "dspark_verify_ratio", "dspark_verify", "dspark_target_probs", "dspark_spec_step",
+           "dspark_verify_ratio", "dspark_verify", "dspark_verify_stats", "verify_stats",
+           "dspark_target_probs", "dspark_spec_step",
            "dspark_spec_step_schedule", "dspark_spec_step_noalloc", "dspark_q_pack",
            "dspark_q_validate", "dspark_verify_match", "verify_match", "dspark_q_chain_sample",
            "q_chain_sample", "dspark_q_build_sample_sharded", "dspark_q_sharded_workspace_bytes",
@@ -279,6 +280,11 @@ def dspark_q_validate(q, sparse_ids, nnz, top_k, V, tokens, expect, counts_out, 
           _i32(tokens), _ptr(expect), _i32(counts_out), _i32(row_status), _stream(stream))
 
 
+def dspark_verify_stats(flags, stats, stream=None):
+    """flags: int32 / uint32 [B] (device); stats: int32 [3] (device)."""
+    _call("dspark_verify_stats", _ptr(flags), int(flags.numel()), _ptr(stats), _stream(stream))
+
+
 def dspark_target_probs(target_logits, p_out, argmax, row_status, stream=None):
     rows, V, ld = _rows(target_logits)
     _call("dspark_target_probs", _ptr(target_logits), _dtype_code(target_logits), ld, rows, V,
@@ -468,6 +474,15 @@ def verify_ratio(target_logits, drafts, q, seed, request_ids=None, stream=None):
     dspark_verify_ratio(target_logits, B, depth, drafts, q["counts"], q["ids"], q["nnz"],
                         q["top_k"], seed, request_ids, acc, com, fl, st, stream)
     return acc, com, fl, st
+
+
+def verify_stats(flags, stream=None):
+    """Counts of the requests with each DSPARK_FLAG_* bit in flags [B]: a
+    tensor [3] (ambiguous decisions, draws near a boundary, degenerate
+    residuals)."""
+    stats = _empty((3,), torch.int32, flags.device)
+    dspark_verify_stats(flags, stats, stream)
+    return stats
 
 
 def target_probs(target_logits, want_p=True, stream=None):

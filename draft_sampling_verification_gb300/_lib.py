@@ -27,6 +27,7 @@ SIGNATURES = {
     "dspark_verify_ratio": [_P, _I32, _I64, _I32, _I32, _I32, _P, _P, _P, _P, _I32, _U64, _P,
                             _P, _P, _P, _P, _P],
     "dspark_target_probs": [_P, _I32, _I64, _I32, _I32, _P, _P, _P, _P],
+    "dspark_verify_stats": [_P, _I32, _P, _P],
     "dspark_verify": [_P, _I32, _I64, _I32, _I32, _I32, _P, _P, _P, _P, _I32, _U64, _P, _P, _P,
                       _P, _P, _P, _P, _P, _P],
     "dspark_spec_step_schedule": [_I32, _I32],

@@ -63,6 +63,8 @@ cudaError_t launch_spec_step(const void* xd, int d_dtype, int64_t ld_d, const vo
                              int32_t* row_status, int32_t* g_acc, int32_t* g_com, int32_t* g_st,
                              int32_t* r_acc, int32_t* r_com, uint32_t* r_flags, int32_t* r_st,
                              uint32_t* workspace, int schedule, cudaStream_t stream);
+cudaError_t launch_verify_stats(const uint32_t* flags, int B, uint32_t* stats,
+                                cudaStream_t stream);
 cudaError_t launch_target_probs(const void* z, int dtype, int64_t ld, int n_rows, int V,
                                 float* p_out, int32_t* argmax, int32_t* status,
                                 cudaStream_t stream);
@@ -600,6 +602,15 @@ int dspark_q_validate(const float* q, const int32_t* sparse_ids, const int32_t* 
   return launch_result(dspark::launch_q_validate(
       q, top_k > 0 ? sparse_ids : nullptr, top_k > 0 ? nnz : nullptr, top_k, n_rows, V, tokens,
       expect, counts_out, row_status, static_cast<cudaStream_t>(stream)));
+}
+
+int dspark_verify_stats(const uint32_t* flags, int32_t B, uint32_t* stats, void* stream) {
+  const NvtxRange nvtx_range("dspark_verify_stats");
+  if (B < 0 || B > kMaxGridRows) return DSPARK_ERR_SIZE;
+  if (!stats || (B > 0 && !flags)) return DSPARK_ERR_NULL;
+  if (!aligned(stats, 4) || (flags && !aligned(flags, 4))) return DSPARK_ERR_ALIGN;
+  return launch_result(
+      dspark::launch_verify_stats(flags, B, stats, static_cast<cudaStream_t>(stream)));
 }
 
 int dspark_target_probs(const void* target_logits, int32_t dtype, int64_t ld, int32_t n_rows,

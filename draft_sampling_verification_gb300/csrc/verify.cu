@@ -391,6 +391,38 @@ cudaError_t launch_target_probs(const void* z, int dtype, int64_t ld, int n_rows
   return cudaGetLastError();
 }
 
+// The verifier's optional statistics from its per-request flags: one CTA
+// counts, for each DSPARK_FLAG_* bit k (ambiguous decision, draw near a
+// boundary, degenerate residual), the requests carrying it into stats[k].
+__global__ void __launch_bounds__(256) verify_stats_kernel(const uint32_t* flags, int B,
+                                                           uint32_t* stats) {
+  __shared__ uint32_t part[3][8];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t c[3] = {0u, 0u, 0u};
+  for (int b = threadIdx.x; b < B; b += 256) {
+    const uint32_t f = flags[b];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) c[k] += (f >> k) & 1u;
+  }
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    c[k] = __reduce_add_sync(0xffffffffu, c[k]);
+    if (lane == 0) part[k][warp] = c[k];
+  }
+  __syncthreads();
+  if (threadIdx.x < 3) {
+    uint32_t t = 0;
+    for (int w = 0; w < 8; ++w) t += part[threadIdx.x][w];
+    stats[threadIdx.x] = t;
+  }
+}
+
+cudaError_t launch_verify_stats(const uint32_t* flags, int B, uint32_t* stats,
+                                cudaStream_t stream) {
+  verify_stats_kernel<<<1, 256, 0, stream>>>(flags, B, stats);
+  return cudaGetLastError();
+}
+
 DSPARK_CHECK_COLLECTOR(verify)
 
 }  // namespace dspark

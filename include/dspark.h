@@ -387,6 +387,23 @@ int dspark_spec_step_host(const void* h_draft_logits, int32_t draft_dtype,
                           int32_t schedule, void* stream);
 
 /*
+ * dspark_verify_stats -- the verifier's optional statistics, counted from the
+ * per-request flags[B] that dspark_verify_ratio, dspark_verify_match,
+ * dspark_verify and the whole-step entries write (the numerical-tolerance
+ * cases that "PP1 q transport and scheduling design", Distribution contract
+ * and precision, asks to be qualified and counted):
+ *   stats[0]  requests with DSPARK_FLAG_AMBIG_ACCEPT (an ambiguous decision),
+ *   stats[1]  requests with DSPARK_FLAG_NEAR_BOUNDARY (a draw near a
+ *             cumulative boundary),
+ *   stats[2]  requests with DSPARK_FLAG_DEGENERATE (a zero residual mass).
+ * flags: device uint32[B] (may be NULL when B == 0); stats: device
+ * uint32[3], overwritten on the stream (zeros for B == 0).  One kernel of one
+ * block.  Errors: DSPARK_ERR_SIZE for B < 0 or too large, DSPARK_ERR_NULL,
+ * DSPARK_ERR_ALIGN (4-byte alignment); nothing is launched then.
+ */
+int dspark_verify_stats(const uint32_t* flags, int32_t B, uint32_t* stats, void* stream);
+
+/*
  * dspark_target_probs -- the target distribution p of n_rows logit rows at
  * T = 1 ("PP1 q transport and scheduling design": the full target p after
  * the unchanged target processors, T = 1, top_p = 1), with the argmax

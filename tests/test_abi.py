@@ -60,6 +60,10 @@ def test_sample_and_verify_argument_errors(lib):
     assert lib.dspark_verify_ratio(P, 0, 8, 1, 5, 8, P, P, None, None, 4, 0, None, P, P,
                                    None, P, None) == -1
     assert lib.dspark_target_probs(P, 0, 8, 1, 0, None, None, P, None) == -2
+    assert lib.dspark_verify_stats(P, -1, P, None) == -2               # B < 0
+    assert lib.dspark_verify_stats(P, 4, None, None) == -1             # no stats
+    assert lib.dspark_verify_stats(None, 4, P, None) == -1             # no flags, B > 0
+    assert lib.dspark_verify_stats(ctypes.c_void_p(18), 4, P, None) == -5
     assert lib.dspark_debug_philox(P, 0, -1, P, None) == -2
     assert lib.dspark_debug_exp_weights(None, 4, None, None, None) == -1
 

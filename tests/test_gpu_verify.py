@@ -54,6 +54,11 @@ def run_workload(oracle, wl):
         else:
             g = ds.verify_ratio(t, tok, q, wl.seed, req)
         torch.cuda.synchronize()
+        if mode == "ratio":
+            # the optional statistics: the requests carrying each flag bit
+            fl = np_(g[2]).view(np.uint32)
+            stats = np_(ds.verify_stats(g[2]))
+            assert [int(x) for x in stats] == [int(((fl >> k) & 1).sum()) for k in range(3)]
         ref = oracle_verify(wl, mode, drafts, qref)
         c = compare_verify(g, ref, mode)
         out[mode] = c
@@ -91,6 +96,19 @@ def test_sweep_variants(oracle, variant, top_k, B):
         tok, _ = ds.draft_sample(q, wl.B, wl.depth, wl.V, wl.seed, req)
         acc, _, _, _ = ds.verify_ratio(t, tok, q, wl.seed, req)
         assert np.all(np_(acc) == 0)
+
+
+def test_verify_stats_counts_flag_bits():
+    """dspark_verify_stats on hand-made flags: an empty batch gives zeros,
+    and every bit is counted over a batch longer than the block."""
+    empty = torch.zeros(0, dtype=torch.int32, device="cuda")
+    assert np_(ds.verify_stats(empty)).tolist() == [0, 0, 0]
+    small = torch.tensor([7, 1, 2, 4, 0, 3], dtype=torch.int32, device="cuda")
+    assert np_(ds.verify_stats(small)).tolist() == [3, 3, 2]
+    rng = np.random.default_rng(5)
+    fl = rng.integers(0, 8, 5003).astype(np.int32)
+    got = np_(ds.verify_stats(torch.from_numpy(fl).cuda())).tolist()
+    assert got == [int(((fl >> k) & 1).sum()) for k in range(3)]
 
 
 @pytest.mark.parametrize("V", [1, 2, 7, 257, 4099])
