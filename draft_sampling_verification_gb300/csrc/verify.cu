@@ -14,6 +14,8 @@
 // the first rejection are never read.  The correction / bonus draw re-reads
 // row L (an L2 hit) and scans exact 46-bit fixed-point residual weights.
 #define DSPARK_TU 9  // this file's number in the checked build's site codes
+#include <mutex>
+
 #include "verify.cuh"
 
 namespace dspark {
@@ -187,16 +189,13 @@ __device__ RowStat slice_stat(const void* row, int dtype, int lo, int n, VShared
 //
 // Cluster size: bf16 rows take 4-CTA clusters (a 64 KB slice per CTA, three
 // CTAs per SM), so twice as many requests walk their row chains at once as
-// with 8-CTA clusters; fp32 rows keep 8 (a 64 KB slice as well).
-template <int kDt>
-constexpr int verify_cluster() {
-  return kDt == DSPARK_BF16 ? 4 : 8;
-}
-
-template <bool kG, bool kR, int kDt, bool kMatch = false>
-__global__ void __cluster_dims__(verify_cluster<kDt>(), 1, 1) __launch_bounds__(kVThreads, 3)
+// with 8-CTA clusters.  fp32 rows take 8 (a 64 KB slice as well), or 7 (a
+// 72 KB slice, still three CTAs per SM) when the batch does not fit the GPU
+// at once with 8: one more request in eight is resident, at a slice an
+// eighth longer.
+template <bool kG, bool kR, int kDt, bool kMatch, int NC>
+__global__ void __cluster_dims__(NC, 1, 1) __launch_bounds__(kVThreads, 3)
     verify_kernel(VParams p) {
-  constexpr int NC = verify_cluster<kDt>();
   __shared__ VSh2 sh;
   __shared__ uint64_t mbar[kVTma];
   extern __shared__ __align__(128) unsigned char vbuf[];
@@ -262,6 +261,76 @@ static int verify_chunk(int V, int nc) {
   return (c + 7) & ~7;
 }
 
+// Clusters of a verify kernel resident at once for a dynamic shared size,
+// per device and cluster size (queried once).
+template <typename K>
+int verify_wave(K kern, int nc, int smem) {
+  static std::mutex mu;
+  static int cached[64][9][2];  // [device][cluster size] {smem, clusters}
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || nc < 1 || nc > 8) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[dev][nc][0] == smem && cached[dev][nc][1] > 0) return cached[dev][nc][1];
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+          cudaSuccess ||
+      cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(nc * 64);
+  cfg.blockDim = dim3(kVThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = nc;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, (void*)kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cached[dev][nc][0] = smem;
+  cached[dev][nc][1] = n;
+  return n;
+}
+
+// Launches verify_kernel<kG, kR, kDt, kMatch, NC> for the p.B requests:
+// bf16 rows on 4-CTA clusters; fp32 rows on 8, or on 7 when the batch does
+// not fit at once on 8-CTA clusters and more 7-CTA clusters do.
+template <bool kG, bool kR, int kDt, bool kMatch>
+cudaError_t launch_verify_kernel(VParams p, cudaStream_t stream) {
+  constexpr int esz = (kDt == DSPARK_F32) ? 4 : 2;
+  auto go = [&](auto kern, int nc) -> cudaError_t {
+    p.chunk = verify_chunk(p.V, nc);
+    // the slice buffer: chunk elements plus one 16-byte group of slack
+    const int smem = p.chunk * esz + 32;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    kern<<<p.B * nc, kVThreads, smem, stream>>>(p);
+    return cudaGetLastError();
+  };
+  if constexpr (kDt == DSPARK_BF16) {
+    return go(verify_kernel<kG, kR, kDt, kMatch, 4>, 4);
+  } else {
+    const int w8 = verify_wave(verify_kernel<kG, kR, kDt, kMatch, 8>, 8,
+                               verify_chunk(p.V, 8) * esz + 32);
+    if (w8 > 0 && p.B > w8) {
+      const int w7 = verify_wave(verify_kernel<kG, kR, kDt, kMatch, 7>, 7,
+                                 verify_chunk(p.V, 7) * esz + 32);
+      if (w7 > w8) return go(verify_kernel<kG, kR, kDt, kMatch, 7>, 7);
+    }
+    return go(verify_kernel<kG, kR, kDt, kMatch, 8>, 8);
+  }
+}
+
 cudaError_t launch_verify_modes(const void* z, int dtype, int64_t ld, int B, int depth, int V,
                                 const int32_t* drafts, const uint32_t* counts, const int32_t* ids,
                                 const int32_t* nnz, int top_k, uint64_t seed,
@@ -289,30 +358,15 @@ cudaError_t launch_verify_modes(const void* z, int dtype, int64_t ld, int B, int
   p.r_committed = r_com;
   p.r_flags = r_flags;
   p.r_status = r_st;
-  const int nc = (dtype == DSPARK_BF16) ? verify_cluster<DSPARK_BF16>()
-                                        : verify_cluster<DSPARK_F32>();
-  p.chunk = verify_chunk(V, nc);
-  // the slice buffer: chunk elements plus one 16-byte group of slack
-  const int esz = (dtype == DSPARK_F32) ? 4 : 2;
-  const int smem = p.chunk * esz + 32;
-  auto go = [&](auto kern) -> cudaError_t {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
-    kern<<<B * nc, kVThreads, smem, stream>>>(p);
-    return cudaGetLastError();
-  };
   const bool g = g_acc != nullptr, r = r_acc != nullptr;
   if (dtype == DSPARK_F32) {
-    if (g && r) return go(verify_kernel<true, true, DSPARK_F32>);
-    if (g) return go(verify_kernel<true, false, DSPARK_F32>);
-    return go(verify_kernel<false, true, DSPARK_F32>);
+    if (g && r) return launch_verify_kernel<true, true, DSPARK_F32, false>(p, stream);
+    if (g) return launch_verify_kernel<true, false, DSPARK_F32, false>(p, stream);
+    return launch_verify_kernel<false, true, DSPARK_F32, false>(p, stream);
   }
-  if (g && r) return go(verify_kernel<true, true, DSPARK_BF16>);
-  if (g) return go(verify_kernel<true, false, DSPARK_BF16>);
-  return go(verify_kernel<false, true, DSPARK_BF16>);
+  if (g && r) return launch_verify_kernel<true, true, DSPARK_BF16, false>(p, stream);
+  if (g) return launch_verify_kernel<true, false, DSPARK_BF16, false>(p, stream);
+  return launch_verify_kernel<false, true, DSPARK_BF16, false>(p, stream);
 }
 
 // The match mode: its outputs take the ratio mode's slots.
@@ -342,22 +396,8 @@ cudaError_t launch_verify_match(const void* z, int dtype, int64_t ld, int B, int
   p.r_committed = committed;
   p.r_flags = flags;
   p.r_status = status;
-  const int nc = (dtype == DSPARK_BF16) ? verify_cluster<DSPARK_BF16>()
-                                        : verify_cluster<DSPARK_F32>();
-  p.chunk = verify_chunk(V, nc);
-  const int esz = (dtype == DSPARK_F32) ? 4 : 2;
-  const int smem = p.chunk * esz + 32;
-  auto go = [&](auto kern) -> cudaError_t {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
-    kern<<<B * nc, kVThreads, smem, stream>>>(p);
-    return cudaGetLastError();
-  };
-  return dtype == DSPARK_F32 ? go(verify_kernel<false, false, DSPARK_F32, true>)
-                             : go(verify_kernel<false, false, DSPARK_BF16, true>);
+  return dtype == DSPARK_F32 ? launch_verify_kernel<false, false, DSPARK_F32, true>(p, stream)
+                             : launch_verify_kernel<false, false, DSPARK_BF16, true>(p, stream);
 }
 
 cudaError_t launch_verify(int mode, const void* z, int dtype, int64_t ld, int B, int depth, int V,

@@ -60,8 +60,12 @@ struct VSh2 {
   // every CTA's partials, pushed here by each CTA before the cluster barrier
   // ([buffer][writer's rank]), so that after it the merge reads local memory
   VX px[2][kVMaxNC];
-  uint64_t bsum[kVMaxBlocks];
-  uint32_t qblk[32 * 8];  // final draw: a sparse q row's counts over one block of ids
+  union {
+    uint64_t bsum[kVMaxBlocks];  // final draw: the mass of each block of 32 groups
+    // then, in the drawing CTA's token search once its block is found: a
+    // sparse q row's counts over that block's ids
+    uint32_t qblk[32 * 8];
+  };
   float wm[8], ws[8];
   int wai[8];
   uint64_t wz[8], wc[8];
