@@ -187,14 +187,15 @@ __device__ RowStat slice_stat(const void* row, int dtype, int lo, int n, VShared
 // mass of every block of 32 groups, and the CTA holding the draw finds its
 // block from those sums and its token with one warp.
 //
-// Cluster size: bf16 rows take 4-CTA clusters (a 64 KB slice per CTA, three
-// CTAs per SM), so twice as many requests walk their row chains at once as
-// with 8-CTA clusters.  fp32 rows take 8 (a 64 KB slice as well), or 7 (a
-// 72 KB slice, still three CTAs per SM) when the batch does not fit the GPU
-// at once with 8: one more request in eight is resident, at a slice an
-// eighth longer.
+// Cluster size: bf16 rows take 5-CTA clusters (a 51 KB slice per CTA, four
+// CTAs per SM within 64 registers), so more requests walk their row chains
+// at once, each on shorter slices, than with 4 or 8 CTAs at three per SM.
+// fp32 rows take 8 (a 64 KB slice, three CTAs per SM), or 7 (a 72 KB slice,
+// still three per SM) when the batch does not fit the GPU at once with 8:
+// one more request in eight is resident, at a slice an eighth longer.
 template <bool kG, bool kR, int kDt, bool kMatch, int NC>
-__global__ void __cluster_dims__(NC, 1, 1) __launch_bounds__(kVThreads, 3)
+__global__ void __cluster_dims__(NC, 1, 1)
+    __launch_bounds__(kVThreads, (kDt == DSPARK_BF16) ? 4 : 3)
     verify_kernel(VParams p) {
   __shared__ VSh2 sh;
   __shared__ uint64_t mbar[kVTma];
@@ -300,7 +301,7 @@ int verify_wave(K kern, int nc, int smem) {
 }
 
 // Launches verify_kernel<kG, kR, kDt, kMatch, NC> for the p.B requests:
-// bf16 rows on 4-CTA clusters; fp32 rows on 8, or on 7 when the batch does
+// bf16 rows on 5-CTA clusters; fp32 rows on 8, or on 7 when the batch does
 // not fit at once on 8-CTA clusters and more 7-CTA clusters do.
 template <bool kG, bool kR, int kDt, bool kMatch>
 cudaError_t launch_verify_kernel(VParams p, cudaStream_t stream) {
@@ -318,7 +319,7 @@ cudaError_t launch_verify_kernel(VParams p, cudaStream_t stream) {
     return cudaGetLastError();
   };
   if constexpr (kDt == DSPARK_BF16) {
-    return go(verify_kernel<kG, kR, kDt, kMatch, 4>, 4);
+    return go(verify_kernel<kG, kR, kDt, kMatch, 5>, 5);
   } else {
     const int w8 = verify_wave(verify_kernel<kG, kR, kDt, kMatch, 8>, 8,
                                verify_chunk(p.V, 8) * esz + 32);
