@@ -230,6 +230,7 @@ __device__ __forceinline__ void verify_request(const VParams& p, int b, VSh2& sh
 
   // the slice buffer holds chunk elements plus one 16-byte group of slack
   const int slice_groups = (p.chunk * ESZ + 32) / 16;
+  (void)slice_groups;  // read by the checked build's bounds only
   auto val = [&](int s) -> float {
     if (!DSPARK_CHECK(s >= 0 && s < slice_groups * EPG)) return -INFINITY;
     if (kDt == DSPARK_F32) return vf[s];
